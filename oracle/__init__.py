@@ -1,0 +1,172 @@
+"""Float64 CPU oracle of the sparse-delta-memory forward hot path (Phase 1 + DW).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg may import this package. It shares no code with the CUDA path and never
+imports it. The arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight loops); this
+module builds it with the host C compiler on first use and marshals numpy arrays.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
+definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
+Python's ``sorted``, rex/cpe closed forms, flag invariants).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdm_oracle.c")
+_lib = None
+
+
+def build(src: str = _SRC, out_dir: str = None) -> str:
+    """Compile sdm_oracle.c into oracle/_build/ (cached by source hash); returns the .so path."""
+    with open(src, "rb") as f:
+        tag = hashlib.sha1(f.read()).hexdigest()[:12]
+    out_dir = out_dir or os.path.join(_HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, f"libsdm_oracle_{tag}.so")
+    if not os.path.exists(so):
+        tmp = so + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-o", tmp, src, "-lm"])
+        os.replace(tmp, so)
+    return so
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.sdm_oracle_phase1.restype = ctypes.c_int
+    lib.sdm_oracle_phase1.argtypes = [i64, i32, i32, i32, i64, i32, i32, i64] + [P] * 26
+    lib.sdm_oracle_dw_chunk.restype = ctypes.c_int
+    lib.sdm_oracle_dw_chunk.argtypes = ([i32, i32, i32, i32, i32, i64, i32] + [P] * 10 +
+                                        [i32, i32, i32, i32, f64])
+    return lib
+
+
+def load_variant(so_path: str):
+    """Load another build of the oracle (the pin tests use this to check that planted
+    mistakes in the C source are caught)."""
+    return _bind(ctypes.CDLL(so_path))
+
+
+def _load(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        _lib = _bind(lib)
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Decode an input array (float32, or bfloat16 stored as uint16 bits) exactly to float64."""
+    if dtype == "bf16":
+        return (np.ascontiguousarray(x, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.ascontiguousarray(x, np.float32).astype(np.float64)
+
+
+def phase1(k_idx, q_idx, k_val, q_val, g, *, S, val_dtype, first_partial=None, valid_last=None,
+           pairs=True, lib=None):
+    """Phase 1 of every chunk in the arrays (chunk-major [n, C, W] / [n, C, R], g [n, C] or [n, C, W]).
+
+    Returns a dict of float64 / integer arrays in the output layouts of the method, plus
+    ``gabs_k`` / ``gabs_q`` (sum of |gate| over each entry's group) and ``A_abs`` / ``QK_abs``
+    (sum of |term| per cell) for tolerances.
+    """
+    lib = _load(lib)
+    n, C, W = k_idx.shape
+    R = q_idx.shape[2]
+    g_per_entry = 1 if g.ndim == 3 else 0
+    if valid_last is None:
+        valid_last = C
+    if first_partial is None:
+        first_partial = n
+    k_idx = np.ascontiguousarray(k_idx, np.int32)
+    q_idx = np.ascontiguousarray(q_idx, np.int32)
+    kv, qv = as_f64(k_val, val_dtype), as_f64(q_val, val_dtype)
+    gg = np.ascontiguousarray(g, np.float32).astype(np.float64)
+    o = {
+        "log_k": np.zeros((n, C, W)), "rex": np.zeros((n, C, W)), "cpe": np.zeros((n, C, W)),
+        "k_eff": np.zeros((n, C, W)), "is_last": np.zeros((n, C, W), np.int8),
+        "is_only": np.zeros((n, C, W), np.int8), "pos_k": np.zeros((n, C, W), np.int32),
+        "gabs_k": np.zeros((n, C, W)),
+        "log_q": np.zeros((n, C, R)), "q_w": np.zeros((n, C, R)), "pos_q": np.zeros((n, C, R), np.int32),
+        "q_last": np.zeros((n, C, R), np.int8), "q_only": np.zeros((n, C, R), np.int8),
+        "gabs_q": np.zeros((n, C, R)),
+        "sorted_k": np.zeros((n, C * W), np.int32), "sorted_q": np.zeros((n, C * R), np.int32),
+    }
+    if pairs:
+        for k in ("A", "QK", "A_abs", "QK_abs"):
+            o[k] = np.zeros((n, C, C))
+    reps = np.zeros(1, np.int64)
+    st = lib.sdm_oracle_phase1(
+        n, C, W, R, first_partial, valid_last, g_per_entry, S, _ptr(k_idx), _ptr(q_idx), _ptr(kv),
+        _ptr(qv), _ptr(gg), _ptr(o["log_k"]), _ptr(o["rex"]), _ptr(o["cpe"]), _ptr(o["k_eff"]),
+        _ptr(o["is_last"]), _ptr(o["is_only"]), _ptr(o["pos_k"]), _ptr(o["gabs_k"]),
+        _ptr(o["log_q"]), _ptr(o["q_w"]), _ptr(o["pos_q"]), _ptr(o["q_last"]), _ptr(o["q_only"]),
+        _ptr(o["gabs_q"]), _ptr(o["sorted_k"]), _ptr(o["sorted_q"]), _ptr(o.get("A")),
+        _ptr(o.get("QK")), _ptr(o.get("A_abs")), _ptr(o.get("QK_abs")), _ptr(reps))
+    if st != 0:
+        raise ValueError("oracle: a valid slot id is outside [0, S)")
+    o["repeats"] = int(reps[0])
+    return o
+
+
+def dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, *, S, V, val_dtype, bank_dtype,
+             round_cpe=True, round_bank=True, alt=None, amb=None, touched=None, amb_rel=2.0 ** -17,
+             lib=None):
+    """Decay-and-write of one chunk ([C, W] / [C, R] inputs, dv [C, hd] float64) into ``bank``
+    ([S, hd] float64, in place). See sdm_oracle_dw_chunk for ``alt`` / ``amb`` / ``touched``."""
+    lib = _load(lib)
+    C, W = k_idx.shape
+    R = q_idx.shape[1]
+    hd = bank.shape[1]
+    assert bank.dtype == np.float64 and bank.flags.c_contiguous and bank.shape[0] == S
+    g_per_entry = 1 if np.ndim(g) == 2 else 0
+    k_idx = np.ascontiguousarray(k_idx, np.int32)
+    q_idx = np.ascontiguousarray(q_idx, np.int32)
+    kv, qv = as_f64(k_val, val_dtype), as_f64(q_val, val_dtype)
+    gg = np.ascontiguousarray(g, np.float32).astype(np.float64)
+    dvv = np.ascontiguousarray(dv, np.float64)
+    st = lib.sdm_oracle_dw_chunk(C, W, R, V, g_per_entry, S, hd, _ptr(k_idx), _ptr(q_idx), _ptr(kv),
+                                 _ptr(qv), _ptr(gg), _ptr(dvv), _ptr(bank), _ptr(alt), _ptr(amb),
+                                 _ptr(touched), int(round_cpe), int(val_dtype == "bf16"),
+                                 int(round_bank), int(bank_dtype == "bf16"), float(amb_rel))
+    if st != 0:
+        raise ValueError("oracle: a valid slot id is outside [0, S)")
+
+
+def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, dv_dtype, bank_dtype,
+              step_begin=0, step_end=None, round_cpe=True, round_bank=True, track=False):
+    """DW of every step in [step_begin, step_end) of one stream, in step order.
+
+    ``inputs`` holds chunk-major arrays of P streams (as synth.make_inputs returns); ``p_local`` is
+    the stream's index among them. ``bank`` is that stream's [S, hd] float64 rows (updated in place).
+    With ``track`` returns (alt, amb, touched) for tolerance bookkeeping.
+    """
+    step_end = steps if step_end is None else step_end
+    hd = bank.shape[1]
+    alt = bank.copy() if track else None
+    amb = np.zeros(S, np.int32) if track else None
+    touched = np.zeros(S, np.int32) if track else None
+    for ti in range(step_begin, step_end):
+        c = ti * P + p_local
+        V = valid_last if ti == steps - 1 else C
+        dv = as_f64(inputs["dv"][c * C:(c + 1) * C], dv_dtype).reshape(C, hd)
+        dw_chunk(bank, inputs["k_idx"][c], inputs["q_idx"][c], inputs["k_val"][c], inputs["q_val"][c],
+                 inputs["g"][c], dv, S=S, V=V, val_dtype=val_dtype, bank_dtype=bank_dtype,
+                 round_cpe=round_cpe, round_bank=round_bank, alt=alt, amb=amb, touched=touched)
+    if track:
+        return alt, amb, touched
+    return None

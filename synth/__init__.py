@@ -1,0 +1,15 @@
+"""Seeded synthetic inputs for the sparse-delta-memory forward (Phase 1 + decay-and-write).
+
+This package is shared by the tests, the benchmark and the oracle's callers. It only draws
+random numbers and lays them out; it holds none of the method's arithmetic.
+"""
+
+from .workloads import (  # noqa: F401
+    WORKLOADS,
+    Workload,
+    bf16_bits_to_f32,
+    f32_to_bf16_bits,
+    make_bank_stream,
+    make_inputs,
+    scaled,
+)

@@ -1,0 +1,419 @@
+"""Pins of the float64 oracle against definitions other than its own code.
+
+* A hand-worked chunk (tests/golden/hand_chunk.json), derived on paper from the definitions of
+  sparse-delta-memory 2.0.0 (phase1_cuda.py module docstring, p1_keys_zw_kernel, p1_scan_kernel,
+  the p1_pairs_kernel comment; DW from the mover_da2_cuda.py / mover_fx_cuda.py docstrings).
+* Sort positions, group peers, the position pack and the sorted-row elements against Python's
+  ``sorted`` and direct counting over all entries.
+* log_k / log_q / rex / cpe against the token form: G_s(t) = sum of the gates of the tokens
+  t' <= t that write slot s, each token once (phase1_cuda.py docstring: log-cumsum of the gates,
+  rex = gates of the later writes, cpe = exp(total gate of the slot)).
+* A and QK against a brute force over all lane pairs, O(C^2 W^2).
+* DW against the token-sequential recurrence: token by token, decay each slot the token writes
+  once by exp(g_t), then add k * dv_t per write lane. The chunk form is the same in exact
+  arithmetic; a single write gives base * exp(g) + k * dv.
+* Rounding to bfloat16 against a neighbour search.
+* Planted mistakes in the oracle's C source fail these pins.
+"""
+
+import json
+import math
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import WORKLOADS, f32_to_bf16_bits, make_inputs, scaled
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ---------------------------------------------------------------- brute-force definitions
+
+def bf_sorted(k_idx, q_idx, V):
+    """Sorted order of one chunk: entries e = t*(W+R)+j keyed by (slot, e); invalid last."""
+    C, W = k_idx.shape
+    R = q_idx.shape[1]
+    ents = []
+    for t in range(C):
+        for j in range(W + R):
+            q = j >= W
+            a = j - W if q else j
+            slot = int(q_idx[t, a] if q else k_idx[t, a])
+            valid = t < V
+            ents.append(dict(e=t * (W + R) + j, t=t, a=a, q=q, slot=slot, valid=valid))
+    order = sorted(ents, key=lambda d: ((0, d["slot"]) if d["valid"] else (1, 0), d["e"]))
+    return order
+
+
+def bf_peers(order, d):
+    """(before, after): valid entries of the same kind and slot before / after d in sorted order."""
+    if not d["valid"]:
+        return 0, 0
+    r = order.index(d)
+    same = [i for i, x in enumerate(order) if x["valid"] and x["slot"] == d["slot"] and x["q"] == d["q"]]
+    return sum(1 for i in same if i < r), sum(1 for i in same if i > r)
+
+
+def token_G(k_idx, g, V):
+    """G[s][t] = sum of g over tokens t' <= t (t' < V) that write slot s (each token once)."""
+    C, W = k_idx.shape
+    G = {}
+    for s in set(int(x) for x in k_idx[:V].ravel()):
+        run, col = 0.0, []
+        for t in range(C):
+            if t < V and s in set(int(x) for x in k_idx[t]):
+                run += float(g[t])
+            col.append(run)
+        G[s] = col
+    return G
+
+
+def Gs(G, s, t):
+    return G[s][t] if s in G else 0.0
+
+
+def random_chunk(rng, C, W, R, S, V):
+    k_idx = rng.integers(0, S, size=(C, W)).astype(np.int32)
+    q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
+    k_idx[V:] = -1
+    q_idx[V:] = -1
+    k_val = rng.standard_normal((C, W)).astype(np.float32)
+    q_val = rng.standard_normal((C, R)).astype(np.float32)
+    z = rng.standard_normal(C) + 1.0
+    g = (np.minimum(z, 0) - np.log1p(np.exp(-np.abs(z)))).astype(np.float32)
+    return k_idx, q_idx, k_val, q_val, g
+
+
+CASES = [  # (C, W, R, S, V): small S gives collisions and repeated slots within a token
+    (8, 3, 2, 5, 8), (8, 3, 2, 5, 6), (6, 4, 4, 3, 6), (10, 2, 3, 7, 4), (5, 1, 1, 2, 5), (7, 5, 1, 4, 7),
+]
+
+
+def run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V, lib=None):
+    return oracle.phase1(k_idx[None], q_idx[None], k_val[None], q_val[None], g[None], S=S,
+                         val_dtype="f32", first_partial=0, valid_last=V, lib=lib)
+
+
+# ---------------------------------------------------------------- pins
+
+def test_hand_chunk_golden():
+    fx = json.load(open(os.path.join(HERE, "golden", "hand_chunk.json")))
+    ev = lambda s: eval(s, {"exp": math.exp})  # noqa: E731  (expressions written in the fixture)
+    k_idx = np.array(fx["k_idx"], np.int32)
+    q_idx = np.array(fx["q_idx"], np.int32)
+    k_val = np.array(fx["k_val"], np.float32)
+    q_val = np.array(fx["q_val"], np.float32)
+    g = np.array(fx["g"], np.float32)
+    o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, fx["S"], fx["V"])
+    for f in ("log_k", "rex", "cpe", "k_eff", "log_q", "q_w", "A", "QK"):
+        want = np.array([[ev(x) for x in row] for row in fx[f]])
+        np.testing.assert_allclose(o[f][0], want, rtol=1e-12, atol=1e-12, err_msg=f)
+    for f in ("is_last", "is_only", "pos_k", "pos_q", "q_last", "q_only"):
+        np.testing.assert_array_equal(o[f][0], np.array(fx[f]), err_msg=f)
+    assert o["repeats"] == fx["repeats"]
+    np.testing.assert_array_equal(o["sorted_k"][0].view(np.uint32), [int(h, 16) for h in fx["sorted_k_hex"]])
+    np.testing.assert_array_equal(o["sorted_q"][0].view(np.uint32), [int(h, 16) for h in fx["sorted_q_hex"]])
+    bank = np.array(fx["bank_in"], np.float64)
+    oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, np.array(fx["dv"], np.float64), S=fx["S"],
+                    V=fx["V"], val_dtype="f32", bank_dtype="f32", round_cpe=False, round_bank=False)
+    want = np.array([[ev(x) for x in row] for row in fx["bank_out"]])
+    np.testing.assert_allclose(bank, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_sort_positions_and_rows_bruteforce(case):
+    C, W, R, S, V = case
+    rng = np.random.default_rng(hash(case) % 2**32)
+    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+    o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V)
+    order = bf_sorted(k_idx, q_idx, V)
+    sk, sq = [], []
+    for r, d in enumerate(order):
+        b, a = bf_peers(order, d)
+        if d["valid"]:
+            asat = min(a, 127)
+            want = r | asat << 17 | min(b + 1 + asat, 127) << 24
+        else:
+            want = r
+        got = o["pos_q" if d["q"] else "pos_k"][0, d["t"], d["a"]]
+        assert got == want, (d, got, want)
+        last, only = (a == 0 and d["valid"]), (a == 0 and b == 0 and d["valid"])
+        if d["q"]:
+            assert o["q_last"][0, d["t"], d["a"]] == last and o["q_only"][0, d["t"], d["a"]] == only
+        else:
+            assert o["is_last"][0, d["t"], d["a"]] == last and o["is_only"][0, d["t"], d["a"]] == only
+        el = d["t"] << 9 | int(d["q"]) << 8 | d["a"] | (0 if d["valid"] else 0x20000)
+        if d["valid"]:
+            el |= min(b, 4095) << 18 | (1 << 31 if b == 0 else 0) | (1 << 30 if a == 0 else 0)
+        else:
+            el |= 3 << 30
+        (sq if d["q"] else sk).append(el)
+    np.testing.assert_array_equal(o["sorted_k"][0].view(np.uint32), np.array(sk, np.uint64).astype(np.uint32))
+    np.testing.assert_array_equal(o["sorted_q"][0].view(np.uint32), np.array(sq, np.uint64).astype(np.uint32))
+    # repeated write entries: a token's write lanes beyond the first on one slot
+    reps = sum(len(k_idx[t]) - len(set(k_idx[t].tolist())) for t in range(V))
+    assert o["repeats"] == reps
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_logs_rex_cpe_token_form(case):
+    C, W, R, S, V = case
+    rng = np.random.default_rng(1 + hash(case) % 2**32)
+    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+    o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V)
+    G = token_G(k_idx, g, V)
+    for t in range(C):
+        for a in range(W):
+            s = int(k_idx[t, a])
+            if t >= V:
+                assert o["log_k"][0, t, a] == 0 and o["rex"][0, t, a] == 0 and o["cpe"][0, t, a] == 1
+                assert o["k_eff"][0, t, a] == 0
+                continue
+            tot = G[s][C - 1]
+            assert o["log_k"][0, t, a] == pytest.approx(G[s][t], abs=1e-12)
+            assert o["rex"][0, t, a] == pytest.approx(tot - G[s][t], abs=1e-12)
+            assert o["cpe"][0, t, a] == pytest.approx(math.exp(tot), rel=1e-12)
+            assert o["k_eff"][0, t, a] == pytest.approx(float(k_val[t, a]) * math.exp(G[s][t]), rel=1e-12)
+            if o["is_last"][0, t, a]:
+                assert o["rex"][0, t, a] == 0.0
+        for a in range(R):
+            s = int(q_idx[t, a])
+            if t >= V:
+                assert o["log_q"][0, t, a] == 0 and o["q_w"][0, t, a] == 0
+                continue
+            assert o["log_q"][0, t, a] == pytest.approx(Gs(G, s, t), abs=1e-12)
+            assert o["q_w"][0, t, a] == pytest.approx(float(q_val[t, a]) * math.exp(Gs(G, s, t)), rel=1e-12)
+
+
+def bf_pairs(k_idx, q_idx, k_val, q_val, g, V):
+    C, W = k_idx.shape
+    R = q_idx.shape[1]
+    G = token_G(k_idx, g, V)
+    A = np.zeros((C, C))
+    QK = np.zeros((C, C))
+    for i in range(V):
+        for j in range(V):
+            for b in range(W):
+                s = int(k_idx[j, b])
+                if j < i:
+                    for a in range(W):
+                        if int(k_idx[i, a]) == s:
+                            A[i, j] += float(k_val[i, a]) * float(k_val[j, b]) * math.exp(G[s][i] - G[s][j])
+                if j <= i:
+                    for a in range(R):
+                        if int(q_idx[i, a]) == s:
+                            QK[i, j] += float(q_val[i, a]) * float(k_val[j, b]) * math.exp(G[s][i] - G[s][j])
+    return A, QK
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_pairs_bruteforce(case):
+    C, W, R, S, V = case
+    rng = np.random.default_rng(2 + hash(case) % 2**32)
+    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+    o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V)
+    A, QK = bf_pairs(k_idx, q_idx, k_val, q_val, g, V)
+    np.testing.assert_allclose(o["A"][0], A, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o["QK"][0], QK, rtol=1e-12, atol=1e-12)
+    assert np.all(np.triu(o["A"][0]) == 0) and np.all(np.triu(o["QK"][0], 1) == 0)
+
+
+def token_recurrence(bank, k_idx, k_val, g, dv, V):
+    for t in range(V):
+        for s in set(int(x) for x in k_idx[t]):
+            bank[s] *= math.exp(float(g[t]))
+        for a in range(k_idx.shape[1]):
+            bank[int(k_idx[t, a])] += float(k_val[t, a]) * dv[t]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_dw_token_recurrence(case):
+    C, W, R, S, V = case
+    hd = 4
+    rng = np.random.default_rng(3 + hash(case) % 2**32)
+    bank = rng.standard_normal((S, hd))
+    want = bank.copy()
+    for step in range(3):   # a stream of three chunks, the last one ragged when V < C
+        Vs = V if step == 2 else C
+        k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, Vs)
+        dv = rng.standard_normal((C, hd)).astype(np.float32).astype(np.float64)
+        oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=Vs, val_dtype="f32",
+                        bank_dtype="f32", round_cpe=False, round_bank=False)
+        token_recurrence(want, k_idx, k_val, g, dv, Vs)
+    np.testing.assert_allclose(bank, want, rtol=1e-11, atol=1e-11)
+
+
+def test_dw_single_entry_closed_form():
+    C, W, R, S, hd = 4, 2, 1, 64, 3
+    k_idx = np.array([[10, 11], [12, 13], [14, 15], [16, 17]], np.int32)
+    q_idx = np.array([[10], [20], [21], [22]], np.int32)
+    k_val = np.array([[0.5, -1.5], [2.0, 0.25], [1.0, 1.0], [-3.0, 0.125]], np.float32)
+    q_val = np.ones((C, R), np.float32)
+    g = np.array([-0.1, -0.7, -2.0, -0.3], np.float32)
+    dv = np.arange(C * hd, dtype=np.float64).reshape(C, hd) - 5.0
+    base = np.random.default_rng(5).standard_normal((S, hd))
+    bank = base.copy()
+    oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=C, val_dtype="f32", bank_dtype="f32",
+                    round_cpe=False, round_bank=False)
+    for t in range(C):
+        for a in range(W):
+            s = k_idx[t, a]
+            want = base[s] * math.exp(float(g[t])) + float(k_val[t, a]) * dv[t]
+            np.testing.assert_allclose(bank[s], want, rtol=1e-13)
+    untouched = np.setdiff1d(np.arange(S), k_idx.ravel())
+    np.testing.assert_array_equal(bank[untouched], base[untouched])
+
+
+def nearest_bf16(x):
+    """Nearest bfloat16 of a float64 by a neighbour search (ties to the even pattern)."""
+    f = np.float32(x)
+    b = int(f32_to_bf16_bits(np.array([f]))[0])
+    cands = [(c & 0xFFFF) for c in (b - 1, b, b + 1)]
+    vals = [float((np.array([c], np.uint32) << 16).view(np.float32)[0]) for c in cands]
+    best = min(range(3), key=lambda i: (abs(vals[i] - x), cands[i] & 1))
+    return vals[best]
+
+
+def test_bank_rounding_bf16():
+    """Singleton groups on a zero base store round(k * dv) exactly (rex = 0)."""
+    rng = np.random.default_rng(9)
+    C, W, R, S, hd = 16, 1, 1, 64, 8
+    k_idx = np.arange(C, dtype=np.int32).reshape(C, 1)
+    q_idx = np.full((C, 1), 40, np.int32)
+    k_val = rng.standard_normal((C, 1)).astype(np.float32)
+    q_val = np.ones((C, 1), np.float32)
+    g = np.full(C, -0.5, np.float32)
+    dv = rng.standard_normal((C, hd)) * 3.0
+    bank = np.zeros((S, hd))
+    oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=C, val_dtype="f32", bank_dtype="bf16",
+                    round_cpe=True, round_bank=True)
+    for t in range(C):
+        for i in range(hd):
+            x = float(k_val[t, 0]) * dv[t, i]
+            assert bank[t, i] == nearest_bf16(x)
+
+
+def test_cpe_rounding_feeds_dw():
+    """DW uses cpe as stored in the value type (bf16): base * round(exp(G)) enters the sum."""
+    C, W, R, S, hd = 2, 1, 1, 8, 2
+    k_idx = np.array([[3], [3]], np.int32)
+    q_idx = np.array([[0], [0]], np.int32)
+    k_val = np.zeros((C, 1), np.float32)
+    q_val = np.zeros((C, 1), np.float32)
+    g = np.array([-0.3, -0.45], np.float32)
+    dv = np.zeros((C, hd))
+    bank = np.zeros((S, hd))
+    bank[3] = [1.0, -2.0]
+    oracle.dw_chunk(bank, k_idx, q_idx, f32_to_bf16_bits(k_val), f32_to_bf16_bits(q_val), g, dv, S=S, V=C,
+                    val_dtype="bf16", bank_dtype="f32", round_cpe=True, round_bank=False)
+    cp = nearest_bf16(math.exp(float(g[0]) + float(g[1])))
+    np.testing.assert_array_equal(bank[3], [cp, -2.0 * cp])
+
+
+def test_flag_invariants_zipf():
+    w = scaled(WORKLOADS["zipf_c256"], P=1, T=512)
+    x = make_inputs(w)
+    o = oracle.phase1(x["k_idx"], x["q_idx"], x["k_val"], x["q_val"], x["g"], S=w.S, val_dtype=w.val_dtype,
+                      pairs=False)
+    for c in range(x["k_idx"].shape[0]):
+        ki = x["k_idx"][c]
+        for s in np.unique(ki):
+            m = ki == s
+            assert o["is_last"][c][m].sum() == 1
+            assert o["is_only"][c][m].sum() == (1 if m.sum() == 1 else 0)
+        assert np.all(o["is_last"][c] >= o["is_only"][c])
+        pk = o["pos_k"][c].view(np.uint32)
+        after, size = (pk >> 17) & 127, (pk >> 24) & 127
+        assert np.all(size >= np.minimum(after + 1, 127))   # both saturate at 127
+        # positions are a permutation of the sorted row
+        r = np.concatenate([pk.ravel() & 0x1FFFF, o["pos_q"][c].view(np.uint32).ravel() & 0x1FFFF])
+        assert np.array_equal(np.sort(r), np.arange(r.size))
+
+
+def test_ragged_tail_invalid_entries():
+    w = scaled(WORKLOADS["wide_ragged"], P=2, T=200, C=64, hd=8)
+    x = make_inputs(w)
+    assert w.valid_last == 200 - 3 * 64
+    fp = (w.steps - 1) * w.P
+    o = oracle.phase1(x["k_idx"], x["q_idx"], x["k_val"], x["q_val"], x["g"], S=w.S, val_dtype=w.val_dtype,
+                      first_partial=fp, valid_last=w.valid_last, pairs=True)
+    V, C, W, R = w.valid_last, w.C, w.W, w.R
+    for c in range(fp, x["k_idx"].shape[0]):
+        assert np.all(o["log_k"][c, V:] == 0) and np.all(o["cpe"][c, V:] == 1) and np.all(o["is_last"][c, V:] == 0)
+        r = o["pos_k"][c, V:].view(np.uint32)
+        assert np.all(r >> 17 == 0) and np.all(r >= V * (W + R) - 0)   # invalid entries sort last
+        assert np.all(o["A"][c, V:] == 0) and np.all(o["QK"][c, V:] == 0) and np.all(o["QK"][c, :, V:] == 0)
+        tail = o["sorted_k"][c].view(np.uint32)[V * W:]
+        assert np.all(tail >> 30 == 3) and np.all(tail & 0x20000)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+MUTATIONS = {
+    "decay_sign": ("exp(ch.logv[e] - ch.logv[f])", "exp(ch.logv[f] - ch.logv[e])"),
+    "repeat_rule_dropped": ("if (!prev_same) xe =", "if (1) xe ="),
+    "rex_includes_own": ("for (int u = s + 1; u < r1; ++u) after", "for (int u = s; u < r1; ++u) after"),
+    "qk_diagonal_dropped": ("ch.isq[e] && j <= i", "ch.isq[e] && j < i"),
+    "pos_after_before_swapped": ("(uint32_t)asat << 17", "(uint32_t)imin(before, 127) << 17"),
+    "dw_cpe_dropped": ("double nv = base * cp + acc[i]", "double nv = base + acc[i]"),
+    "dw_rex_dropped": ("const double sc = ch.val[e] * exp(ch.rex[e])", "const double sc = ch.val[e]"),
+    "after_count_off_by_one": ("ch->ka[e] = nk - kseen;", "ch->ka[e] = nk - kseen + 1;"),
+    "group_total_drops_last": ("tot += xe;", "tot += (s + 1 < r1) ? xe : 0.0;"),
+}
+
+
+def _pins_pass(lib):
+    try:
+        for case in CASES[:4]:
+            C, W, R, S, V = case
+            rng = np.random.default_rng(11 + hash(case) % 2**32)
+            k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+            o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V, lib=lib)
+            A, QK = bf_pairs(k_idx, q_idx, k_val, q_val, g, V)
+            if not (np.allclose(o["A"][0], A, 1e-12, 1e-12) and np.allclose(o["QK"][0], QK, 1e-12, 1e-12)):
+                return False
+            G = token_G(k_idx, g, V)
+            order = bf_sorted(k_idx, q_idx, V)
+            for r, d in enumerate(order):
+                b, a = bf_peers(order, d)
+                if d["valid"]:
+                    want = r | min(a, 127) << 17 | min(b + 1 + min(a, 127), 127) << 24
+                    if o["pos_q" if d["q"] else "pos_k"][0, d["t"], d["a"]] != want:
+                        return False
+                    lg = o["log_q" if d["q"] else "log_k"][0, d["t"], d["a"]]
+                    if abs(lg - Gs(G, d["slot"], d["t"])) > 1e-12:
+                        return False
+                    if not d["q"] and abs(o["rex"][0, d["t"], d["a"]] - (G[d["slot"]][C - 1] - G[d["slot"]][d["t"]])) > 1e-12:
+                        return False
+            hd = 3
+            bank = rng.standard_normal((S, hd))
+            want = bank.copy()
+            dv = rng.standard_normal((C, hd))
+            oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=V, val_dtype="f32", bank_dtype="f32",
+                            round_cpe=False, round_bank=False, lib=lib)
+            token_recurrence(want, k_idx, k_val, g, dv, V)
+            if not np.allclose(bank, want, 1e-11, 1e-11):
+                return False
+        return True
+    except Exception:
+        return False
+
+
+def test_pins_pass_on_the_oracle():
+    assert _pins_pass(oracle._load())
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "sdm_oracle.c")).read()
+    assert old in src, f"mutation anchor missing: {old}"
+    mutated = tmp_path / "sdm_oracle.c"
+    mutated.write_text(src.replace(old, new, 1))
+    so = oracle.build(str(mutated), str(tmp_path))
+    lib = oracle.load_variant(so)
+    assert not _pins_pass(lib), f"planted mistake '{name}' was not caught by the pins"
+    shutil.rmtree(tmp_path, ignore_errors=True)
