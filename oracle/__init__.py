@@ -44,7 +44,7 @@ def _bind(lib):
     lib.sdm_oracle_phase1.restype = ctypes.c_int
     lib.sdm_oracle_phase1.argtypes = [i64, i32, i32, i32, i64, i32, i32, i64] + [P] * 26
     lib.sdm_oracle_dw_chunk.restype = ctypes.c_int
-    lib.sdm_oracle_dw_chunk.argtypes = ([i32, i32, i32, i32, i32, i64, i32] + [P] * 10 +
+    lib.sdm_oracle_dw_chunk.argtypes = ([i32, i32, i32, i32, i32, i64, i32] + [P] * 11 +
                                         [i32, i32, i32, i32, f64])
     return lib
 
@@ -124,7 +124,7 @@ def phase1(k_idx, q_idx, k_val, q_val, g, *, S, val_dtype, first_partial=None, v
 
 
 def dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, *, S, V, val_dtype, bank_dtype,
-             round_cpe=True, round_bank=True, alt=None, amb=None, touched=None, amb_rel=2.0 ** -17,
+             round_cpe=True, round_bank=True, alt=None, amb=None, touched=None, mag=None, amb_rel=2.0 ** -17,
              lib=None):
     """Decay-and-write of one chunk ([C, W] / [C, R] inputs, dv [C, hd] float64) into ``bank``
     ([S, hd] float64, in place). See sdm_oracle_dw_chunk for ``alt`` / ``amb`` / ``touched``."""
@@ -141,7 +141,7 @@ def dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, *, S, V, val_dtype, bank_d
     dvv = np.ascontiguousarray(dv, np.float64)
     st = lib.sdm_oracle_dw_chunk(C, W, R, V, g_per_entry, S, hd, _ptr(k_idx), _ptr(q_idx), _ptr(kv),
                                  _ptr(qv), _ptr(gg), _ptr(dvv), _ptr(bank), _ptr(alt), _ptr(amb),
-                                 _ptr(touched), int(round_cpe), int(val_dtype == "bf16"),
+                                 _ptr(touched), _ptr(mag), int(round_cpe), int(val_dtype == "bf16"),
                                  int(round_bank), int(bank_dtype == "bf16"), float(amb_rel))
     if st != 0:
         raise ValueError("oracle: a valid slot id is outside [0, S)")
@@ -153,20 +153,21 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
 
     ``inputs`` holds chunk-major arrays of P streams (as synth.make_inputs returns); ``p_local`` is
     the stream's index among them. ``bank`` is that stream's [S, hd] float64 rows (updated in place).
-    With ``track`` returns (alt, amb, touched) for tolerance bookkeeping.
+    With ``track`` returns (alt, amb, touched, mag) for tolerance bookkeeping.
     """
     step_end = steps if step_end is None else step_end
     hd = bank.shape[1]
     alt = bank.copy() if track else None
     amb = np.zeros(S, np.int32) if track else None
     touched = np.zeros(S, np.int32) if track else None
+    mag = np.zeros_like(bank) if track else None
     for ti in range(step_begin, step_end):
         c = ti * P + p_local
         V = valid_last if ti == steps - 1 else C
         dv = as_f64(inputs["dv"][c * C:(c + 1) * C], dv_dtype).reshape(C, hd)
         dw_chunk(bank, inputs["k_idx"][c], inputs["q_idx"][c], inputs["k_val"][c], inputs["q_val"][c],
                  inputs["g"][c], dv, S=S, V=V, val_dtype=val_dtype, bank_dtype=bank_dtype,
-                 round_cpe=round_cpe, round_bank=round_bank, alt=alt, amb=amb, touched=touched)
+                 round_cpe=round_cpe, round_bank=round_bank, alt=alt, amb=amb, touched=touched, mag=mag)
     if track:
-        return alt, amb, touched
+        return alt, amb, touched, mag
     return None

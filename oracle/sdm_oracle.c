@@ -314,31 +314,37 @@ int sdm_oracle_phase1(int64_t nchunks, int C, int W, int R, int64_t first_partia
  * alt (nullable, [S, hd]): for a row whose cpe lies so near a rounding boundary of the value type
  * that float32 arithmetic may round it the other way, the row's value with the other rounding;
  * elsewhere the same value as bank. amb (nullable, [S]) counts such rows; touched ([S]) counts writes.
+ * mag (nullable, [S, hd]): |base * cpe_last| + sum_m |sc_m * dv[tok_m]| of the row's last write, the
+ * scale of the rounding error a float32 evaluation of the row can make.
  * Returns 0, or -1 if a valid slot id is out of range.
  */
 int sdm_oracle_dw_chunk(int C, int W, int R, int V, int g_per_entry, int64_t S, int hd,
                         const int32_t* k_idx, const int32_t* q_idx, const double* k_val,
                         const double* q_val, const double* g, const double* dv, double* bank,
-                        double* alt, int32_t* amb, int32_t* touched, int round_cpe, int val_bf16,
+                        double* alt, int32_t* amb, int32_t* touched, double* mag, int round_cpe, int val_bf16,
                         int round_bank, int bank_bf16, double amb_rel) {
     const int g_width = g_per_entry ? W : 1, g_ls = g_per_entry ? 1 : 0;
     chunk_t ch;
     const int st = chunk_analyze(&ch, C, W, R, V, S, k_idx, q_idx, k_val, q_val, g, g_width, g_ls);
     double* acc = (double*)calloc((size_t)hd, sizeof(double));
+    double* aabs = (double*)calloc((size_t)hd, sizeof(double));
     int r = 0;
     while (r < ch.n) {
         const int e0 = ch.order[r];
         const int r1 = ch.gend[e0];
         /* members: the group's valid write entries, in sorted order */
         int members = 0;
-        for (int i = 0; i < hd; ++i) acc[i] = 0.0;
+        for (int i = 0; i < hd; ++i) acc[i] = aabs[i] = 0.0;
         int64_t s = -1;
         for (int u = r; u < r1; ++u) {
             const int e = ch.order[u];
             if (!ch.valid[e] || ch.isq[e]) continue;
             const double sc = ch.val[e] * exp(ch.rex[e]);
             const double* row = dv + (int64_t)ch.tok[e] * hd;
-            for (int i = 0; i < hd; ++i) acc[i] += sc * row[i];
+            for (int i = 0; i < hd; ++i) {
+                acc[i] += sc * row[i];
+                aabs[i] += fabs(sc * row[i]);
+            }
             s = ch.slot[e];
             ++members;
         }
@@ -359,6 +365,7 @@ int sdm_oracle_dw_chunk(int C, int W, int R, int V, int g_per_entry, int64_t S, 
             double* arow = alt ? alt + s * hd : NULL;
             for (int i = 0; i < hd; ++i) {
                 const double base = brow[i];
+                if (mag) mag[s * hd + i] = fabs(base * cp) + aabs[i];
                 double nv = base * cp + acc[i];
                 if (arow) {
                     /* an earlier ambiguity of this row carries on through its own alternative */
@@ -374,6 +381,7 @@ int sdm_oracle_dw_chunk(int C, int W, int R, int V, int g_per_entry, int64_t S, 
         r = r1;
     }
     free(acc);
+    free(aabs);
     chunk_free(&ch);
     return st;
 }
