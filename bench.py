@@ -1,0 +1,370 @@
+"""Benchmark of the sparse-delta-memory forward (Phase 1 + DW over every step) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large] [--impl ours|reference]
+
+One step = one forward over the whole workload: Phase 1 of every chunk and the decay-and-write
+of every step, through the library's C ABI. The default workload is the large one (P = 32
+streams x T = 8192 tokens, C = 256, S = 2^20 slots per stream, hd = 128, W = R = 16, bf16; an
+8 GiB bank, far larger than L2, so no flush is needed between steps). Under torchrun each rank
+runs its own copy of the workload (independent streams: weak scaling, no collective on the data
+path); rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle (the only reference this method has) on a bounded
+sample of the same workload, on this host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, make_inputs  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per launch from one ncu capture, keyed by workload, kernel and the
+# hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
+# voids the figure (reported as null).
+NCU_TRAFFIC = {}
+
+
+def src_hash() -> str:
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "sparse_slot_memory_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 3 + i and r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def count_groups(x, w):
+    """Slot groups with at least one valid write entry, per chunk (exactly, from the data)."""
+    k = x["k_idx"].reshape(x["k_idx"].shape[0], -1).astype(np.int64)
+    N = k.shape[0]
+    total = 0
+    for c0 in range(0, N, 256):
+        blk = np.sort(k[c0:c0 + 256], axis=1)
+        valid = blk >= 0
+        distinct = np.concatenate([np.ones((blk.shape[0], 1), bool), blk[:, 1:] != blk[:, :-1]], axis=1)
+        total += int((distinct & valid).sum())
+    return total
+
+
+def algorithmic_bytes(w, x, groups):
+    """Bytes per forward (SURVEY section 8(d) accounting): inputs read once, outputs written once,
+    dv rows read once, per slot group one base-row read and one row write."""
+    vt = 2 if w.val_dtype == "bf16" else 4
+    dvt = 2 if w.dv_dtype == "bf16" else 4
+    bt = 2 if w.bank_dtype == "bf16" else 4
+    N, C, W, R = x["k_idx"].shape[0], w.C, w.W, w.R
+    tok = N * C
+    p1_in = tok * (W * (4 + vt) + R * (4 + vt) + 4)
+    p1_out = tok * (W * (4 + 4 + vt + vt + 1 + 1 + 4) + R * (4 + vt + 4 + 1 + 1)) + N * C * C * 4 * 2
+    dw = tok * w.hd * dvt + groups * w.hd * bt * 2
+    return {"phase1": p1_in + p1_out, "dw": dw, "total": p1_in + p1_out + dw}
+
+
+def valid_tokens(w, P):
+    return P * w.T
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_slot_memory_gb300 as sdm
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sdm.build()
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.cuda()
+
+    host = {"k_idx": x["k_idx"], "q_idx": x["q_idx"], "k_val": x["k_val"], "q_val": x["q_val"], "g": x["g"],
+            "dv": x["dv"]}
+    dts = {"k_idx": "i", "q_idx": "i", "g": "f32", "k_val": w.val_dtype, "q_val": w.val_dtype, "dv": w.dv_dtype}
+    d = {k: dev(v, dts[k]) for k, v in host.items()}
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + w.seed + rank)
+    bdt = torch.bfloat16 if w.bank_dtype == "bf16" else torch.float32
+    bank = (torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen) * w.bank_scale).to(bdt)
+    ws = sdm.alloc_workspace(shape)
+    out = sdm.alloc_outputs(shape)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sdm.phase1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
+        sdm.dw(shape, d["dv"], bank, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert sdm.device_status(ws) == 0
+
+    # timed region: K forwards; per-kernel events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            sdm.phase1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
+            ev[i][1].record(stream)
+            sdm.dw(shape, d["dv"], bank, ws)
+            ev[i][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    p1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dw_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    assert sdm.device_status(ws) == 0
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = valid_tokens(w, w.P)
+    value = tokens * world / (ms / 1e3)
+
+    # end to end through the public API with host buffers: inputs H2D, forward, outputs D2H
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if dts[k] == "bf16" else np.ascontiguousarray(v))
+               .pin_memory() for k, v in host.items()}
+        outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in out.values())
+
+        def e2e_step():
+            for k, v in pin.items():
+                dst = d[k].view(torch.int16) if dts[k] == "bf16" else d[k]
+                dst.copy_(v, non_blocking=True)
+            sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws)
+            for k, v in out.items():
+                outs_h[k].copy_(v, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        n2 = max(2, min(args.steps, 5))
+        for _ in range(n2):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a0.elapsed_time(a1) / n2
+        if world > 1:
+            tt = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "inputs H2D from pinned host memory and every Phase-1 output D2H each step; the bank is resident state"}
+
+    groups = count_groups(x, w)
+    ab = algorithmic_bytes(w, x, groups)
+    peak, peak_kind = peaks()
+    dom = "dw" if dw_ms >= p1_ms else "phase1"
+    dom_ms = dw_ms if dom == "dw" else p1_ms
+    achieved = ab[dom] / (dom_ms / 1e3) / 1e9
+    key = f"{args.workload}:{dom}:{src_hash()}"
+    traffic = NCU_TRAFFIC.get(key)
+    result = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(w, x, budget_s=args.cpu_seconds)
+        result = {
+            "metric": "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.val_dtype, "data": "synthetic (seeded generators of the workload's distributions)",
+            "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "tokens_per_step_per_gpu": tokens, "parallelism": f"replicas x{world} (independent streams)",
+                       "l2": "inputs larger than L2 (8 GiB bank)"},
+            "hbm_gbs_total": ab["total"] / (ms / 1e3) / 1e9,
+            "kernels_ms": {"phase1": p1_ms, "dw": dw_ms},
+            "algorithmic_bytes": ab, "groups": groups,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "total_frac": ab["total"] / (ms / 1e3) / 1e9 / peak},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+            "impl": "ours",
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
+    """The oracle as it stands (float64, single thread) on a bounded sample: whole steps of one
+    stream (Phase 1 with the pair triangles, then DW), until ~budget_s seconds have passed."""
+    import oracle
+
+    P, C = x["P"], w.C
+    oracle.build()
+    t0 = time.perf_counter()
+    chunks = 0
+    p = 0
+    S = w.S
+    # the oracle's DW runs on the rows the sampled stream touches (compacted: same arithmetic)
+    ids = x["k_idx"][p::P].ravel()
+    slots = np.unique(ids[ids >= 0])
+    bank = np.zeros((len(slots), w.hd))
+    for ti in range(w.steps):
+        c = ti * P + p
+        V = w.valid_last if ti == w.steps - 1 else C
+        oracle.phase1(x["k_idx"][c:c + 1], x["q_idx"][c:c + 1], x["k_val"][c:c + 1], x["q_val"][c:c + 1],
+                      x["g"][c:c + 1], S=S, val_dtype=w.val_dtype, first_partial=0 if V < C else 1, valid_last=V)
+        kk = np.searchsorted(slots, x["k_idx"][c]).astype(np.int32)
+        kk[x["k_idx"][c] < 0] = -1
+        qq = np.zeros_like(x["q_idx"][c])
+        dvr = oracle.as_f64(x["dv"][c * C:(c + 1) * C], w.dv_dtype)
+        oracle.dw_chunk(bank, kk, qq, x["k_val"][c], x["q_val"][c], x["g"][c], dvr, S=len(slots), V=V,
+                        val_dtype=w.val_dtype, bank_dtype=w.bank_dtype)
+        chunks += 1
+        if time.perf_counter() - t0 > budget_s or (max_chunks and chunks >= max_chunks):
+            break
+    dt = time.perf_counter() - t0
+    toks = chunks * C
+    return {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks ({toks} tokens) of stream 0: Phase 1 with A/QK + DW, float64, "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w, streams=[0])
+    for _ in range(args.warmup):
+        cpu_baseline(w, x, budget_s=1.0, max_chunks=1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, x, budget_s=args.cpu_seconds / max(1, args.steps)))
+    el = time.perf_counter() - t0
+    v = statistics.mean(r["value"] for r in vals)
+    print(json.dumps({
+        "impl": "reference", "metric": "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+        "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": w.name, **w.describe()},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="large", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

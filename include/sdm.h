@@ -1,0 +1,179 @@
+/*
+ * sdm.h -- C ABI of the GB300 (sm_103a) forward hot path of the chunked sparse-delta-memory
+ * (SDM) recurrence: Phase 1 and the Phase-2 decay-and-write (DW).
+ *
+ * Definitions followed (sparse-delta-memory 2.0.0):
+ *   phase1_cuda.py, module docstring ........ the Phase-1 outputs and the determinism contract
+ *   phase1_cuda.py, p1_keys_zw_kernel ........ entry order and payload bits, invalid tokens
+ *   phase1_cuda.py, p1_scan_kernel ........... gates, log-cumsums, rex, cpe, flags, pos pack,
+ *                                              sorted-row elements
+ *   phase1_cuda.py, p1_pairs_kernel comment .. the A / QK pair triangles
+ *   mover_da2_cuda.py, module docstring ...... DW: bank[s] = fma(base, cpe_last, acc),
+ *                                              acc = fma(sc_m, dv[tok_m], acc) in sorted order
+ *   mover_fx_cuda.py, module docstring ....... the bank-direct DW contract (base read from the
+ *                                              bank row itself; one writer per row and launch)
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller. The library never allocates
+ *     device or host memory. It launches on `stream` and never synchronizes it (except
+ *     sdm_device_status, which reads a word back).
+ *   - Layout is chunk-major: chunk c = ti * P + p holds tokens [ti*C, (ti+1)*C) of stream p,
+ *     for ti in [0, steps). N = steps * P chunks.
+ *       k_idx [N, C, W] int32, q_idx [N, C, R] int32: stream-local slot ids in [0, S). Ids of
+ *         invalid tokens (t >= valid_last in the last step's chunks) are ignored.
+ *       k_val [N, C, W], q_val [N, C, R]: val_dtype (float32 or bfloat16).
+ *       g: float32 [N, C] one gate per token (gate_per_entry = 0) or [N, C, W] per write entry (1).
+ *       dv [N * C, hd]: dv_dtype; row c * C + t is token t of chunk c.
+ *       bank [P * S, hd]: bank_dtype; stream p owns rows [p*S, (p+1)*S). Updated in place.
+ *   - Alignment: bank, dv and every output array 16-byte aligned; hd a multiple of 4.
+ *   - Limits: 1 <= C <= 256, 1 <= W, R <= 256, C * (W + R) <= 8192 (one chunk sorts on chip),
+ *     1 <= S <= 2^31 - 1, P * S * hd fits in int64.
+ *   - Shape, dtype, alignment and workspace errors are returned BEFORE any launch. Errors the
+ *     device finds (a valid slot id outside [0, S), a bounded wait that ran out) are OR-ed into
+ *     a status word inside the workspace; read it with sdm_device_status. No kernel traps.
+ *   - Determinism: for fixed inputs, shapes and GPU type every output is bitwise reproducible.
+ *     The sort is stable, scans combine in a fixed tree, every A/QK cell and every bank row has
+ *     one writer that adds its terms in an input-determined order, and no atomics touch a sum.
+ */
+#ifndef SDM_H
+#define SDM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* sdm_stream_t;
+
+typedef enum {
+    SDM_OK = 0,
+    SDM_ERR_ARG = -1,       /* a required pointer is NULL, or a step range is empty / out of range */
+    SDM_ERR_SHAPE = -2,     /* a size is outside the limits above */
+    SDM_ERR_DTYPE = -3,     /* an unknown dtype code */
+    SDM_ERR_ALIGN = -4,     /* a pointer is not 16-byte aligned, or hd % 4 != 0 */
+    SDM_ERR_WORKSPACE = -5, /* ws is NULL, misaligned or smaller than sdm_workspace_bytes */
+    SDM_ERR_SMEM = -6,      /* the chunk does not fit the device's shared memory */
+    SDM_ERR_CUDA = -7,      /* a CUDA runtime call failed (launch, attribute, memset) */
+    SDM_ERR_DEVICE = -8     /* sdm_device_status found a nonzero device status word */
+} sdm_status;
+
+typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
+
+/* Bits of the device status word (sdm_device_status). */
+#define SDM_DEV_BAD_SLOT 0x1u /* a valid entry's slot id was outside [0, S): the entry is dropped */
+#define SDM_DEV_TIMEOUT 0x2u  /* a bounded wait of the DW kernel ran out: the bank is undefined */
+
+typedef struct {
+    int32_t P;              /* streams */
+    int32_t C;              /* tokens per chunk */
+    int32_t W;              /* write (K) entries per token */
+    int32_t R;              /* read (Q) entries per token */
+    int32_t hd;             /* bank / dv row width */
+    int32_t valid_last;     /* valid tokens of the last step's chunks, 1..C */
+    int64_t steps;          /* chunks per stream */
+    int64_t S;              /* slots per stream */
+    int32_t val_dtype;      /* sdm_dtype of k_val, q_val and of cpe / k_eff / q_w */
+    int32_t dv_dtype;       /* sdm_dtype of dv */
+    int32_t bank_dtype;     /* sdm_dtype of the bank */
+    int32_t gate_per_entry; /* 0: g [N, C]; 1: g [N, C, W] */
+} sdm_shape;
+
+/*
+ * Phase-1 outputs, entry order (phase1_cuda.py module docstring and p1_scan_kernel). Any field
+ * may be NULL: it is not written.
+ *   [N, C, W]: log_k f32 (log-cumsum of the slot's gates at the entry, own token included),
+ *              rex f32 (gates of the slot's later writes in the chunk), cpe val_dtype
+ *              (exp of the slot's total gate in the chunk), k_eff val_dtype (k * exp(log_k)),
+ *              is_last / is_only int8, pos_k int32 (position pack below).
+ *   [N, C, R]: log_q f32, q_w val_dtype (q * exp(log_q)), pos_q int32, q_last / q_only int8.
+ *   A, QK [N, C, C] f32: A[i][j] = sum over shared slots of k_i k_j exp(log_k_i - log_k_j),
+ *              j < i; QK[i][j] = sum of q_i k_j exp(log_q_i - log_k_j), j <= i; zero elsewhere.
+ *   sorted_k [N, C*W], sorted_q [N, C*R] int32: each kind's entries in sorted order as
+ *              (entry bits: lane | isQ << 8 | token << 9 | invalid << 17)
+ *              | min(peers before, 4095) << 18 | LAST << 30 | FIRST << 31; invalid: | 3 << 30.
+ *   repeats: one int64 to which the count of repeated write entries (a token's write entry on
+ *            a slot its previous write entry of the group already holds) is ADDED.
+ * Position pack: r | min(after, 127) << 17 | min(before + 1 + min(after, 127), 127) << 24 for a
+ * valid entry (r = position in the chunk's sorted row, before / after = valid entries of the
+ * same kind and slot before / after it), r alone for an invalid entry. Invalid entries:
+ * log 0, rex 0, cpe 1, k_eff / q_w 0, flags 0.
+ */
+typedef struct {
+    float* log_k;
+    float* rex;
+    void* cpe;
+    void* k_eff;
+    int8_t* is_last;
+    int8_t* is_only;
+    int32_t* pos_k;
+    float* log_q;
+    void* q_w;
+    int32_t* pos_q;
+    int8_t* q_last;
+    int8_t* q_only;
+    float* A;
+    float* QK;
+    int32_t* sorted_k;
+    int32_t* sorted_q;
+    int64_t* repeats;
+} sdm_p1_out;
+
+/*
+ * Bytes of the caller-allocated device workspace for this shape (DW records of every chunk,
+ * tile bounds, counters and the status word). The workspace must be 256-byte aligned and, before
+ * its first use, zeroed with sdm_workspace_init. Returns 0 for an invalid shape.
+ */
+size_t sdm_workspace_bytes(const sdm_shape* shape);
+
+/* Zeroes the workspace's header (status word and counters) on `stream`. */
+sdm_status sdm_workspace_init(void* ws, size_t ws_bytes, sdm_stream_t stream);
+
+/*
+ * Phase 1 of the chunks of steps [step_begin, step_end) (all P streams): the outputs in `out`
+ * and, in `ws`, the DW records of those chunks. Inputs are the full [N, ...] arrays; only the
+ * range's chunks are read and written. Launches one kernel (one CTA per chunk).
+ */
+sdm_status sdm_phase1(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                      const void* k_val, const void* q_val, const float* g, const sdm_p1_out* out,
+                      int64_t step_begin, int64_t step_end, void* ws, size_t ws_bytes,
+                      sdm_stream_t stream);
+
+/*
+ * DW of steps [step_begin, step_end), in step order, from the records sdm_phase1 left in `ws`
+ * for those steps: per slot group of each chunk, bank[p*S + s] = fma(base, cpe_last, acc),
+ * acc = fma(sc_m, dv[tok_m], acc) over the group's write entries in sorted order starting at 0,
+ * sc = f32(k) * expf(rex), base = the row before this step (stored RN in bfloat16, or as the f32
+ * result). One persistent kernel runs every step; a step of stream p starts once the previous
+ * step of p has finished (per-stream counters in `ws`, bounded waits).
+ */
+sdm_status sdm_dw(const sdm_shape* shape, const void* dv, void* bank, int64_t step_begin,
+                  int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);
+
+/*
+ * The forward over steps [step_begin, step_end): sdm_phase1 then sdm_dw on `stream`.
+ * `out` may be NULL (no Phase-1 outputs written; records still go to ws). Running [0, k) then
+ * [k, steps) gives the same bits as [0, steps).
+ */
+sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                              const void* k_val, const void* q_val, const float* g, const void* dv,
+                              void* bank, const sdm_p1_out* out, int64_t step_begin,
+                              int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);
+
+/*
+ * Synchronizes `stream`, reads the workspace's device status word into *code_out (0 = fine,
+ * else SDM_DEV_* bits) and, if `clear`, zeroes it. Returns SDM_ERR_DEVICE when the word is
+ * nonzero, SDM_ERR_CUDA when the copy fails.
+ */
+sdm_status sdm_device_status(const void* ws, int32_t* code_out, int32_t clear, sdm_stream_t stream);
+
+/* A static string naming a status code. */
+const char* sdm_status_string(sdm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H */

@@ -1,0 +1,149 @@
+"""Python face of the C ABI: argument marshalling only.
+
+Tensors are CUDA tensors owned by the caller; every call passes their device pointers and the
+current torch stream to ``libsdm_gb300.so``. Every step of the computation runs in the
+library's kernels; there is no host or PyTorch fallback, and a CPU tensor is an error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from . import _abi
+
+_DT = {"f32": _abi.SDM_F32, "bf16": _abi.SDM_BF16}
+_TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+class SdmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = _abi.load().sdm_status_string(status).decode()
+        super().__init__(f"{what}: {msg} ({status})")
+        self.status = status
+
+
+@dataclasses.dataclass(frozen=True)
+class ShapeSpec:
+    P: int
+    C: int
+    W: int
+    R: int
+    hd: int
+    steps: int
+    S: int
+    valid_last: int
+    val_dtype: str = "bf16"
+    dv_dtype: str = "bf16"
+    bank_dtype: str = "bf16"
+    gate_per_entry: bool = False
+
+    @property
+    def N(self) -> int:
+        return self.steps * self.P
+
+    def c(self) -> _abi.Shape:
+        return _abi.Shape(self.P, self.C, self.W, self.R, self.hd, self.valid_last, self.steps, self.S,
+                          _DT[self.val_dtype], _DT[self.dv_dtype], _DT[self.bank_dtype], int(self.gate_per_entry))
+
+    @classmethod
+    def from_workload(cls, w, P=None) -> "ShapeSpec":
+        return cls(P=w.P if P is None else P, C=w.C, W=w.W, R=w.R, hd=w.hd, steps=w.steps, S=w.S,
+                   valid_last=w.valid_last, val_dtype=w.val_dtype, dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("expected a CUDA tensor (the library runs on the GPU only)")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != _abi.SDM_OK:
+        raise SdmError(st, what)
+
+
+def workspace_bytes(shape: ShapeSpec) -> int:
+    n = _abi.load().sdm_workspace_bytes(ctypes.byref(shape.c()))
+    if n == 0:
+        raise ValueError(f"invalid shape {shape}")
+    return int(n)
+
+
+def alloc_workspace(shape: ShapeSpec, device="cuda", stream=None) -> torch.Tensor:
+    """A zero-initialised workspace (torch allocations are 256-byte aligned)."""
+    n = workspace_bytes(shape)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(_abi.load().sdm_workspace_init(_ptr(ws), n, _stream(stream)), "sdm_workspace_init")
+    return ws
+
+
+def alloc_outputs(shape: ShapeSpec, device="cuda", fields=_abi.P1_FIELDS) -> dict:
+    N, C, W, R = shape.N, shape.C, shape.W, shape.R
+    vt = _TORCH_DT[shape.val_dtype]
+    spec = {
+        "log_k": ((N, C, W), torch.float32), "rex": ((N, C, W), torch.float32), "cpe": ((N, C, W), vt),
+        "k_eff": ((N, C, W), vt), "is_last": ((N, C, W), torch.int8), "is_only": ((N, C, W), torch.int8),
+        "pos_k": ((N, C, W), torch.int32), "log_q": ((N, C, R), torch.float32), "q_w": ((N, C, R), vt),
+        "pos_q": ((N, C, R), torch.int32), "q_last": ((N, C, R), torch.int8), "q_only": ((N, C, R), torch.int8),
+        "A": ((N, C, C), torch.float32), "QK": ((N, C, C), torch.float32),
+        "sorted_k": ((N, C * W), torch.int32), "sorted_q": ((N, C * R), torch.int32), "repeats": ((2,), torch.int64),
+    }
+    out = {}
+    for f in fields:
+        shp, dt = spec[f]
+        out[f] = torch.zeros(shp, dtype=dt, device=device) if f == "repeats" else torch.empty(shp, dtype=dt, device=device)
+    return out
+
+
+def _p1out(out):
+    o = _abi.P1Out()
+    if out:
+        for f in _abi.P1_FIELDS:
+            if f in out and out[f] is not None:
+                setattr(o, f, _ptr(out[f]).value)
+    return o
+
+
+def phase1(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws, step_begin=0, step_end=None, stream=None):
+    step_end = shape.steps if step_end is None else step_end
+    o = _p1out(out)
+    st = _abi.load().sdm_phase1(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val), _ptr(g),
+                                ctypes.byref(o), step_begin, step_end, _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "sdm_phase1")
+
+
+def dw(shape: ShapeSpec, dv, bank, ws, step_begin=0, step_end=None, stream=None):
+    step_end = shape.steps if step_end is None else step_end
+    st = _abi.load().sdm_dw(ctypes.byref(shape.c()), _ptr(dv), _ptr(bank), step_begin, step_end, _ptr(ws), ws.numel(),
+                            _stream(stream))
+    _check(st, "sdm_dw")
+
+
+def forward_chunks(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, out, ws, step_begin=0, step_end=None,
+                   stream=None):
+    step_end = shape.steps if step_end is None else step_end
+    o = _p1out(out)
+    st = _abi.load().sdm_forward_chunks(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val),
+                                        _ptr(g), _ptr(dv), _ptr(bank), ctypes.byref(o) if out else None, step_begin,
+                                        step_end, _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "sdm_forward_chunks")
+
+
+def device_status(ws, clear: bool = True, stream=None) -> int:
+    code = _abi.c_i32(0)
+    st = _abi.load().sdm_device_status(_ptr(ws), ctypes.byref(code), int(clear), _stream(stream))
+    if st not in (_abi.SDM_OK, -8):
+        _check(st, "sdm_device_status")
+    return int(code.value)

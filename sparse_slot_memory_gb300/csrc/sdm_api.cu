@@ -1,0 +1,312 @@
+// sdm_api.cu -- the extern "C" entry points declared in include/sdm.h: argument checks, the
+// workspace layout and the launches. Every check runs before any launch; nothing here allocates.
+#include <cstdint>
+#include <cstring>
+
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per bounded wait
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int prev_pow2(int x) {
+    int p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Derives every size and offset from the shape alone. Returns SDM_OK or the error code.
+sdm_status geometry(const sdm_shape* s, Geometry* g) {
+    if (s == nullptr) return SDM_ERR_ARG;
+    if (s->val_dtype < 0 || s->val_dtype > 1 || s->dv_dtype < 0 || s->dv_dtype > 1 || s->bank_dtype < 0 ||
+        s->bank_dtype > 1)
+        return SDM_ERR_DTYPE;
+    if (s->P < 1 || s->C < 1 || s->C > kMaxC || s->W < 1 || s->W > kMaxLanes || s->R < 1 || s->R > kMaxLanes ||
+        s->steps < 1 || s->S < 1 || s->S > 0x7FFFFFFFll || s->hd < 1 || s->valid_last < 1 || s->valid_last > s->C ||
+        (s->gate_per_entry != 0 && s->gate_per_entry != 1))
+        return SDM_ERR_SHAPE;
+    if (s->hd % 4 != 0) return SDM_ERR_ALIGN;
+    const int64_t n = static_cast<int64_t>(s->C) * (s->W + s->R);
+    if (n > kMaxRow) return SDM_ERR_SHAPE;
+    if (s->steps > (int64_t(1) << 40) / s->P) return SDM_ERR_SHAPE;
+    const int64_t N = s->steps * s->P;
+    // every flattened index must fit int64 with room: bank rows, dv rows, A/QK cells
+    if (s->S > (int64_t(1) << 62) / s->P / s->hd) return SDM_ERR_SHAPE;
+    if (N > (int64_t(1) << 62) / (static_cast<int64_t>(s->C) * s->C + s->C * int64_t(s->hd) + n)) return SDM_ERR_SHAPE;
+    memset(g, 0, sizeof(*g));
+    g->C = s->C;
+    g->W = s->W;
+    g->R = s->R;
+    g->wr = s->W + s->R;
+    g->n = static_cast<int>(n);
+    g->nk = s->C * s->W;
+    g->nq = s->C * s->R;
+    g->P = s->P;
+    g->hd = s->hd;
+    g->steps = s->steps;
+    g->N = N;
+    g->S = s->S;
+    int kb = 1;
+    while ((int64_t(1) << kb) < s->S) ++kb;
+    g->key_bits = kb;
+    g->passes = (kb + 7) / 8;
+    g->digit_bits = (kb + g->passes - 1) / g->passes;
+    int threads = static_cast<int>((n + kItems - 1) / kItems);
+    threads = static_cast<int>(round_up(static_cast<size_t>(threads), 32));
+    g->threads = threads;
+    g->npad = threads * kItems;
+    g->nwarps = threads / 32;
+    int L = prev_pow2(g->nk / 256 > 1 ? g->nk / 256 : 1);
+    L = L < 8 ? 8 : (L > 128 ? 128 : L);
+    g->L = L;
+    g->ntk = (g->nk + L - 1) / L;
+    g->nsl = (s->hd + 127) / 128;
+    // workspace
+    g->hdr_bytes = kHdrCounters + round_up(8 * static_cast<size_t>(s->P), 256);
+    g->krec_off = g->hdr_bytes;
+    g->tb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->nk * sizeof(int4), 256);
+    g->ws_bytes = g->tb_off + round_up(static_cast<size_t>(N) * (g->ntk + 1) * sizeof(int32_t), 256);
+    // Phase-1 shared memory: keys | vals | sidx | (pong + hist) or log-cumsums | pos | kb | rex | cpe | scratch
+    const size_t np = static_cast<size_t>(g->npad);
+    size_t off = 0;
+    g->sm_keys = off;
+    off += np * 4;
+    g->sm_vals = off;
+    off += np * 4;
+    g->sm_sidx = off;
+    off += np * 2;
+    g->sm_regd = off;
+    g->sm_pong = off;
+    g->sm_hist = off + np * 2;
+    off += np * 4;
+    g->sm_pos = off;
+    off += np * 4;
+    g->sm_kb = off;
+    off += np * 2;
+    g->sm_rex = off;
+    off += round_up(static_cast<size_t>(g->nk) * 4, 16);
+    g->sm_tot = off;
+    off += round_up(static_cast<size_t>(g->nk) * 4, 16);
+    g->sm_scr = off;
+    off += 64 * 16 + 64 * 4;
+    g->smem_bytes = round_up(off, 128);
+    return SDM_OK;
+}
+
+sdm_status check_ws(const Geometry& g, const void* ws, size_t ws_bytes) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < g.ws_bytes) return SDM_ERR_WORKSPACE;
+    return SDM_OK;
+}
+
+sdm_status check_range(const Geometry& g, int64_t b, int64_t e) {
+    if (b < 0 || e > g.steps || b > e) return SDM_ERR_ARG;
+    return SDM_OK;
+}
+
+sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_idx, const int32_t* q_idx,
+                      const void* k_val, const void* q_val, const float* gate, const sdm_p1_out* out,
+                      int64_t b, int64_t e, void* ws, cudaStream_t stream) {
+    P1Args a;
+    memset(&a, 0, sizeof(a));
+    a.k_idx = k_idx;
+    a.q_idx = q_idx;
+    a.k_val = k_val;
+    a.q_val = q_val;
+    a.g = gate;
+    if (out != nullptr) a.out = *out;
+    unsigned char* const w = static_cast<unsigned char*>(ws);
+    a.krec = reinterpret_cast<int4*>(w + g.krec_off);
+    a.tb = reinterpret_cast<int32_t*>(w + g.tb_off);
+    a.status = reinterpret_cast<uint32_t*>(w + kHdrStatus);
+    a.C = g.C;
+    a.W = g.W;
+    a.R = g.R;
+    a.wr = g.wr;
+    a.n = g.n;
+    a.nk = g.nk;
+    a.nq = g.nq;
+    a.npad = g.npad;
+    a.nwarps = g.nwarps;
+    a.key_bits = g.key_bits;
+    a.passes = g.passes;
+    a.digit_bits = g.digit_bits;
+    a.S = g.S;
+    a.c0 = b * g.P;
+    a.first_partial = (g.steps - 1) * g.P;
+    a.valid_last = s->valid_last;
+    a.g_width = s->gate_per_entry ? g.W : 1;
+    a.g_lane_stride = s->gate_per_entry ? 1 : 0;
+    a.wr_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.wr - 1) / g.wr);
+    a.L = g.L;
+    a.ntk = g.ntk;
+    a.sm_keys = static_cast<uint32_t>(g.sm_keys);
+    a.sm_vals = static_cast<uint32_t>(g.sm_vals);
+    a.sm_sidx = static_cast<uint32_t>(g.sm_sidx);
+    a.sm_pong = static_cast<uint32_t>(g.sm_pong);
+    a.sm_hist = static_cast<uint32_t>(g.sm_hist);
+    a.sm_lv = static_cast<uint32_t>(g.sm_regd);
+    a.sm_pos = static_cast<uint32_t>(g.sm_pos);
+    a.sm_kb = static_cast<uint32_t>(g.sm_kb);
+    a.sm_rex = static_cast<uint32_t>(g.sm_rex);
+    a.sm_tot = static_cast<uint32_t>(g.sm_tot);
+    a.sm_scr = static_cast<uint32_t>(g.sm_scr);
+    const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
+    return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
+}
+
+sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* bank, int64_t b, int64_t e, void* ws,
+                  cudaStream_t stream) {
+    unsigned char* const w = static_cast<unsigned char*>(ws);
+    // DW counters and the abort flag start at zero for every launch (the status word is kept)
+    if (cudaMemsetAsync(w + kHdrAbort, 0, g.hdr_bytes - kHdrAbort, stream) != cudaSuccess) return SDM_ERR_CUDA;
+    DWArgs a;
+    memset(&a, 0, sizeof(a));
+    a.krec = reinterpret_cast<const int4*>(w + g.krec_off);
+    a.tb = reinterpret_cast<const int32_t*>(w + g.tb_off);
+    a.dv = dv;
+    a.bank = bank;
+    a.status = reinterpret_cast<uint32_t*>(w + kHdrStatus);
+    a.abort_flag = reinterpret_cast<uint32_t*>(w + kHdrAbort);
+    a.claim = reinterpret_cast<uint32_t*>(w + kHdrCounters);
+    a.done = a.claim + g.P;
+    a.P = g.P;
+    a.C = g.C;
+    a.nk = g.nk;
+    a.ntk = g.ntk;
+    a.nsl = g.nsl;
+    a.hd = g.hd;
+    a.S = g.S;
+    a.step_begin = b;
+    a.per_step = static_cast<int64_t>(g.ntk) * g.nsl;
+    a.per_stream = (e - b) * a.per_step;
+    a.timeout_ns = kWaitTimeoutNs;
+    const cudaError_t err = launch_dw(a, s->dv_dtype == SDM_BF16, s->bank_dtype == SDM_BF16, stream);
+    return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
+}
+
+sdm_status check_p1_args(const Geometry& g, const int32_t* k_idx, const int32_t* q_idx, const void* k_val,
+                         const void* q_val, const float* gate, const sdm_p1_out* out) {
+    if (k_idx == nullptr || q_idx == nullptr || k_val == nullptr || q_val == nullptr || gate == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(k_idx) || !aligned16(q_idx) || !aligned16(k_val) || !aligned16(q_val) || !aligned16(gate))
+        return SDM_ERR_ALIGN;
+    if (out != nullptr) {
+        const void* ptrs[] = {out->log_k, out->rex, out->cpe, out->k_eff, out->is_last, out->is_only,
+                              out->pos_k, out->log_q, out->q_w, out->pos_q, out->q_last, out->q_only,
+                              out->A, out->QK, out->sorted_k, out->sorted_q, out->repeats};
+        for (const void* p : ptrs)
+            if (p != nullptr && !aligned16(p)) return SDM_ERR_ALIGN;
+    }
+    (void)g;
+    return SDM_OK;
+}
+
+sdm_status check_smem(const Geometry& g) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SDM_ERR_CUDA;
+    size_t lim = 0;
+    if (phase1_smem_limit(dev, &lim) != cudaSuccess) return SDM_ERR_CUDA;
+    return g.smem_bytes <= lim ? SDM_OK : SDM_ERR_SMEM;
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" size_t sdm_workspace_bytes(const sdm_shape* shape) {
+    Geometry g;
+    if (geometry(shape, &g) != SDM_OK) return 0;
+    return g.ws_bytes;
+}
+
+extern "C" sdm_status sdm_workspace_init(void* ws, size_t ws_bytes, sdm_stream_t stream) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < kHdrCounters)
+        return SDM_ERR_WORKSPACE;
+    return cudaMemsetAsync(ws, 0, kHdrCounters, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SDM_OK
+                                                                                                        : SDM_ERR_CUDA;
+}
+
+extern "C" sdm_status sdm_phase1(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                                 const void* k_val, const void* q_val, const float* g, const sdm_p1_out* out,
+                                 int64_t step_begin, int64_t step_end, void* ws, size_t ws_bytes,
+                                 sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if ((st = check_p1_args(geo, k_idx, q_idx, k_val, q_val, g, out)) != SDM_OK) return st;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if ((st = check_smem(geo)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    return run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sdm_status sdm_dw(const sdm_shape* shape, const void* dv, void* bank, int64_t step_begin, int64_t step_end,
+                             void* ws, size_t ws_bytes, sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if (dv == nullptr || bank == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(dv) || !aligned16(bank)) return SDM_ERR_ALIGN;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    return run_dw(shape, geo, dv, bank, step_begin, step_end, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                                         const void* k_val, const void* q_val, const float* g, const void* dv,
+                                         void* bank, const sdm_p1_out* out, int64_t step_begin, int64_t step_end,
+                                         void* ws, size_t ws_bytes, sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if ((st = check_p1_args(geo, k_idx, q_idx, k_val, q_val, g, out)) != SDM_OK) return st;
+    if (dv == nullptr || bank == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(dv) || !aligned16(bank)) return SDM_ERR_ALIGN;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if ((st = check_smem(geo)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
+        return st;
+    return run_dw(shape, geo, dv, bank, step_begin, step_end, ws, cs);
+}
+
+extern "C" sdm_status sdm_device_status(const void* ws, int32_t* code_out, int32_t clear, sdm_stream_t stream) {
+    if (ws == nullptr || code_out == nullptr) return SDM_ERR_ARG;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, static_cast<const unsigned char*>(ws) + kHdrStatus, sizeof(word), cudaMemcpyDeviceToHost,
+                        cs) != cudaSuccess)
+        return SDM_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return SDM_ERR_CUDA;
+    *code_out = static_cast<int32_t>(word);
+    if (clear && word != 0u) {
+        if (cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(word), cs) != cudaSuccess) return SDM_ERR_CUDA;
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return SDM_ERR_CUDA;
+    }
+    return word == 0u ? SDM_OK : SDM_ERR_DEVICE;
+}
+
+extern "C" const char* sdm_status_string(sdm_status status) {
+    switch (status) {
+        case SDM_OK: return "SDM_OK";
+        case SDM_ERR_ARG: return "SDM_ERR_ARG: a required pointer is NULL or a step range is invalid";
+        case SDM_ERR_SHAPE: return "SDM_ERR_SHAPE: a size is outside the supported limits";
+        case SDM_ERR_DTYPE: return "SDM_ERR_DTYPE: unknown dtype code";
+        case SDM_ERR_ALIGN: return "SDM_ERR_ALIGN: a pointer is not 16-byte aligned or hd % 4 != 0";
+        case SDM_ERR_WORKSPACE: return "SDM_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case SDM_ERR_SMEM: return "SDM_ERR_SMEM: the chunk does not fit the device's shared memory";
+        case SDM_ERR_CUDA: return "SDM_ERR_CUDA: a CUDA runtime call failed";
+        case SDM_ERR_DEVICE: return "SDM_ERR_DEVICE: the device status word is nonzero";
+    }
+    return "unknown sdm_status";
+}

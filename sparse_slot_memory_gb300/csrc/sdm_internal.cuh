@@ -1,0 +1,113 @@
+// sdm_internal.cuh -- shared definitions of the sm_103a kernels behind include/sdm.h.
+//
+// Bit layouts follow sparse-delta-memory 2.0.0 (phase1_cuda.py, p1_scan_kernel and the
+// Records comment): the payload / sorted-row entry bits (lane | isQ << 8 | token << 9 |
+// invalid << 17), FIRST = bit 31, LAST = bit 30, distance-to-FIRST at bits 18..29, and the
+// position pack (r | after << 17 | size << 24, counts saturating at 127).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/sdm.h"
+
+namespace sdm {
+
+// ---- layouts fixed by the method --------------------------------------------------------------
+constexpr uint32_t kIsQBit = 1u << 8;
+constexpr int kTokenShift = 9;
+constexpr uint32_t kInvalidBit = 1u << 17;
+constexpr uint32_t kEntryMask = 0x3FFFFu;
+constexpr uint32_t kFirst = 1u << 31;
+constexpr uint32_t kLast = 1u << 30;
+constexpr int kDistShift = 18;
+constexpr uint32_t kDistMax = 4095u;
+constexpr int kPosBits = 17;
+constexpr uint32_t kPosMask = (1u << kPosBits) - 1u;
+constexpr int kPosAfterShift = 17;
+constexpr int kPosSizeShift = 24;
+constexpr uint32_t kPosCountMax = 127u;
+
+// ---- this implementation's limits and geometry ------------------------------------------------
+constexpr int kMaxC = 256;
+constexpr int kMaxLanes = 256;          // W, R (8-bit lane field)
+constexpr int kItems = 8;               // sorted positions per thread in the Phase-1 kernel
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxRow = kItems * kMaxThreads;   // entries of one chunk held on chip
+constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid entry
+
+// Device status word bits (mirrors SDM_DEV_* in sdm.h).
+constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
+constexpr uint32_t kDevTimeout = SDM_DEV_TIMEOUT;
+
+// DW record of one write entry in the chunk's sorted write row (16 bytes, one vector load):
+//   x = token | LAST << 30 | FIRST << 31 | kRecInvalid, y = stream-local slot,
+//   z = f32 bits of sc = k * expf(rex), w = f32 bits of cpe (the value-type cpe widened).
+constexpr uint32_t kRecInvalid = 1u << 29;
+constexpr uint32_t kRecTokMask = 0xFFFFu;
+
+// Workspace header (bytes): [0] status word, [4] DW abort flag, [256..) per-stream DW claim
+// counters then per-stream DW done counters (uint32 each).
+constexpr size_t kHdrStatus = 0;
+constexpr size_t kHdrAbort = 4;
+constexpr size_t kHdrCounters = 256;
+
+struct Geometry {
+    int C, W, R, wr, n, nk, nq, P, hd;
+    int64_t steps, N, S;
+    int key_bits, passes, digit_bits;
+    int threads, npad, nwarps;
+    int L, ntk;            // DW tile length (write-row entries) and tiles per chunk
+    int nsl;               // DW column slices of 128 columns
+    size_t hdr_bytes, krec_off, tb_off, ws_bytes;
+    size_t smem_bytes;
+    // Phase-1 shared-memory carve (byte offsets)
+    size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_scr;
+};
+
+struct P1Args {
+    const int32_t* k_idx;
+    const int32_t* q_idx;
+    const void* k_val;
+    const void* q_val;
+    const float* g;
+    sdm_p1_out out;
+    int4* krec;
+    int32_t* tb;
+    uint32_t* status;
+    int C, W, R, wr, n, nk, nq, npad, nwarps;
+    int key_bits, passes, digit_bits;
+    int64_t S;
+    int64_t c0;             // first chunk of the launch
+    int64_t first_partial;  // first chunk whose tokens t >= valid_last are invalid
+    int valid_last;
+    int g_width, g_lane_stride;
+    uint32_t wr_magic;      // ceil(2^32 / wr): e / wr == umulhi(e, wr_magic) for e * wr < 2^32
+    int L, ntk;
+    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_scr, sm_lv;
+};
+
+struct DWArgs {
+    const int4* krec;
+    const int32_t* tb;
+    const void* dv;
+    void* bank;
+    uint32_t* status;
+    uint32_t* abort_flag;
+    uint32_t* claim;   // [P]
+    uint32_t* done;    // [P]
+    int P, C, nk, ntk, nsl, hd;
+    int64_t S;
+    int64_t step_begin;
+    int64_t per_step;   // items of one stream per step = ntk * nsl
+    int64_t per_stream; // items of one stream over the launch's steps
+    unsigned long long timeout_ns;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_phase1(const P1Args& a, int val_bf16, int64_t nchunks, int threads, size_t smem,
+                          cudaStream_t stream);
+cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream);
+cudaError_t phase1_smem_limit(int device, size_t* bytes);
+
+}  // namespace sdm

@@ -1,0 +1,617 @@
+// sdm_phase1.cu -- Phase 1 of the chunked sparse-delta-memory forward, one CTA per chunk, on chip.
+//
+// What it computes (sparse-delta-memory 2.0.0, phase1_cuda.py: module docstring,
+// p1_keys_zw_kernel, p1_scan_kernel, p1_pairs_kernel comment): the chunk's write (K) and read (Q)
+// entries are sorted stably by slot; per slot group, the log-cumsum of the gates (a write entry's
+// gate counts once per token: a token's repeated write entry adds 0), rex = gates after the
+// entry, cpe = exp(group total) in the value type, the flags, the packed positions and the sorted
+// rows; then the pair triangles A (write x earlier write of another token) and QK (read x
+// earlier write, own token included). It also writes the DW records of the chunk's sorted write
+// row and the FIRST-snapped tile bounds the DW kernel walks.
+//
+// GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
+// memory from load to the last output byte:
+//   0. load ids and values (coalesced) into entry-indexed arrays;
+//   1. stable LSD radix sort of entry indices by slot: per pass, warps rank their 256 positions
+//      with __match_any_sync against per-warp digit counters, one block scan of the counters,
+//      one scatter (no global round trips, no merge kernel);
+//   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
+//      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
+//      the DW records / sorted rows / tile bounds in sorted order;
+//   3. every entry-order output written from shared memory by consecutive threads;
+//   4. pair triangles: one warp per (row, triangle); each walk reads 32 earlier positions per
+//      step, lanes of one cell are summed by a fixed shuffle tree, one lane adds the cell's
+//      partial to the warp's row buffer; the row is written once (zeros included).
+#include <cuda_bf16.h>
+
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+__device__ __forceinline__ uint32_t lanemask_le() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_le;" : "=r"(m));
+    return m;
+}
+
+// ---- compensated segmented-scan elements ------------------------------------------------------
+// Forward element: the sum (s + c) and the valid K / Q counts of the LAST segment of the range
+// (cnt: K in bits 0..15, Q in bits 16..30), the unsegmented K / Q entry counts (allh: K in
+// 0..15, Q in 16..30) and, in allh bit 31, whether a segment (group) starts inside the range.
+struct Fwd {
+    float s, c;
+    uint32_t cnt, allh;
+};
+// Reverse element (the reversed sequence): the same sum and counts of the range's last segment
+// in reversed order, cnt bit 31 = a group's last entry lies inside the range, and tot = the
+// log-cumsum at that last entry (the group total).
+struct Bwd {
+    float s, c;
+    uint32_t cnt;
+    float tot;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// a precedes b
+__device__ __forceinline__ Fwd fcomb(const Fwd& a, const Fwd& b) {
+    const uint32_t all = (a.allh & 0x7FFFFFFFu) + (b.allh & 0x7FFFFFFFu);
+    Fwd r;
+    if (b.allh >> 31) {
+        r.s = b.s;
+        r.c = b.c;
+        r.cnt = b.cnt;
+        r.allh = all | 0x80000000u;
+    } else {
+        float err;
+        two_sum(a.s, b.s, r.s, err);
+        r.c = __fadd_rn(__fadd_rn(a.c, b.c), err);
+        r.cnt = a.cnt + b.cnt;
+        r.allh = all | (a.allh & 0x80000000u);
+    }
+    return r;
+}
+
+// A precedes B in the reversed order (A holds later positions)
+__device__ __forceinline__ Bwd bcomb(const Bwd& A, const Bwd& B) {
+    if (B.cnt >> 31) return B;
+    Bwd r;
+    float err;
+    two_sum(A.s, B.s, r.s, err);
+    r.c = __fadd_rn(__fadd_rn(A.c, B.c), err);
+    r.cnt = ((A.cnt & 0x7FFFFFFFu) + B.cnt) | (A.cnt & 0x80000000u);
+    r.tot = A.tot;
+    return r;
+}
+
+__device__ __forceinline__ Fwd shfl_up_f(const Fwd& v, int d) {
+    return {__shfl_up_sync(kFull, v.s, d), __shfl_up_sync(kFull, v.c, d), __shfl_up_sync(kFull, v.cnt, d),
+            __shfl_up_sync(kFull, v.allh, d)};
+}
+__device__ __forceinline__ Bwd shfl_down_b(const Bwd& v, int d) {
+    return {__shfl_down_sync(kFull, v.s, d), __shfl_down_sync(kFull, v.c, d), __shfl_down_sync(kFull, v.cnt, d),
+            __shfl_down_sync(kFull, v.tot, d)};
+}
+
+// Exclusive prefix (aggregate of every earlier thread) of the threads' aggregates, forward.
+// scr: 64 elements of scratch. Contains two block barriers.
+__device__ Fwd fwd_block_prefix(Fwd x, Fwd* scr, int lane, int warp, int nw) {
+    const Fwd zero = {0.f, 0.f, 0u, 0u};
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Fwd y = shfl_up_f(x, d);
+        if (lane >= d) x = fcomb(y, x);
+    }
+    if (lane == 31) scr[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        Fwd w = lane < nw ? scr[lane] : zero;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Fwd y = shfl_up_f(w, d);
+            if (lane >= d) w = fcomb(y, w);
+        }
+        Fwd ex = shfl_up_f(w, 1);
+        if (lane == 0) ex = zero;
+        if (lane < nw) scr[32 + lane] = ex;
+    }
+    __syncthreads();
+    Fwd lx = shfl_up_f(x, 1);
+    if (lane == 0) lx = zero;
+    return fcomb(scr[32 + warp], lx);
+}
+
+// Exclusive prefix in the reversed order (aggregate of every later thread).
+__device__ Bwd bwd_block_prefix(Bwd x, Bwd* scr, int lane, int warp, int nw) {
+    const Bwd zero = {0.f, 0.f, 0u, 0.f};
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Bwd y = shfl_down_b(x, d);
+        if (lane + d < 32) x = bcomb(y, x);
+    }
+    if (lane == 0) scr[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        Bwd w = lane < nw ? scr[lane] : zero;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Bwd y = shfl_down_b(w, d);
+            if (lane + d < nw) w = bcomb(y, w);
+        }
+        Bwd ex = shfl_down_b(w, 1);
+        if (lane == nw - 1) ex = zero;
+        if (lane < nw) scr[32 + lane] = ex;
+    }
+    __syncthreads();
+    Bwd lx = shfl_down_b(x, 1);
+    if (lane == 31) lx = zero;
+    return bcomb(scr[32 + warp], lx);
+}
+
+// In-place exclusive scan of cnt uint16 counters (block-wide; total < 65536).
+__device__ void block_exscan_u16(uint16_t* a, int cnt, uint32_t* scr, int lane, int warp, int nw) {
+    const int per = (cnt + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * per;
+    uint32_t s = 0;
+    for (int j = 0; j < per; ++j)
+        if (i0 + j < cnt) s += a[i0 + j];
+    uint32_t x = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) scr[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < nw ? scr[lane] : 0u;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, w, d);
+            if (lane >= d) w += y;
+        }
+        if (lane < nw) scr[32 + lane] = w - (lane < nw ? scr[lane] : 0u);
+    }
+    __syncthreads();
+    uint32_t run = scr[32 + warp] + x - s;
+    for (int j = 0; j < per; ++j) {
+        if (i0 + j < cnt) {
+            const uint32_t v = a[i0 + j];
+            a[i0 + j] = static_cast<uint16_t>(run);
+            run += v;
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void st_stream(T* p, T v) {
+    __stcs(p, v);
+}
+
+template <typename ValT>
+__global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + a.sm_keys);   // entry -> key word
+    float* const vals = reinterpret_cast<float*>(smem + a.sm_vals);        // entry -> value
+    uint16_t* const sidx = reinterpret_cast<uint16_t*>(smem + a.sm_sidx);  // sorted position -> entry
+    uint16_t* const pong = reinterpret_cast<uint16_t*>(smem + a.sm_pong);
+    uint16_t* const hist = reinterpret_cast<uint16_t*>(smem + a.sm_hist);
+    float* const lv = reinterpret_cast<float*>(smem + a.sm_lv);            // entry -> log-cumsum
+    uint32_t* const posv = reinterpret_cast<uint32_t*>(smem + a.sm_pos);   // entry -> position pack
+    uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
+    float* const rexv = reinterpret_cast<float*>(smem + a.sm_rex);         // write entry o -> rex
+    float* const cpev = reinterpret_cast<float*>(smem + a.sm_tot);         // write entry o -> cpe (value type)
+    Fwd* const fscr = reinterpret_cast<Fwd*>(smem + a.sm_scr);
+    Bwd* const bscr = reinterpret_cast<Bwd*>(smem + a.sm_scr);
+    uint32_t* const uscr = reinterpret_cast<uint32_t*>(smem + a.sm_scr + 64 * sizeof(Fwd));
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = a.nwarps, nthr = blockDim.x;
+    const int64_t c = a.c0 + blockIdx.x;
+    const int C = a.C, W = a.W, R = a.R, wr = a.wr, n = a.n, nk = a.nk, nq = a.nq, npad = a.npad;
+    const int V = c >= a.first_partial ? a.valid_last : C;
+    const uint32_t kmax = (a.key_bits >= 31) ? 0x7FFFFFFFu : ((1u << a.key_bits) - 1u);
+    const ValT* kv = static_cast<const ValT*>(a.k_val) + c * nk;
+    const ValT* qv = static_cast<const ValT*>(a.q_val) + c * nq;
+    const int32_t* kid = a.k_idx + c * nk;
+    const int32_t* qid = a.q_idx + c * nq;
+    const float* gch = a.g + c * C * a.g_width;
+
+    // ---- 0. load ------------------------------------------------------------------------------
+    bool bad = false;
+    for (int o = tid; o < nk; o += nthr) {
+        const int t = o / W, ln = o - t * W, e = t * wr + ln;
+        uint32_t key = kmax | kKeyInvalid;
+        float v = 0.f;
+        if (t < V) {
+            const int32_t id = __ldg(kid + o);
+            if (id >= 0 && static_cast<int64_t>(id) < a.S) {
+                key = static_cast<uint32_t>(id);
+                v = to_f(kv[o]);
+            } else {
+                bad = true;
+            }
+        }
+        keys[e] = key;
+        vals[e] = v;
+    }
+    for (int o = tid; o < nq; o += nthr) {
+        const int t = o / R, ln = o - t * R, e = t * wr + W + ln;
+        uint32_t key = kmax | kKeyInvalid;
+        float v = 0.f;
+        if (t < V) {
+            const int32_t id = __ldg(qid + o);
+            if (id >= 0 && static_cast<int64_t>(id) < a.S) {
+                key = static_cast<uint32_t>(id);
+                v = to_f(qv[o]);
+            } else {
+                bad = true;
+            }
+        }
+        keys[e] = key;
+        vals[e] = v;
+    }
+    for (int e = n + tid; e < npad; e += nthr) {
+        keys[e] = kmax | kKeyInvalid;
+        vals[e] = 0.f;
+    }
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
+    __syncthreads();
+
+    // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits) ---------------------
+    {
+        const uint32_t lt = lanemask_lt();
+        for (int pass = 0; pass < a.passes; ++pass) {
+            const int sh = pass * a.digit_bits;
+            const int nb = min(a.digit_bits, a.key_bits - sh);
+            const int nbins = 1 << nb;
+            const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+            // the last pass writes sidx
+            uint16_t* const dst = ((a.passes - 1 - pass) & 1) ? pong : sidx;
+            const uint16_t* const src = ((a.passes - pass) & 1) ? pong : sidx;
+            for (int i = tid; i < nbins * nw; i += nthr) hist[i] = 0;
+            __syncthreads();
+            uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 16
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int p = warp * (32 * kItems) + k * 32 + lane;
+                const uint32_t e = pass == 0 ? static_cast<uint32_t>(p) : src[p];
+                const uint32_t d = (keys[e] >> sh) & dmask;
+                const uint32_t peers = __match_any_sync(kFull, d);
+                const uint32_t rin = __popc(peers & lt);
+                uint16_t* const h = hist + d * nw + warp;
+                const uint32_t base = *h;
+                __syncwarp();
+                if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
+                __syncwarp();
+                mer[k] = e | (base + rin) << 16;
+            }
+            __syncthreads();
+            block_exscan_u16(hist, nbins * nw, uscr, lane, warp, nw);
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const uint32_t e = mer[k] & 0xFFFFu;
+                const uint32_t d = (keys[e] >> sh) & dmask;
+                dst[hist[d * nw + warp] + (mer[k] >> 16)] = static_cast<uint16_t>(e);
+            }
+            __syncthreads();
+        }
+        if (a.passes == 0) {
+            for (int p = tid; p < npad; p += nthr) sidx[p] = static_cast<uint16_t>(p);
+            __syncthreads();
+        }
+    }
+
+    // ---- 2. segmented scans over the sorted row -------------------------------------------------
+    const int r0 = tid * kItems;
+    uint32_t ke[kItems];   // entry at each of this thread's sorted positions
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) ke[k] = sidx[r0 + k];
+    auto tok_of = [&](uint32_t e) { return __umulhi(e, a.wr_magic); };
+    auto is_q_of = [&](uint32_t e) { return static_cast<int>(e - tok_of(e) * wr) >= W; };
+    // head / tail bits, gates (a token's repeated write entry of a group adds 0)
+    uint32_t headm = 0, tailm = 0;
+    float x[kItems];
+    uint32_t repc = 0;
+    {
+        uint32_t pk = kKeyInvalid, pe = 0;
+        if (r0 > 0) {
+            pe = sidx[r0 - 1];
+            pk = keys[pe];
+        }
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const uint32_t e = ke[k], key = keys[e];
+            const bool inv = key >> 31, pinv = pk >> 31;
+            const bool head = (r0 + k == 0) || inv || pinv || (key != pk);
+            headm |= (head ? 1u : 0u) << k;
+            if (k > 0) tailm |= (head ? 1u : 0u) << (k - 1);
+            const uint32_t t = tok_of(e);
+            const int j = static_cast<int>(e - t * wr);
+            const bool isq = j >= W;
+            const bool rep = !head && !isq && !is_q_of(pe) && tok_of(pe) == t;
+            repc += rep ? 1u : 0u;
+            x[k] = (!inv && !isq && !rep) ? __ldg(gch + t * a.g_width + j * a.g_lane_stride) : 0.f;
+            pk = key;
+            pe = e;
+        }
+        // the last item ends its group when the next position starts one
+        const uint32_t nkey = r0 + kItems < npad ? keys[sidx[r0 + kItems]] : kKeyInvalid;
+        const bool tail = (pk >> 31) || (nkey >> 31) || (nkey != pk);
+        tailm |= (tail ? 1u : 0u) << (kItems - 1);
+    }
+    // valid K / Q counts, and non-padding K / Q counts (kind-row indices)
+    auto cnt_of = [&](int k) -> uint32_t {
+        if (keys[ke[k]] >> 31) return 0u;
+        return is_q_of(ke[k]) ? (1u << 16) : 1u;
+    };
+    auto all_of = [&](int k) -> uint32_t {
+        if (ke[k] >= static_cast<uint32_t>(n)) return 0u;
+        return is_q_of(ke[k]) ? (1u << 16) : 1u;
+    };
+
+    // forward: inclusive log-cumsum (lv, by entry); valid K entries before (kbv); own-kind peers
+    // before and the index in the own kind's row, packed as before | index << 16 (both < 2^14), held
+    // in posv until the reverse pass replaces it with the position pack
+    {
+        Fwd agg = {0.f, 0.f, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const Fwd it = {x[k], 0.f, cnt_of(k), all_of(k) | (((headm >> k) & 1u) << 31)};
+            agg = k == 0 ? it : fcomb(agg, it);
+        }
+        Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const uint32_t ownc = cnt_of(k), owna = all_of(k);
+            const Fwd it = {x[k], 0.f, ownc, owna | (((headm >> k) & 1u) << 31)};
+            run = fcomb(run, it);
+            const float logv = __fadd_rn(run.s, run.c);
+            const uint32_t b = run.cnt - ownc;   // valid K before | valid Q before << 16
+            const uint32_t ex = (run.allh & 0x7FFFFFFFu) - owna;
+            const bool isq = is_q_of(ke[k]);
+            const uint32_t own_b = isq ? (b >> 16) : (b & 0xFFFFu);
+            const uint32_t jxv = isq ? (ex >> 16) : (ex & 0xFFFFu);
+            const uint32_t e = ke[k];
+            const bool valid = !(keys[e] >> 31);
+            posv[e] = own_b | jxv << 16;
+            lv[e] = valid ? logv : 0.f;
+            kbv[e] = static_cast<uint16_t>(valid ? (b & 0xFFFFu) : 0u);
+        }
+    }
+    __syncthreads();   // the scratch is reused by the reverse scan
+
+    // reverse: rex, peers after, group total; then every per-entry result
+    {
+        Bwd agg = {0.f, 0.f, 0u, 0.f};
+#pragma unroll
+        for (int k = kItems - 1; k >= 0; --k) {
+            const bool tail = (tailm >> k) & 1u;
+            const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
+            agg = k == kItems - 1 ? it : bcomb(agg, it);
+        }
+        Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
+        const int64_t kbase = c * nk, qbase = c * nq;
+        const int64_t tbase = c * (a.ntk + 1);
+#pragma unroll
+        for (int k = kItems - 1; k >= 0; --k) {
+            const bool tail = (tailm >> k) & 1u;
+            const Bwd ex = run;
+            const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
+            run = bcomb(run, it);
+            const uint32_t e = ke[k];
+            if (e >= static_cast<uint32_t>(n)) continue;
+            const int r = r0 + k;
+            const uint32_t key = keys[e];
+            const bool valid = !(key >> 31);
+            const uint32_t t = tok_of(e);
+            const int j = static_cast<int>(e - t * wr);
+            const bool isq = j >= W;
+            const int ln = isq ? j - W : j;
+            const uint32_t acnt = tail ? 0u : (ex.cnt & 0x7FFFFFFFu);
+            const uint32_t after = isq ? (acnt >> 16) : (acnt & 0xFFFFu);
+            const uint32_t bjv = posv[e];
+            const uint32_t before = bjv & 0xFFFFu;
+            const uint32_t jx = bjv >> 16;
+            const uint32_t asat = min(after, kPosCountMax);
+            const uint32_t pack = valid ? (static_cast<uint32_t>(r) | asat << kPosAfterShift |
+                                           min(before + 1u + asat, kPosCountMax) << kPosSizeShift)
+                                        : static_cast<uint32_t>(r);
+            posv[e] = pack;
+            const uint32_t payload = t << kTokenShift | (isq ? kIsQBit : 0u) | static_cast<uint32_t>(ln) |
+                                     (valid ? 0u : kInvalidBit);
+            const uint32_t el = (payload & kEntryMask) |
+                                (valid ? (min(before, kDistMax) << kDistShift | (before == 0 ? kFirst : 0u) |
+                                          (after == 0 ? kLast : 0u))
+                                       : (kFirst | kLast));
+            if (isq) {
+                if (a.out.sorted_q != nullptr) st_stream(a.out.sorted_q + qbase + jx, static_cast<int32_t>(el));
+            } else {
+                const int o = static_cast<int>(t) * W + ln;
+                const float rex = (valid && !tail) ? __fadd_rn(ex.s, ex.c) : 0.f;
+                const float cpe_f = valid ? to_f(from_f<ValT>(expf(run.tot))) : 1.0f;
+                rexv[o] = rex;
+                cpev[o] = cpe_f;
+                const float sc = valid ? __fmul_rn(vals[e], expf(rex)) : 0.f;
+                const uint32_t w0 = t | (valid ? ((before == 0 ? kFirst : 0u) | (after == 0 ? kLast : 0u))
+                                              : (kFirst | kLast | kRecInvalid));
+                const uint32_t slot = valid ? (key & 0x7FFFFFFFu) : 0u;
+                st_stream(a.krec + kbase + jx, make_int4(static_cast<int>(w0), static_cast<int>(slot),
+                                                         __float_as_int(sc), __float_as_int(cpe_f)));
+                if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
+                if (jx % static_cast<uint32_t>(a.L) == 0u) {
+                    const int first = (!valid || before == 0) ? static_cast<int>(jx) : static_cast<int>(jx + after + 1u);
+                    a.tb[tbase + jx / a.L] = first;
+                }
+            }
+        }
+        if (tid == 0) a.tb[tbase + a.ntk] = nk;
+    }
+    if (a.out.repeats != nullptr) {
+        const uint32_t wsum = __reduce_add_sync(kFull, repc);
+        if (lane == 0 && wsum != 0u)
+            atomicAdd(reinterpret_cast<unsigned long long*>(a.out.repeats), static_cast<unsigned long long>(wsum));
+    }
+    __syncthreads();
+
+    // ---- 3. entry-order outputs -------------------------------------------------------------------
+    {
+        const int64_t kbase = c * nk;
+        ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
+        ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);
+        for (int o = tid; o < nk; o += nthr) {
+            const int t = o / W, e = t * wr + (o - t * W);
+            const uint32_t pk = posv[e];
+            const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
+            const bool valid = size != 0u;
+            const float lg = lv[e];
+            if (a.out.log_k) st_stream(a.out.log_k + kbase + o, lg);
+            if (a.out.rex) st_stream(a.out.rex + kbase + o, rexv[o]);
+            if (cpe_o) st_stream(cpe_o + kbase + o, from_f<ValT>(cpev[o]));
+            if (keff_o) st_stream(keff_o + kbase + o, from_f<ValT>(valid ? vals[e] * expf(lg) : 0.f));
+            if (a.out.is_last)
+                st_stream(a.out.is_last + kbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
+            if (a.out.is_only) st_stream(a.out.is_only + kbase + o, static_cast<int8_t>(size == 1u));
+            if (a.out.pos_k) st_stream(a.out.pos_k + kbase + o, static_cast<int32_t>(pk));
+        }
+        const int64_t qbase = c * nq;
+        ValT* const qw_o = static_cast<ValT*>(a.out.q_w);
+        for (int o = tid; o < nq; o += nthr) {
+            const int t = o / R, e = t * wr + W + (o - t * R);
+            const uint32_t pk = posv[e];
+            const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
+            const bool valid = size != 0u;
+            const float lg = lv[e];
+            if (a.out.log_q) st_stream(a.out.log_q + qbase + o, lg);
+            if (qw_o) st_stream(qw_o + qbase + o, from_f<ValT>(valid ? vals[e] * expf(lg) : 0.f));
+            if (a.out.q_last)
+                st_stream(a.out.q_last + qbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
+            if (a.out.q_only) st_stream(a.out.q_only + qbase + o, static_cast<int8_t>(size == 1u));
+            if (a.out.pos_q) st_stream(a.out.pos_q + qbase + o, static_cast<int32_t>(pk));
+        }
+    }
+
+    // ---- 4. pair triangles --------------------------------------------------------------------------
+    if (a.out.A == nullptr && a.out.QK == nullptr) return;
+    __syncthreads();   // the key array becomes the row buffers
+    float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
+    const uint32_t le = lanemask_le();
+    const bool vec4 = (C % 4) == 0;
+    for (int u = warp; u < 2 * C; u += nw) {
+        const int i = u >> 1;
+        const bool qk = u & 1;
+        float* const outp = qk ? a.out.QK : a.out.A;
+        if (outp == nullptr) continue;
+        bool any = false;
+        const int lanes = qk ? R : W;
+        if (i < V) {
+            for (int ab = 0; ab < lanes; ++ab) {
+                const int e = i * wr + (qk ? W + ab : ab);
+                const uint32_t kb = kbv[e];
+                if (kb == 0u) continue;   // no earlier write entry in its group: no term
+                if (!any) {
+                    for (int j = lane; j < C; j += 32) rowbuf[j] = 0.f;
+                    __syncwarp();
+                    any = true;
+                }
+                const int r = static_cast<int>(posv[e] & kPosMask);
+                const float ve = vals[e], lge = lv[e];
+                uint32_t met = 0;
+                for (int top = r - 1; met < kb && top >= 0; top -= 32) {
+                    const int p = top - lane;
+                    const bool in = p >= 0;
+                    uint32_t f = 0;
+                    bool isk = false;
+                    if (in) {
+                        f = sidx[p];
+                        isk = f < static_cast<uint32_t>(n) && !is_q_of(f) &&
+                              ((posv[f] >> kPosSizeShift) & kPosCountMax) != 0u;
+                    }
+                    const uint32_t bk = __ballot_sync(kFull, isk);
+                    const uint32_t before_me = __popc(bk & le) - (isk ? 1u : 0u);
+                    const bool incl = in && (met + before_me < kb);
+                    const int tf = incl ? static_cast<int>(tok_of(f)) : -1;
+                    float v = 0.f;
+                    if (incl && isk && (qk || tf != i)) {
+                        v = __fmul_rn(__fmul_rn(ve, vals[f]), expf(__fsub_rn(lge, lv[f])));
+                    }
+                    // segmented suffix sums over lanes of equal token (tokens are non-increasing
+                    // along the lanes): a fixed shuffle tree
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const float ov = __shfl_down_sync(kFull, v, d);
+                        const int ot = __shfl_down_sync(kFull, tf, d);
+                        if (lane + d < 32 && ot == tf) v = __fadd_rn(v, ov);
+                    }
+                    const int tprev = __shfl_up_sync(kFull, tf, 1);
+                    if (tf >= 0 && (lane == 0 || tprev != tf)) rowbuf[tf] = __fadd_rn(rowbuf[tf], v);
+                    __syncwarp();
+                    met += __popc(bk);
+                }
+            }
+        }
+        float* const row = outp + (c * C + i) * static_cast<int64_t>(C);
+        if (vec4) {
+            for (int j = lane * 4; j < C; j += 128) {
+                float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (any) w = *reinterpret_cast<const float4*>(rowbuf + j);
+                __stcs(reinterpret_cast<float4*>(row + j), w);
+            }
+        } else {
+            for (int j = lane; j < C; j += 32) __stcs(row + j, any ? rowbuf[j] : 0.f);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_phase1(const P1Args& a, int val_bf16, int64_t nchunks, int threads, size_t smem,
+                          cudaStream_t stream) {
+    if (nchunks <= 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(nchunks));
+    if (val_bf16) {
+        cudaError_t e = cudaFuncSetAttribute(p1_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        p1_kernel<__nv_bfloat16><<<grid, threads, smem, stream>>>(a);
+    } else {
+        cudaError_t e = cudaFuncSetAttribute(p1_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        p1_kernel<float><<<grid, threads, smem, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t phase1_smem_limit(int device, size_t* bytes) {
+    int v = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return e;
+    *bytes = static_cast<size_t>(v);
+    return cudaSuccess;
+}
+
+}  // namespace sdm

@@ -1,0 +1,101 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function include/sdm.h
+declares, sizes workspaces, and rejects bad arguments before any CUDA call (no launches here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_slot_memory_gb300 as sdm
+from sparse_slot_memory_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sdm.build()
+    import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+    return _abi.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sdm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(_abi.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def shape(**kw):
+    base = dict(P=32, C=256, W=16, R=16, hd=128, valid_last=256, steps=32, S=1 << 20, val_dtype=1, dv_dtype=1,
+                bank_dtype=1, gate_per_entry=0)
+    base.update(kw)
+    return _abi.Shape(**base)
+
+
+def test_workspace_bytes(lib):
+    n = lib.sdm_workspace_bytes(ctypes.byref(shape()))
+    # DW records (16 B per write entry) dominate
+    assert n >= 1024 * 4096 * 16
+    assert lib.sdm_workspace_bytes(ctypes.byref(shape(C=257))) == 0
+    assert lib.sdm_workspace_bytes(ctypes.byref(shape(W=17, R=16))) == 0   # C * (W + R) > 8192
+    assert lib.sdm_workspace_bytes(ctypes.byref(shape(hd=6))) == 0
+    assert lib.sdm_workspace_bytes(None) == 0
+
+
+FAKE = 0x100000  # never dereferenced: every case fails a host check first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(C=0), -2), (dict(C=300), -2), (dict(W=0), -2), (dict(R=300), -2), (dict(W=20, R=20), -2),
+    (dict(valid_last=0), -2), (dict(valid_last=257), -2), (dict(steps=0), -2), (dict(S=0), -2),
+    (dict(S=1 << 31), -2), (dict(val_dtype=7), -3), (dict(bank_dtype=-1), -3), (dict(hd=126), -4),
+    (dict(gate_per_entry=2), -2),
+])
+def test_shape_errors(lib, kw, code):
+    st = lib.sdm_phase1(ctypes.byref(shape(**kw)), FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE, 1 << 40, None)
+    assert st == code
+    st = lib.sdm_dw(ctypes.byref(shape(**kw)), FAKE, FAKE, 0, 1, FAKE, 1 << 40, None)
+    assert st == code
+
+
+def test_argument_errors(lib):
+    s = ctypes.byref(shape())
+    assert lib.sdm_phase1(s, None, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE, 1 << 40, None) == -1
+    assert lib.sdm_phase1(s, FAKE + 4, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE, 1 << 40, None) == -4
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 1, FAKE, 1 << 40, None) == -1
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 33, FAKE, 1 << 40, None) == -1
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE, 1024, None) == -5
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE + 16, 1 << 40, None) == -5
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, None, 1 << 40, None) == -5
+    out = _abi.P1Out()
+    out.A = FAKE + 8
+    assert lib.sdm_phase1(s, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(out), 0, 1, FAKE, 1 << 40, None) == -4
+    assert lib.sdm_dw(s, None, FAKE, 0, 1, FAKE, 1 << 40, None) == -1
+    assert lib.sdm_dw(s, FAKE, FAKE + 2, 0, 1, FAKE, 1 << 40, None) == -4
+    assert lib.sdm_forward_chunks(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0, 1, FAKE, 1 << 40,
+                                  None) == -1
+    code = ctypes.c_int32(0)
+    assert lib.sdm_device_status(None, ctypes.byref(code), 0, None) == -1
+    assert lib.sdm_workspace_init(FAKE + 8, 4096, None) == -5
+
+
+def test_status_strings(lib):
+    for c in range(-8, 1):
+        s = lib.sdm_status_string(c).decode()
+        assert s.startswith("SDM_")
+    assert "unknown" in lib.sdm_status_string(5).decode()
+
+
+def test_no_cpu_path_for_host_tensors():
+    import torch
+    spec = sdm.ShapeSpec(P=1, C=4, W=1, R=1, hd=4, steps=1, S=8, valid_last=4)
+    with pytest.raises(TypeError):
+        sdm.dw(spec, torch.zeros(4, 4), torch.zeros(8, 4), torch.zeros(1 << 16, dtype=torch.uint8))

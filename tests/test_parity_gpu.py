@@ -1,0 +1,234 @@
+"""GPU parity of Phase 1 and DW against the float64 oracle, through the C ABI.
+
+Workloads are the five synthetic workloads at sizes the oracle finishes in seconds (several
+tiles, ragged tails), plus degenerate chunks (one slot for a whole chunk: 127 / 4095
+saturations; tiny chunks; a single column). Full-size runs are in test_fullsize_gpu.py.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_slot_memory_gb300 as sdm
+from sdm_testlib import bank_tolerance_ok, compare_p1, host, inputs_to_dev, oracle_p1, run_phase1, ulp_bf16
+from synth import WORKLOADS, bf16_bits_to_f32, make_bank_stream, make_inputs, scaled
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny": WORKLOADS["tiny"],
+    "uniform_c128": scaled(WORKLOADS["uniform_c128"], P=2, T=1024),
+    "zipf_c256": scaled(WORKLOADS["zipf_c256"], P=2, T=1024),
+    "large": scaled(WORKLOADS["large"], P=2, T=1024),
+    "wide_ragged": scaled(WORKLOADS["wide_ragged"], P=2, T=300),
+    "one_slot": scaled(WORKLOADS["large"], P=1, T=512, S=1, hd=8, name="one_slot"),
+    "few_slots": scaled(WORKLOADS["tiny"], P=3, T=200, C=64, S=8, hd=16, W=5, R=3, name="few_slots"),
+    "c1_w1_r1": scaled(WORKLOADS["tiny"], P=3, T=5, C=1, S=16, hd=4, W=1, R=1, name="c1_w1_r1"),
+    "bf16_hd4_ragged": scaled(WORKLOADS["uniform_c128"], P=2, T=100, C=48, S=64, hd=4, W=3, R=7,
+                              name="bf16_hd4_ragged"),
+}
+
+
+def _setup(name):
+    w = CASES[name]
+    x = make_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+    d = inputs_to_dev(x, w)
+    ws = sdm.alloc_workspace(shape)
+    return w, x, shape, d, ws
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_phase1_parity(name):
+    w, x, shape, d, ws = _setup(name)
+    out = run_phase1(shape, d, ws)
+    assert sdm.device_status(ws) == 0
+    orc, lo, hi = oracle_p1(x, w)
+    rep = compare_p1(out, orc, lo, hi, w.val_dtype)
+    assert int(out["repeats"][0]) == orc["repeats"]
+    print(name, rep)
+
+
+def _init_bank(w, P):
+    """Initial bank rows of every stream as float32 [P, S, hd] (exact for either bank type)."""
+    rows = []
+    for p in range(P):
+        b = make_bank_stream(w, p)
+        rows.append(bf16_bits_to_f32(b) if w.bank_dtype == "bf16" else b)
+    return np.stack(rows, 0)
+
+
+def _bank_dev(rows64: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(rows64, np.float32)).cuda()
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+def _stream_compact(w, x, p):
+    """The slots stream p touches, and its chunks' ids relabelled to [0, U) by rank (a monotone
+    relabelling keeps every sort order and group, so the oracle can run on U rows)."""
+    P = x["P"]
+    cs = [ti * P + p for ti in range(w.steps)]
+    kk, qq = x["k_idx"][cs], x["q_idx"][cs]
+    ids = np.concatenate([kk.ravel(), qq.ravel()])
+    slots = np.unique(ids[(ids >= 0) & (ids < w.S)])
+
+    def remap(a):
+        r = np.searchsorted(slots, a)
+        return np.where((a >= 0) & (a < w.S), r, a).astype(np.int32)
+
+    xs = dict(x)
+    xs["k_idx"], xs["q_idx"] = x["k_idx"].copy(), x["q_idx"].copy()
+    xs["k_idx"][cs], xs["q_idx"][cs] = remap(kk), remap(qq)
+    return slots, xs
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_dw_parity_stepwise(name):
+    """Each step from the oracle's own pre-step rows (copied into the GPU bank first): every
+    touched row within tolerance, every other row bitwise unchanged."""
+    w, x, shape, d, ws = _setup(name)
+    run_phase1(shape, d, ws, fields=("repeats",))
+    P, S, hd, C = x["P"], w.S, w.hd, w.C
+    init = _init_bank(w, P)
+    gpu_bank = _bank_dev(init.reshape(P * S, hd), w.bank_dtype)
+    comp = [_stream_compact(w, x, p) for p in range(P)]
+    banks = [init[p][comp[p][0]].astype(np.float64) for p in range(P)]    # oracle state on the touched slots
+    rng = np.random.default_rng(0)
+    for ti in range(w.steps):
+        for p in range(P):
+            rows = torch.from_numpy(p * S + comp[p][0]).cuda()
+            gpu_bank.index_copy_(0, rows, _bank_dev(banks[p], w.bank_dtype))
+        snapshot = gpu_bank.clone()
+        sdm.dw(shape, d["dv"], gpu_bank, ws, ti, ti + 1)
+        torch.cuda.synchronize()
+        assert sdm.device_status(ws) == 0
+        changed = (gpu_bank != snapshot).any(dim=1).cpu().numpy()
+        for p in range(P):
+            slots, xs = comp[p]
+            U = len(slots)
+            before = banks[p].copy()
+            alt = banks[p].copy()
+            amb = np.zeros(U, np.int32)
+            touched = np.zeros(U, np.int32)
+            mag = np.zeros_like(banks[p])
+            c = ti * P + p
+            V = w.valid_last if ti == w.steps - 1 else C
+            dvr = oracle.as_f64(x["dv"][c * C:(c + 1) * C], w.dv_dtype)
+            oracle.dw_chunk(banks[p], xs["k_idx"][c], xs["q_idx"][c], x["k_val"][c], x["q_val"][c], x["g"][c], dvr,
+                            S=U, V=V, val_dtype=w.val_dtype, bank_dtype=w.bank_dtype, alt=alt, amb=amb,
+                            touched=touched, mag=mag)
+            got = host(gpu_bank[torch.from_numpy(p * S + slots).cuda()]).astype(np.float64)
+            t = touched > 0
+            assert np.array_equal(got[~t], before[~t]), f"step {ti} stream {p}: an untouched row changed"
+            ok = bank_tolerance_ok(got[t], banks[p][t], np.where(amb[t, None] > 0, alt[t], np.nan), mag[t],
+                                   w.bank_dtype)
+            assert ok.all(), (f"step {ti} stream {p}: {int((~ok).sum())} bank elements beyond tolerance; "
+                              f"first gpu {got[t][~ok][0]} oracle {banks[p][t][~ok][0]}")
+            # rows of the stream that no entry names are never written
+            others = np.setdiff1d(rng.integers(0, S, size=min(S, 4096)), slots)
+            assert not changed[p * S + others].any()
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform_c128", "zipf_c256", "wide_ragged", "few_slots", "large"])
+def test_forward_end_to_end(name):
+    """sdm_forward_chunks over every step vs the oracle run step after step in its own state.
+    A difference of one rounding can carry into a row's later writes: a row written k times is
+    allowed k times the one-step tolerance."""
+    w, x, shape, d, ws = _setup(name)
+    P, S, hd = x["P"], w.S, w.hd
+    init = _init_bank(w, P)
+    gpu_bank = _bank_dev(init.reshape(P * S, hd), w.bank_dtype)
+    out = sdm.alloc_outputs(shape)
+    sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], gpu_bank, out, ws)
+    torch.cuda.synchronize()
+    assert sdm.device_status(ws) == 0
+    orc, lo, hi = oracle_p1(x, w)
+    compare_p1(out, orc, lo, hi, w.val_dtype)
+    worst, over1 = 0.0, 0
+    for p in range(P):
+        slots, xs = _stream_compact(w, x, p)
+        bank = init[p][slots].astype(np.float64)
+        alt, amb, touched, mag = oracle.dw_stream(bank, xs, p, S=len(slots), C=w.C, P=P, steps=w.steps,
+                                                  valid_last=w.valid_last, val_dtype=w.val_dtype,
+                                                  dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype, track=True)
+        got = host(gpu_bank[torch.from_numpy(p * S + slots).cuda()]).astype(np.float64)
+        t = touched > 0
+        assert np.array_equal(got[~t], init[p][slots][~t])
+        k = touched[t][:, None].astype(np.float64)
+        dlt = np.abs(got[t] - bank[t])
+        dla = np.abs(got[t] - alt[t])
+        if w.bank_dtype == "bf16":
+            u = ulp_bf16(bank[t])
+            tol = k * (u + 2.0 ** -17 * mag[t])
+            worst = max(worst, float(np.max(dlt / u)) if dlt.size else 0.0)
+            over1 += int((dlt > u).sum())
+        else:
+            tol = k * (1e-5 * mag[t] + 1e-30)
+        ok = (dlt <= tol) | ((amb[t, None] > 0) & (dla <= tol))
+        assert ok.all(), f"stream {p}: {int((~ok).sum())} elements beyond tolerance"
+    print(name, "bank: max ulp", worst, "elements > 1 ulp", over1)
+
+
+@pytest.mark.parametrize("name", ["uniform_c128", "zipf_c256", "wide_ragged", "large"])
+def test_resume_and_determinism(name):
+    """[0, k) then [k, steps) equals [0, steps) bit for bit; repeated runs are bitwise identical."""
+    w, x, shape, d, ws = _setup(name)
+    P = x["P"]
+    init = _init_bank(w, P).reshape(P * w.S, w.hd)
+    results = []
+    for split in (None, None, None, max(1, w.steps // 2)):
+        bank = _bank_dev(init, w.bank_dtype)
+        out = sdm.alloc_outputs(shape)
+        if split is None:
+            sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws)
+        else:
+            sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws,
+                               0, split)
+            sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws,
+                               split, w.steps)
+        torch.cuda.synchronize()
+        out["repeats"].zero_()
+        results.append({"bank": bank.view(torch.int16 if w.bank_dtype == "bf16" else torch.int32).cpu().numpy(),
+                        **{k: v.view(torch.uint8).cpu().numpy() for k, v in out.items()}})
+    for r in results[1:]:
+        for k in r:
+            assert np.array_equal(r[k], results[0][k]), f"{k} differs between runs"
+
+
+def test_bad_slot_sets_status_without_fault():
+    w = scaled(WORKLOADS["tiny"], P=1, T=128, name="bad")
+    x = make_inputs(w)
+    x["k_idx"][1, 3, 2] = w.S + 5      # out of range
+    x["q_idx"][0, 0, 0] = -7
+    shape = sdm.ShapeSpec.from_workload(w)
+    d = inputs_to_dev(x, w)
+    ws = sdm.alloc_workspace(shape)
+    bank = torch.zeros(w.P * w.S, w.hd, device="cuda")
+    sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, None, ws)
+    code = sdm.device_status(ws, clear=True)
+    assert code & 0x1
+    assert sdm.device_status(ws) == 0   # cleared
+    assert torch.isfinite(bank).all()
+
+
+def test_empty_range_is_noop():
+    w, x, shape, d, ws = _setup("tiny")
+    bank = torch.ones(w.P * w.S, w.hd, device="cuda")
+    sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, None, ws, 3, 3)
+    torch.cuda.synchronize()
+    assert bool((bank == 1).all())
+
+
+def test_host_checks_before_launch():
+    w, x, shape, d, ws = _setup("tiny")
+    bank = torch.zeros(w.P * w.S, w.hd, device="cuda")
+    with pytest.raises(sdm.SdmError) as e:
+        sdm.dw(shape, d["dv"], bank, ws[:1024], 0, 1)
+    assert e.value.status == -5
+    with pytest.raises(sdm.SdmError) as e:
+        sdm.dw(shape, d["dv"], bank.view(-1)[1:1 + w.P * w.S * w.hd - 64].view(-1, w.hd), ws, 0, 1)
+    assert e.value.status == -4
+    with pytest.raises(sdm.SdmError) as e:
+        sdm.dw(shape, d["dv"], bank, ws, 2, 1)
+    assert e.value.status == -1
