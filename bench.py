@@ -30,7 +30,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synth import WORKLOADS, make_inputs  # noqa: E402
+from synth import WORKLOADS, make_inputs, scaled  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 
@@ -154,6 +154,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     sdm.build()
     w = WORKLOADS[args.workload]
+    if args.streams:
+        w = scaled(w, P=args.streams)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -359,6 +361,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--streams", type=int, default=0, help="override the workload's stream count (profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

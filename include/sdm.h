@@ -29,8 +29,9 @@
  *   - Limits: 1 <= C <= 256, 1 <= W, R <= 256, C * (W + R) <= 8192 (one chunk sorts on chip),
  *     1 <= S <= 2^31 - 1, P * S * hd fits in int64.
  *   - Shape, dtype, alignment and workspace errors are returned BEFORE any launch. Errors the
- *     device finds (a valid slot id outside [0, S), a bounded wait that ran out) are OR-ed into
- *     a status word inside the workspace; read it with sdm_device_status. No kernel traps.
+ *     device finds (a valid slot id outside [0, S)) are OR-ed into a status word inside the
+ *     workspace; read it with sdm_device_status. No kernel traps, and no kernel waits on another
+ *     thread block.
  *   - Determinism: for fixed inputs, shapes and GPU type every output is bitwise reproducible.
  *     The sort is stable, scans combine in a fixed tree, every A/QK cell and every bank row has
  *     one writer that adds its terms in an input-determined order, and no atomics touch a sum.
@@ -50,7 +51,7 @@ typedef struct CUstream_st* sdm_stream_t;
 
 typedef enum {
     SDM_OK = 0,
-    SDM_ERR_ARG = -1,       /* a required pointer is NULL, or a step range is empty / out of range */
+    SDM_ERR_ARG = -1,       /* a required pointer is NULL, or a step range is reversed / out of range */
     SDM_ERR_SHAPE = -2,     /* a size is outside the limits above */
     SDM_ERR_DTYPE = -3,     /* an unknown dtype code */
     SDM_ERR_ALIGN = -4,     /* a pointer is not 16-byte aligned, or hd % 4 != 0 */
@@ -64,7 +65,6 @@ typedef enum { SDM_F32 = 0, SDM_BF16 = 1 } sdm_dtype;
 
 /* Bits of the device status word (sdm_device_status). */
 #define SDM_DEV_BAD_SLOT 0x1u /* a valid entry's slot id was outside [0, S): the entry is dropped */
-#define SDM_DEV_TIMEOUT 0x2u  /* a bounded wait of the DW kernel ran out: the bank is undefined */
 
 typedef struct {
     int32_t P;              /* streams */
@@ -122,13 +122,15 @@ typedef struct {
 } sdm_p1_out;
 
 /*
- * Bytes of the caller-allocated device workspace for this shape (DW records of every chunk,
- * tile bounds, counters and the status word). The workspace must be 256-byte aligned and, before
- * its first use, zeroed with sdm_workspace_init. Returns 0 for an invalid shape.
+ * Bytes of the caller-allocated device workspace for this shape: a 256-byte header (status word,
+ * DW work counter), the DW records of every chunk (16 bytes per write entry) and the per-chunk
+ * slot-bucket bounds of the DW work split. The workspace must be 256-byte aligned and, before its
+ * first use, initialised with sdm_workspace_init. One workspace serves one stream of calls at a
+ * time. Returns 0 for an invalid shape.
  */
 size_t sdm_workspace_bytes(const sdm_shape* shape);
 
-/* Zeroes the workspace's header (status word and counters) on `stream`. */
+/* Zeroes the workspace's header (status word and work counter) on `stream`. */
 sdm_status sdm_workspace_init(void* ws, size_t ws_bytes, sdm_stream_t stream);
 
 /*
@@ -146,8 +148,8 @@ sdm_status sdm_phase1(const sdm_shape* shape, const int32_t* k_idx, const int32_
  * for those steps: per slot group of each chunk, bank[p*S + s] = fma(base, cpe_last, acc),
  * acc = fma(sc_m, dv[tok_m], acc) over the group's write entries in sorted order starting at 0,
  * sc = f32(k) * expf(rex), base = the row before this step (stored RN in bfloat16, or as the f32
- * result). One persistent kernel runs every step; a step of stream p starts once the previous
- * step of p has finished (per-stream counters in `ws`, bounded waits).
+ * result). One launch runs every step: each warp owns a range of slots of one stream and applies
+ * the range's groups of all steps in order, so no warp ever waits for another.
  */
 sdm_status sdm_dw(const sdm_shape* shape, const void* dv, void* bank, int64_t step_begin,
                   int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);

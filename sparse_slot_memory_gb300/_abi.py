@@ -11,7 +11,7 @@ c_i32, c_i64, c_p, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctype
 
 SDM_OK = 0
 SDM_F32, SDM_BF16 = 0, 1
-SDM_DEV_BAD_SLOT, SDM_DEV_TIMEOUT = 0x1, 0x2
+SDM_DEV_BAD_SLOT = 0x1
 
 # every symbol include/sdm.h declares
 EXPORTS = ("sdm_workspace_bytes", "sdm_workspace_init", "sdm_phase1", "sdm_dw", "sdm_forward_chunks",

@@ -8,15 +8,10 @@
 namespace sdm {
 namespace {
 
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per bounded wait
+ // DW work items (stream, slot bucket, column slice) aimed at per launch: ~3x the warps a GB300 holds.
+constexpr int64_t kDwTargetItems = 16384;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-int prev_pow2(int x) {
-    int p = 1;
-    while (p * 2 <= x) p *= 2;
-    return p;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -61,16 +56,17 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->threads = threads;
     g->npad = threads * kItems;
     g->nwarps = threads / 32;
-    int L = prev_pow2(g->nk / 256 > 1 ? g->nk / 256 : 1);
-    L = L < 8 ? 8 : (L > 128 ? 128 : L);
-    g->L = L;
-    g->ntk = (g->nk + L - 1) / L;
     g->nsl = (s->hd + 127) / 128;
-    // workspace
-    g->hdr_bytes = kHdrCounters + round_up(8 * static_cast<size_t>(s->P), 256);
-    g->krec_off = g->hdr_bytes;
-    g->tb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->nk * sizeof(int4), 256);
-    g->ws_bytes = g->tb_off + round_up(static_cast<size_t>(N) * (g->ntk + 1) * sizeof(int32_t), 256);
+    // DW slot buckets: 2^bshift consecutive slots each, about kDwTargetItems items per launch
+    int64_t want = kDwTargetItems / (static_cast<int64_t>(s->P) * g->nsl);
+    int lb = 0;
+    while ((int64_t(1) << lb) < want) ++lb;
+    g->bshift = kb > lb ? kb - lb : 0;
+    g->B = static_cast<int>((s->S + (int64_t(1) << g->bshift) - 1) >> g->bshift);
+    // workspace: header | DW records [N, C*W] | bucket bounds [P, B + 1, steps]
+    g->krec_off = kHdrBytes;
+    g->bb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->nk * sizeof(int4), 256);
+    g->ws_bytes = g->bb_off + round_up(static_cast<size_t>(s->P) * (g->B + 1) * s->steps * sizeof(int32_t), 256);
     // Phase-1 shared memory: keys | vals | sidx | (pong + hist) or log-cumsums | pos | kb | rex | cpe | scratch
     const size_t np = static_cast<size_t>(g->npad);
     size_t off = 0;
@@ -91,6 +87,8 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->sm_rex = off;
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_tot = off;
+    off += round_up(static_cast<size_t>(g->nk) * 4, 16);
+    g->sm_kslot = off;
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_scr = off;
     off += 64 * 16 + 64 * 4;
@@ -121,7 +119,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     if (out != nullptr) a.out = *out;
     unsigned char* const w = static_cast<unsigned char*>(ws);
     a.krec = reinterpret_cast<int4*>(w + g.krec_off);
-    a.tb = reinterpret_cast<int32_t*>(w + g.tb_off);
+    a.bb = reinterpret_cast<int32_t*>(w + g.bb_off);
     a.status = reinterpret_cast<uint32_t*>(w + kHdrStatus);
     a.C = g.C;
     a.W = g.W;
@@ -142,8 +140,10 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.g_width = s->gate_per_entry ? g.W : 1;
     a.g_lane_stride = s->gate_per_entry ? 1 : 0;
     a.wr_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.wr - 1) / g.wr);
-    a.L = g.L;
-    a.ntk = g.ntk;
+    a.P = g.P;
+    a.B = g.B;
+    a.bshift = g.bshift;
+    a.steps = g.steps;
     a.sm_keys = static_cast<uint32_t>(g.sm_keys);
     a.sm_vals = static_cast<uint32_t>(g.sm_vals);
     a.sm_sidx = static_cast<uint32_t>(g.sm_sidx);
@@ -154,6 +154,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_kb = static_cast<uint32_t>(g.sm_kb);
     a.sm_rex = static_cast<uint32_t>(g.sm_rex);
     a.sm_tot = static_cast<uint32_t>(g.sm_tot);
+    a.sm_kslot = static_cast<uint32_t>(g.sm_kslot);
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
     const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
@@ -162,29 +163,26 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
 sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* bank, int64_t b, int64_t e, void* ws,
                   cudaStream_t stream) {
     unsigned char* const w = static_cast<unsigned char*>(ws);
-    // DW counters and the abort flag start at zero for every launch (the status word is kept)
-    if (cudaMemsetAsync(w + kHdrAbort, 0, g.hdr_bytes - kHdrAbort, stream) != cudaSuccess) return SDM_ERR_CUDA;
+    // the work counter starts at zero for every launch (the status word is kept)
+    if (cudaMemsetAsync(w + kHdrClaim, 0, sizeof(uint32_t), stream) != cudaSuccess) return SDM_ERR_CUDA;
     DWArgs a;
     memset(&a, 0, sizeof(a));
     a.krec = reinterpret_cast<const int4*>(w + g.krec_off);
-    a.tb = reinterpret_cast<const int32_t*>(w + g.tb_off);
+    a.bb = reinterpret_cast<const int32_t*>(w + g.bb_off);
     a.dv = dv;
     a.bank = bank;
-    a.status = reinterpret_cast<uint32_t*>(w + kHdrStatus);
-    a.abort_flag = reinterpret_cast<uint32_t*>(w + kHdrAbort);
-    a.claim = reinterpret_cast<uint32_t*>(w + kHdrCounters);
-    a.done = a.claim + g.P;
+    a.claim = reinterpret_cast<uint32_t*>(w + kHdrClaim);
     a.P = g.P;
     a.C = g.C;
     a.nk = g.nk;
-    a.ntk = g.ntk;
+    a.B = g.B;
     a.nsl = g.nsl;
     a.hd = g.hd;
     a.S = g.S;
+    a.steps = g.steps;
     a.step_begin = b;
-    a.per_step = static_cast<int64_t>(g.ntk) * g.nsl;
-    a.per_stream = (e - b) * a.per_step;
-    a.timeout_ns = kWaitTimeoutNs;
+    a.step_end = e;
+    a.items = static_cast<int64_t>(g.P) * g.B * g.nsl;
     const cudaError_t err = launch_dw(a, s->dv_dtype == SDM_BF16, s->bank_dtype == SDM_BF16, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
 }
@@ -225,10 +223,10 @@ extern "C" size_t sdm_workspace_bytes(const sdm_shape* shape) {
 }
 
 extern "C" sdm_status sdm_workspace_init(void* ws, size_t ws_bytes, sdm_stream_t stream) {
-    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < kHdrCounters)
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < kHdrBytes)
         return SDM_ERR_WORKSPACE;
-    return cudaMemsetAsync(ws, 0, kHdrCounters, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SDM_OK
-                                                                                                        : SDM_ERR_CUDA;
+    return cudaMemsetAsync(ws, 0, kHdrBytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SDM_OK
+                                                                                                    : SDM_ERR_CUDA;
 }
 
 extern "C" sdm_status sdm_phase1(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,

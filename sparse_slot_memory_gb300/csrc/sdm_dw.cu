@@ -5,19 +5,20 @@
 //   acc = 0; acc = fmaf(sc_m, dv[tok_m], acc) over the group's write entries;
 //   bank[slot] = RN(fmaf(base, cpe_last, acc)), base = the row before this step,
 // sc = k * expf(rex) and cpe_last (the value-type cpe widened) come from the Phase-1 record.
-// A float32 bank stores the fmaf result itself. Every group is summed by one warp in sorted
-// order and its row has one writer per step, so the result does not depend on the tiling.
+// A float32 bank stores the fmaf result itself. Steps apply in order.
 //
-// GB300 design: ONE persistent launch runs every step. Work items are (stream p, step, tile,
-// 128-column slice); each stream has its own claim counter, items are claimed in (step, tile,
-// slice) order, and an item of step t waits (bounded) until stream p's per-stream done counter
-// shows every item of step t-1 finished. Claims are in order, so every item a warp waits on is
-// already held by a running warp: no co-residency is needed and nothing can deadlock. While it
-// waits, a warp prefetches its groups' bank rows into L2 (cp.async.bulk.prefetch), so the next
-// step's random row reads are L2 hits by the time its predecessor finishes. Rows move as 8-byte
-// (bf16) / 16-byte (f32) lane vectors, 256 / 512 bytes per warp access; records are staged per
-// warp in shared memory; per 8-entry sub-batch every token-row and base-row load is issued
-// before the dependent FMAs.
+// GB300 design: ONE launch runs every step, with no synchronization between warps. Each
+// stream's slots are cut into buckets of 2^bshift consecutive slots; a work item is
+// (stream p, bucket b, 128-column slice) and one warp walks ALL steps of the item in order:
+// step t of stream p touches bucket b through the contiguous range [bb[t][b], bb[t][b+1]) of the
+// chunk's slot-sorted write row (Phase 1 writes these bounds). A bank row is written only by its
+// bucket's warp, and a lane always handles the same 4 columns of every row, so a row rewritten
+// in a later step is re-read by the very thread that stored it: program order alone orders the
+// steps. Per group the arithmetic and order are those of a step-by-step DW, so the bits are
+// the same. Items are claimed from one counter (load balance across uneven buckets).
+// Rows move as 8-byte (bf16) / 16-byte (f32) lane vectors: 256 / 512 contiguous bytes per warp
+// access. The next step's records are loaded while the current step runs; per sub-batch every
+// token-row and base-row load is issued before the dependent FMAs.
 #include <cuda_bf16.h>
 
 #include "sdm_internal.cuh"
@@ -28,28 +29,6 @@ namespace {
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kDwThreads = 256;
 constexpr int kDwWarps = kDwThreads / 32;
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // A lane's 4 columns of a row, kept in the storage type until used: 8 bytes (bf16) / 16 bytes (f32).
 template <typename T>
@@ -86,143 +65,113 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
     *reinterpret_cast<uint2*>(p) = u;
 }
 
-// Waits until *ctr >= need (lane 0 of the warp). Bounded: gives up after timeout_ns or when
-// another warp raised the abort flag; on a timeout sets the status bit and the abort flag.
-__device__ bool wait_done(const DWArgs& a, const uint32_t* ctr, uint32_t need) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) {
-        if (ld_acquire(ctr) < need) {
-            const unsigned long long t0 = globaltimer();
-            unsigned ns = 32;
-            for (uint32_t it = 0;; ++it) {
-                if (ld_acquire(ctr) >= need) break;
-                if (ld_relaxed(a.abort_flag) != 0u) {
-                    ok = false;
-                    break;
-                }
-                if (globaltimer() - t0 > a.timeout_ns || it > (1u << 28)) {
-                    atomicOr(a.status, kDevTimeout);
-                    atomicExch(a.abort_flag, 1u);
-                    ok = false;
-                    break;
-                }
-                __nanosleep(ns);
-                ns = ns < 512 ? ns * 2 : 512;
-            }
-        }
-    }
-    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
-}
-
 template <typename BankT, typename DvT>
 __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
+    constexpr int kSub = (sizeof(BankT) == 2 && sizeof(DvT) == 2) ? 8 : 4;   // entries per sub-batch
     __shared__ int4 recs_s[kDwWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int4* const rs = recs_s[warp];
     BankT* const bank = static_cast<BankT*>(a.bank);
     const DvT* const dv = static_cast<const DvT*>(a.dv);
-    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kDwWarps + warp;
-    int p = static_cast<int>(gwarp % a.P);
-    int exhausted = 0;
-    while (exhausted < a.P) {
-        if (ld_relaxed(a.abort_flag) != 0u) return;
+    const int64_t nsteps = a.step_end - a.step_begin;
+    for (;;) {
         uint32_t it = 0;
-        if (lane == 0) it = atomicAdd(a.claim + p, 1u);
+        if (lane == 0) it = atomicAdd(a.claim, 1u);
         it = __shfl_sync(kFull, it, 0);
-        if (static_cast<int64_t>(it) >= a.per_stream) {
-            p = p + 1 == a.P ? 0 : p + 1;
-            ++exhausted;
-            continue;
-        }
-        exhausted = 0;
-        const int64_t ts = static_cast<int64_t>(it) / a.per_step;
-        const int64_t rem = static_cast<int64_t>(it) - ts * a.per_step;
-        const int tile = static_cast<int>(rem / a.nsl);
-        const int sl = static_cast<int>(rem - static_cast<int64_t>(tile) * a.nsl);
-        const int64_t ti = a.step_begin + ts;
-        const int64_t c = ti * a.P + p;
-        const int s0 = __ldg(a.tb + c * (a.ntk + 1) + tile);
-        const int s1 = __ldg(a.tb + c * (a.ntk + 1) + tile + 1);
+        if (static_cast<int64_t>(it) >= a.items) return;
+        const int sl = static_cast<int>(it % static_cast<uint32_t>(a.nsl));
+        const uint32_t rest = it / static_cast<uint32_t>(a.nsl);
+        const int b = static_cast<int>(rest % static_cast<uint32_t>(a.B));
+        const int p = static_cast<int>(rest / static_cast<uint32_t>(a.B));
         const int col = sl * 128 + lane * 4;
         const bool active = col < a.hd;
-        const int4* const rec = a.krec + c * a.nk;
         const int64_t brow0 = static_cast<int64_t>(p) * a.S;
-        const int64_t drow0 = c * a.C;
-        const uint32_t need = static_cast<uint32_t>(ts * a.per_step);
-
-        if (ts > 0) {
-            // Every item of a step > 0 waits, even an empty one: an item completes only after every
-            // item of the earlier steps, so done >= t * per_step means steps < t are finished.
-            // Before waiting: pull this item's first base rows into L2.
-            if (s0 < s1 && ld_relaxed(a.done + p) < need) {
-                const int m = s0 + lane;
-                if (m < s1) {
-                    const int4 r = __ldg(rec + m);
-                    const uint32_t w0 = static_cast<uint32_t>(r.x);
-                    if ((w0 & kLast) && !(w0 & kRecInvalid)) {
-                        const int64_t row = brow0 + static_cast<uint32_t>(r.y);
-                        const int w = min(128, a.hd - sl * 128);
-                        const uint32_t bytes = static_cast<uint32_t>(w * sizeof(BankT));
-                        const BankT* const src = bank + row * a.hd + sl * 128;
-                        if (((bytes | static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src))) & 15u) == 0u)
-                            prefetch_l2(src, bytes);
-                    }
-                }
+        const int32_t* const bb0 = a.bb + (static_cast<int64_t>(p) * (a.B + 1) + b) * a.steps;
+        const int32_t* const bb1 = bb0 + a.steps;
+        for (int64_t t0 = 0; t0 < nsteps; t0 += 32) {
+            // this item's range in each of the next (up to) 32 steps: lane t holds step t0 + t
+            const int tn = static_cast<int>(nsteps - t0 < 32 ? nsteps - t0 : 32);
+            int s0l = 0, s1l = 0;
+            if (lane < tn) {
+                s0l = __ldg(bb0 + a.step_begin + t0 + lane);
+                s1l = __ldg(bb1 + a.step_begin + t0 + lane);
             }
-            if (!wait_done(a, a.done + p, need)) return;
-        }
-
-        constexpr int kSub = (sizeof(BankT) == 2 && sizeof(DvT) == 2) ? 8 : 4;   // entries per sub-batch
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int b = s0; b < s1; b += 32) {
-            const int cnt = min(32, s1 - b);
-            __syncwarp();
-            if (lane < cnt) rs[lane] = __ldg(rec + b + lane);
-            __syncwarp();
-            for (int m = 0; m < cnt; m += kSub) {
-                Raw4<DvT> dvv[kSub];
-                Raw4<BankT> bv[kSub];
-                // issue every token-row and base-row load of the sub-batch first
+            const uint32_t nonempty = __ballot_sync(kFull, s1l > s0l);
+            auto next_nonempty = [&](int from) {
+                const uint32_t m = from >= 32 ? 0u : (nonempty & (kFull << from));
+                return m ? __ffs(m) - 1 : tn;
+            };
+            int t = next_nonempty(0);
+            // the records of the first non-empty step, prefetched into a register
+            int4 pre = make_int4(0, 0, 0, 0);
+            if (t < tn) {
+                const int s0 = __shfl_sync(kFull, s0l, t), s1 = __shfl_sync(kFull, s1l, t);
+                const int64_t c = (a.step_begin + t0 + t) * a.P + p;
+                if (lane < s1 - s0) pre = __ldg(a.krec + c * a.nk + s0 + lane);
+            }
+            while (t < tn) {
+                const int s0 = __shfl_sync(kFull, s0l, t), s1 = __shfl_sync(kFull, s1l, t);
+                const int64_t c = (a.step_begin + t0 + t) * a.P + p;
+                const int4* const rec = a.krec + c * a.nk;
+                const int64_t drow0 = c * a.C;
+                const int tnext = next_nonempty(t + 1);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int bs = s0; bs < s1; bs += 32) {
+                    const int cnt = min(32, s1 - bs);
+                    __syncwarp();
+                    if (bs == s0) {
+                        rs[lane] = pre;
+                    } else if (lane < cnt) {
+                        rs[lane] = __ldg(rec + bs + lane);
+                    }
+                    __syncwarp();
+                    if (bs + 32 >= s1) {   // last batch of this step: prefetch the next step's records
+                        pre = make_int4(0, 0, 0, 0);
+                        if (tnext < tn) {
+                            const int n0 = __shfl_sync(kFull, s0l, tnext), n1 = __shfl_sync(kFull, s1l, tnext);
+                            const int64_t cn = (a.step_begin + t0 + tnext) * a.P + p;
+                            if (lane < n1 - n0) pre = __ldg(a.krec + cn * a.nk + n0 + lane);
+                        }
+                    }
+                    for (int m = 0; m < cnt; m += kSub) {
+                        Raw4<DvT> dvv[kSub];
+                        Raw4<BankT> bv[kSub];
 #pragma unroll
-                for (int k = 0; k < kSub; ++k) {
-                    const int4 r = rs[min(m + k, cnt - 1)];
-                    const uint32_t w0 = static_cast<uint32_t>(r.x);
-                    const bool in = m + k < cnt && active;
-                    dvv[k].zero();
-                    bv[k].zero();
-                    if (in && !(w0 & kRecInvalid)) dvv[k].ld_nc(dv + (drow0 + (w0 & kRecTokMask)) * a.hd + col);
-                    if (in && (w0 & kLast) && !(w0 & kRecInvalid))
-                        bv[k].ld_cg(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col);
-                }
+                        for (int k = 0; k < kSub; ++k) {
+                            const int4 r = rs[min(m + k, cnt - 1)];
+                            const uint32_t w0 = static_cast<uint32_t>(r.x);
+                            const bool in = m + k < cnt && active && !(w0 & kRecInvalid);
+                            dvv[k].zero();
+                            bv[k].zero();
+                            if (in) dvv[k].ld_nc(dv + (drow0 + (w0 & kRecTokMask)) * a.hd + col);
+                            if (in && (w0 & kLast)) bv[k].ld_cg(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col);
+                        }
 #pragma unroll
-                for (int k = 0; k < kSub; ++k) {
-                    if (m + k < cnt) {
-                        const int4 r = rs[m + k];
-                        const uint32_t w0 = static_cast<uint32_t>(r.x);
-                        const float sc = __int_as_float(r.z);
+                        for (int k = 0; k < kSub; ++k) {
+                            if (m + k < cnt) {
+                                const int4 r = rs[m + k];
+                                const uint32_t w0 = static_cast<uint32_t>(r.x);
+                                const float sc = __int_as_float(r.z);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
-                        if (w0 & kLast) {
-                            if (!(w0 & kRecInvalid) && active) {
-                                const float cp = __int_as_float(r.w);
-                                float o[4];
+                                for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
+                                if (w0 & kLast) {
+                                    if (!(w0 & kRecInvalid) && active) {
+                                        const float cp = __int_as_float(r.w);
+                                        float o[4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
-                                st4(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col, o);
+                                        for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
+                                        st4(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col, o);
+                                    }
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+                                }
                             }
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) acc[i] = 0.f;
                         }
                     }
                 }
+                t = tnext;
             }
         }
-        // publish: every lane's row stores before the stream's done count
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) red_release_add(a.done + p, 1u);
     }
 }
 
@@ -236,9 +185,8 @@ cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dw_kernel<BankT, DvT>, kDwThreads, 0);
     if (e != cudaSuccess) return e;
     per_sm = per_sm < 1 ? 1 : per_sm;
-    const int64_t items = a.per_stream * a.P;
     int64_t blocks = static_cast<int64_t>(sms) * per_sm;
-    const int64_t need_blocks = (items + kDwWarps - 1) / kDwWarps;
+    const int64_t need_blocks = (a.items + kDwWarps - 1) / kDwWarps;
     if (blocks > need_blocks) blocks = need_blocks;
     if (blocks < 1) blocks = 1;
     dw_kernel<BankT, DvT><<<static_cast<unsigned>(blocks), kDwThreads, 0, stream>>>(a);
@@ -248,7 +196,7 @@ cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream) {
-    if (a.per_stream <= 0) return cudaSuccess;
+    if (a.items <= 0 || a.step_end <= a.step_begin) return cudaSuccess;
     if (bank_bf16) {
         return dv_bf16 ? launch_t<__nv_bfloat16, __nv_bfloat16>(a, stream) : launch_t<__nv_bfloat16, float>(a, stream);
     }

@@ -38,7 +38,6 @@ constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid e
 
 // Device status word bits (mirrors SDM_DEV_* in sdm.h).
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
-constexpr uint32_t kDevTimeout = SDM_DEV_TIMEOUT;
 
 // DW record of one write entry in the chunk's sorted write row (16 bytes, one vector load):
 //   x = token | LAST << 30 | FIRST << 31 | kRecInvalid, y = stream-local slot,
@@ -46,23 +45,22 @@ constexpr uint32_t kDevTimeout = SDM_DEV_TIMEOUT;
 constexpr uint32_t kRecInvalid = 1u << 29;
 constexpr uint32_t kRecTokMask = 0xFFFFu;
 
-// Workspace header (bytes): [0] status word, [4] DW abort flag, [256..) per-stream DW claim
-// counters then per-stream DW done counters (uint32 each).
+// Workspace header (bytes): [0] status word, [4] the DW work counter.
 constexpr size_t kHdrStatus = 0;
-constexpr size_t kHdrAbort = 4;
-constexpr size_t kHdrCounters = 256;
+constexpr size_t kHdrClaim = 4;
+constexpr size_t kHdrBytes = 256;
 
 struct Geometry {
     int C, W, R, wr, n, nk, nq, P, hd;
     int64_t steps, N, S;
     int key_bits, passes, digit_bits;
     int threads, npad, nwarps;
-    int L, ntk;            // DW tile length (write-row entries) and tiles per chunk
+    int B, bshift;         // DW slot buckets per stream: bucket(s) = s >> bshift, B = ceil(S / 2^bshift)
     int nsl;               // DW column slices of 128 columns
-    size_t hdr_bytes, krec_off, tb_off, ws_bytes;
+    size_t krec_off, bb_off, ws_bytes;
     size_t smem_bytes;
     // Phase-1 shared-memory carve (byte offsets)
-    size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_scr;
+    size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_scr;
 };
 
 struct P1Args {
@@ -73,7 +71,7 @@ struct P1Args {
     const float* g;
     sdm_p1_out out;
     int4* krec;
-    int32_t* tb;
+    int32_t* bb;            // [P][B + 1][steps] first write-row index of each slot bucket, per chunk
     uint32_t* status;
     int C, W, R, wr, n, nk, nq, npad, nwarps;
     int key_bits, passes, digit_bits;
@@ -83,25 +81,21 @@ struct P1Args {
     int valid_last;
     int g_width, g_lane_stride;
     uint32_t wr_magic;      // ceil(2^32 / wr): e / wr == umulhi(e, wr_magic) for e * wr < 2^32
-    int L, ntk;
-    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_scr, sm_lv;
+    int P, B, bshift;
+    int64_t steps;
+    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_scr, sm_lv;
 };
 
 struct DWArgs {
     const int4* krec;
-    const int32_t* tb;
+    const int32_t* bb;  // [P][B + 1][steps]
     const void* dv;
     void* bank;
-    uint32_t* status;
-    uint32_t* abort_flag;
-    uint32_t* claim;   // [P]
-    uint32_t* done;    // [P]
-    int P, C, nk, ntk, nsl, hd;
-    int64_t S;
-    int64_t step_begin;
-    int64_t per_step;   // items of one stream per step = ntk * nsl
-    int64_t per_stream; // items of one stream over the launch's steps
-    unsigned long long timeout_ns;
+    uint32_t* claim;    // work counter
+    int P, C, nk, B, nsl, hd;
+    int64_t S, steps;
+    int64_t step_begin, step_end;
+    int64_t items;      // P * B * nsl
 };
 
 // Launchers (return a cudaError_t from the launch).

@@ -7,21 +7,22 @@
 // entry, cpe = exp(group total) in the value type, the flags, the packed positions and the sorted
 // rows; then the pair triangles A (write x earlier write of another token) and QK (read x
 // earlier write, own token included). It also writes the DW records of the chunk's sorted write
-// row and the FIRST-snapped tile bounds the DW kernel walks.
+// row and, per slot bucket, where the bucket starts in that row (the DW kernel's work split).
 //
 // GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
 // memory from load to the last output byte:
 //   0. load ids and values (coalesced) into entry-indexed arrays;
 //   1. stable LSD radix sort of entry indices by slot: per pass, warps rank their 256 positions
-//      with __match_any_sync against per-warp digit counters, one block scan of the counters,
-//      one scatter (no global round trips, no merge kernel);
+//      (lanes of equal digit found with one ballot per digit bit) against per-warp digit
+//      counters, one block scan of the counters, one scatter (no global round trips, no merge);
 //   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
 //      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
-//      the DW records / sorted rows / tile bounds in sorted order;
+//      the DW records / sorted rows in sorted order, then the slot-bucket bounds;
 //   3. every entry-order output written from shared memory by consecutive threads;
-//   4. pair triangles: one warp per (row, triangle); each walk reads 32 earlier positions per
-//      step, lanes of one cell are summed by a fixed shuffle tree, one lane adds the cell's
-//      partial to the warp's row buffer; the row is written once (zeros included).
+//   4. pair triangles: A and QK are zero-filled in slices between the earlier phases (the stores
+//      drain while the sort and scans compute); then one warp per (row, triangle) walks: 32
+//      earlier positions per step, lanes of one cell summed by a fixed shuffle tree, one lane adds
+//      the cell's partial to the warp's row buffer; only rows with terms are rewritten.
 #include <cuda_bf16.h>
 
 #include "sdm_internal.cuh"
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
     float* const rexv = reinterpret_cast<float*>(smem + a.sm_rex);         // write entry o -> rex
     float* const cpev = reinterpret_cast<float*>(smem + a.sm_tot);         // write entry o -> cpe (value type)
+    uint32_t* const kslot = reinterpret_cast<uint32_t*>(smem + a.sm_kslot); // write-row index -> key word
     Fwd* const fscr = reinterpret_cast<Fwd*>(smem + a.sm_scr);
     Bwd* const bscr = reinterpret_cast<Bwd*>(smem + a.sm_scr);
     uint32_t* const uscr = reinterpret_cast<uint32_t*>(smem + a.sm_scr + 64 * sizeof(Fwd));
@@ -238,45 +240,76 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const int32_t* qid = a.q_idx + c * nq;
     const float* gch = a.g + c * C * a.g_width;
 
-    // ---- 0. load ------------------------------------------------------------------------------
-    bool bad = false;
-    for (int o = tid; o < nk; o += nthr) {
-        const int t = o / W, ln = o - t * W, e = t * wr + ln;
-        uint32_t key = kmax | kKeyInvalid;
-        float v = 0.f;
-        if (t < V) {
-            const int32_t id = __ldg(kid + o);
-            if (id >= 0 && static_cast<int64_t>(id) < a.S) {
-                key = static_cast<uint32_t>(id);
-                v = to_f(kv[o]);
-            } else {
-                bad = true;
+    // ---- 0. load: every id and value of the chunk, all loads of a thread in flight together ------
+    {
+        bool bad = false;
+        const int total = nk + nq;
+        for (int i0 = tid; i0 < total; i0 += kItems * nthr) {
+            int32_t id[kItems];
+            ValT vv[kItems];
+#pragma unroll
+            for (int u = 0; u < kItems; ++u) {
+                const int i = i0 + u * nthr;
+                if (i < nk) {
+                    id[u] = __ldg(kid + i);
+                    vv[u] = kv[i];
+                } else if (i < total) {
+                    id[u] = __ldg(qid + (i - nk));
+                    vv[u] = qv[i - nk];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kItems; ++u) {
+                const int i = i0 + u * nthr;
+                if (i < total) {
+                    const bool isq = i >= nk;
+                    const int o = isq ? i - nk : i;
+                    const int lanes = isq ? R : W;
+                    const int t = o / lanes, ln = o - t * lanes;
+                    const int e = t * wr + (isq ? W : 0) + ln;
+                    uint32_t key = kmax | kKeyInvalid;
+                    float v = 0.f;
+                    if (t < V) {
+                        if (id[u] >= 0 && static_cast<int64_t>(id[u]) < a.S) {
+                            key = static_cast<uint32_t>(id[u]);
+                            v = to_f(vv[u]);
+                        } else {
+                            bad = true;
+                        }
+                    }
+                    keys[e] = key;
+                    vals[e] = v;
+                }
             }
         }
-        keys[e] = key;
-        vals[e] = v;
+        for (int e = n + tid; e < npad; e += nthr) {
+            keys[e] = kmax | kKeyInvalid;
+            vals[e] = 0.f;
+        }
+        if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
     }
-    for (int o = tid; o < nq; o += nthr) {
-        const int t = o / R, ln = o - t * R, e = t * wr + W + ln;
-        uint32_t key = kmax | kKeyInvalid;
-        float v = 0.f;
-        if (t < V) {
-            const int32_t id = __ldg(qid + o);
-            if (id >= 0 && static_cast<int64_t>(id) < a.S) {
-                key = static_cast<uint32_t>(id);
-                v = to_f(qv[o]);
+    // A and QK are zero-filled in four slices issued between the compute phases below, so their
+    // stores drain while the sort and the scans run; rows with terms are rewritten at the end
+    // (after block barriers, which order the two stores to a cell).
+    auto zero_slice = [&](int slice) {
+        const int64_t cells = static_cast<int64_t>(C) * C;
+        float* mats[2] = {a.out.A, a.out.QK};
+        for (int m = 0; m < 2; ++m) {
+            float* const base = mats[m];
+            if (base == nullptr) continue;
+            float* const chunk = base + c * cells;
+            if ((cells & 3) == 0) {
+                const int64_t n4 = cells >> 2;
+                const int64_t lo = n4 * slice / 4, hi = n4 * (slice + 1) / 4;
+                for (int64_t i = lo + tid; i < hi; i += nthr)
+                    __stcs(reinterpret_cast<float4*>(chunk) + i, make_float4(0.f, 0.f, 0.f, 0.f));
             } else {
-                bad = true;
+                const int64_t lo = cells * slice / 4, hi = cells * (slice + 1) / 4;
+                for (int64_t i = lo + tid; i < hi; i += nthr) __stcs(chunk + i, 0.f);
             }
         }
-        keys[e] = key;
-        vals[e] = v;
-    }
-    for (int e = n + tid; e < npad; e += nthr) {
-        keys[e] = kmax | kKeyInvalid;
-        vals[e] = 0.f;
-    }
-    if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
+    };
+    zero_slice(0);
     __syncthreads();
 
     // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits) ---------------------
@@ -298,7 +331,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 const int p = warp * (32 * kItems) + k * 32 + lane;
                 const uint32_t e = pass == 0 ? static_cast<uint32_t>(p) : src[p];
                 const uint32_t d = (keys[e] >> sh) & dmask;
-                const uint32_t peers = __match_any_sync(kFull, d);
+                // lanes holding the same digit: one ballot per digit bit
+                uint32_t peers = kFull;
+#pragma unroll
+                for (int bit = 0; bit < 8; ++bit) {
+                    if (bit < nb) {
+                        const bool on = (d >> bit) & 1u;
+                        const uint32_t bal = __ballot_sync(kFull, on);
+                        peers &= on ? bal : ~bal;
+                    }
+                }
                 const uint32_t rin = __popc(peers & lt);
                 uint16_t* const h = hist + d * nw + warp;
                 const uint32_t base = *h;
@@ -323,6 +365,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             __syncthreads();
         }
     }
+    zero_slice(1);
 
     // ---- 2. segmented scans over the sorted row -------------------------------------------------
     const int r0 = tid * kItems;
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     auto tok_of = [&](uint32_t e) { return __umulhi(e, a.wr_magic); };
     auto is_q_of = [&](uint32_t e) { return static_cast<int>(e - tok_of(e) * wr) >= W; };
     // head / tail bits, gates (a token's repeated write entry of a group adds 0)
-    uint32_t headm = 0, tailm = 0;
+    uint32_t headm = 0, tailm = 0, validm = 0, qm = 0, padm = 0;
     float x[kItems];
     uint32_t repc = 0;
     {
@@ -351,6 +394,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const uint32_t t = tok_of(e);
             const int j = static_cast<int>(e - t * wr);
             const bool isq = j >= W;
+            validm |= (inv ? 0u : 1u) << k;
+            qm |= (isq ? 1u : 0u) << k;
+            padm |= (e >= static_cast<uint32_t>(n) ? 1u : 0u) << k;
             const bool rep = !head && !isq && !is_q_of(pe) && tok_of(pe) == t;
             repc += rep ? 1u : 0u;
             x[k] = (!inv && !isq && !rep) ? __ldg(gch + t * a.g_width + j * a.g_lane_stride) : 0.f;
@@ -364,12 +410,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     // valid K / Q counts, and non-padding K / Q counts (kind-row indices)
     auto cnt_of = [&](int k) -> uint32_t {
-        if (keys[ke[k]] >> 31) return 0u;
-        return is_q_of(ke[k]) ? (1u << 16) : 1u;
+        if (!((validm >> k) & 1u)) return 0u;
+        return ((qm >> k) & 1u) ? (1u << 16) : 1u;
     };
     auto all_of = [&](int k) -> uint32_t {
-        if (ke[k] >= static_cast<uint32_t>(n)) return 0u;
-        return is_q_of(ke[k]) ? (1u << 16) : 1u;
+        if ((padm >> k) & 1u) return 0u;
+        return ((qm >> k) & 1u) ? (1u << 16) : 1u;
     };
 
     // forward: inclusive log-cumsum (lv, by entry); valid K entries before (kbv); own-kind peers
@@ -391,16 +437,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const float logv = __fadd_rn(run.s, run.c);
             const uint32_t b = run.cnt - ownc;   // valid K before | valid Q before << 16
             const uint32_t ex = (run.allh & 0x7FFFFFFFu) - owna;
-            const bool isq = is_q_of(ke[k]);
+            const bool isq = (qm >> k) & 1u;
             const uint32_t own_b = isq ? (b >> 16) : (b & 0xFFFFu);
             const uint32_t jxv = isq ? (ex >> 16) : (ex & 0xFFFFu);
             const uint32_t e = ke[k];
-            const bool valid = !(keys[e] >> 31);
+            const bool valid = (validm >> k) & 1u;
             posv[e] = own_b | jxv << 16;
             lv[e] = valid ? logv : 0.f;
             kbv[e] = static_cast<uint16_t>(valid ? (b & 0xFFFFu) : 0u);
         }
     }
+    zero_slice(2);
     __syncthreads();   // the scratch is reused by the reverse scan
 
     // reverse: rex, peers after, group total; then every per-entry result
@@ -414,7 +461,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
         const int64_t kbase = c * nk, qbase = c * nq;
-        const int64_t tbase = c * (a.ntk + 1);
 #pragma unroll
         for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
@@ -461,13 +507,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 st_stream(a.krec + kbase + jx, make_int4(static_cast<int>(w0), static_cast<int>(slot),
                                                          __float_as_int(sc), __float_as_int(cpe_f)));
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
-                if (jx % static_cast<uint32_t>(a.L) == 0u) {
-                    const int first = (!valid || before == 0) ? static_cast<int>(jx) : static_cast<int>(jx + after + 1u);
-                    a.tb[tbase + jx / a.L] = first;
-                }
+                kslot[jx] = valid ? key : 0xFFFFFFFFu;
             }
         }
-        if (tid == 0) a.tb[tbase + a.ntk] = nk;
     }
     if (a.out.repeats != nullptr) {
         const uint32_t wsum = __reduce_add_sync(kFull, repc);
@@ -475,6 +517,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             atomicAdd(reinterpret_cast<unsigned long long*>(a.out.repeats), static_cast<unsigned long long>(wsum));
     }
     __syncthreads();
+
+    zero_slice(3);
+    // DW slot buckets: bb[p][b][ti] = the first write-row index whose slot is >= b << bshift (the
+    // write row is sorted by slot; invalid entries, key 0xFFFFFFFF, come last), for b in [0, B].
+    {
+        const int64_t p = c % a.P, ti = c / a.P;
+        for (int b = tid; b <= a.B; b += nthr) {
+            const uint64_t thr = static_cast<uint64_t>(b) << a.bshift;
+            int lo = 0, hi = nk;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (static_cast<uint64_t>(kslot[mid]) < thr) lo = mid + 1; else hi = mid;
+            }
+            a.bb[(p * (a.B + 1) + b) * a.steps + ti] = lo;
+        }
+    }
 
     // ---- 3. entry-order outputs -------------------------------------------------------------------
     {
@@ -572,15 +630,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 }
             }
         }
+        if (!any) continue;   // the row stays as the zero fill left it
         float* const row = outp + (c * C + i) * static_cast<int64_t>(C);
         if (vec4) {
-            for (int j = lane * 4; j < C; j += 128) {
-                float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (any) w = *reinterpret_cast<const float4*>(rowbuf + j);
-                __stcs(reinterpret_cast<float4*>(row + j), w);
-            }
+            for (int j = lane * 4; j < C; j += 128)
+                __stcs(reinterpret_cast<float4*>(row + j), *reinterpret_cast<const float4*>(rowbuf + j));
         } else {
-            for (int j = lane; j < C; j += 32) __stcs(row + j, any ? rowbuf[j] : 0.f);
+            for (int j = lane; j < C; j += 32) __stcs(row + j, rowbuf[j]);
         }
         __syncwarp();
     }

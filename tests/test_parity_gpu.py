@@ -97,7 +97,7 @@ def test_dw_parity_stepwise(name):
     rng = np.random.default_rng(0)
     for ti in range(w.steps):
         for p in range(P):
-            rows = torch.from_numpy(p * S + comp[p][0]).cuda()
+            rows = torch.from_numpy(p * S + comp[p][0].astype(np.int64)).cuda()
             gpu_bank.index_copy_(0, rows, _bank_dev(banks[p], w.bank_dtype))
         snapshot = gpu_bank.clone()
         sdm.dw(shape, d["dv"], gpu_bank, ws, ti, ti + 1)
@@ -118,7 +118,7 @@ def test_dw_parity_stepwise(name):
             oracle.dw_chunk(banks[p], xs["k_idx"][c], xs["q_idx"][c], x["k_val"][c], x["q_val"][c], x["g"][c], dvr,
                             S=U, V=V, val_dtype=w.val_dtype, bank_dtype=w.bank_dtype, alt=alt, amb=amb,
                             touched=touched, mag=mag)
-            got = host(gpu_bank[torch.from_numpy(p * S + slots).cuda()]).astype(np.float64)
+            got = host(gpu_bank[torch.from_numpy(p * S + slots.astype(np.int64)).cuda()]).astype(np.float64)
             t = touched > 0
             assert np.array_equal(got[~t], before[~t]), f"step {ti} stream {p}: an untouched row changed"
             ok = bank_tolerance_ok(got[t], banks[p][t], np.where(amb[t, None] > 0, alt[t], np.nan), mag[t],
@@ -152,7 +152,7 @@ def test_forward_end_to_end(name):
         alt, amb, touched, mag = oracle.dw_stream(bank, xs, p, S=len(slots), C=w.C, P=P, steps=w.steps,
                                                   valid_last=w.valid_last, val_dtype=w.val_dtype,
                                                   dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype, track=True)
-        got = host(gpu_bank[torch.from_numpy(p * S + slots).cuda()]).astype(np.float64)
+        got = host(gpu_bank[torch.from_numpy(p * S + slots.astype(np.int64)).cuda()]).astype(np.float64)
         t = touched > 0
         assert np.array_equal(got[~t], init[p][slots][~t])
         k = touched[t][:, None].astype(np.float64)
