@@ -78,7 +78,6 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += np * 2;
     g->sm_regd = off;
     g->sm_pong = off;
-    g->sm_hist = off + np * 2;
     off += np * 4;
     g->sm_pos = off;
     off += np * 4;
@@ -92,6 +91,11 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_scr = off;
     off += 64 * 16 + 64 * 4;
+    // the sort's digit counters [2^digit_bits][warps + 1] (uint32) reuse the position-pack region
+    // onwards, idle until the scans
+    g->sm_hist = g->sm_pos;
+    const size_t hist_end = g->sm_hist + (size_t(1) << g->digit_bits) * (g->nwarps + 1) * 4;
+    if (hist_end > g->sm_scr) off += hist_end - g->sm_scr;
     g->smem_bytes = round_up(off, 128);
     return SDM_OK;
 }

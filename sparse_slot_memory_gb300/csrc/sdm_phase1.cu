@@ -170,13 +170,14 @@ __device__ Bwd bwd_block_prefix(Bwd x, Bwd* scr, int lane, int warp, int nw) {
     return bcomb(scr[32 + warp], lx);
 }
 
-// In-place exclusive scan of cnt uint16 counters (block-wide; total < 65536).
-__device__ void block_exscan_u16(uint16_t* a, int cnt, uint32_t* scr, int lane, int warp, int nw) {
+// In-place exclusive scan (block-wide) of cnt counters stored with one padding word after every
+// `group` of them: logical index i lives at a[i + i / group].
+__device__ void block_exscan_padded(uint32_t* a, int cnt, int group, uint32_t* scr, int lane, int warp, int nw) {
     const int per = (cnt + blockDim.x - 1) / blockDim.x;
     const int i0 = threadIdx.x * per;
     uint32_t s = 0;
     for (int j = 0; j < per; ++j)
-        if (i0 + j < cnt) s += a[i0 + j];
+        if (i0 + j < cnt) s += a[i0 + j + (i0 + j) / group];
     uint32_t x = s;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -195,12 +196,13 @@ __device__ void block_exscan_u16(uint16_t* a, int cnt, uint32_t* scr, int lane, 
         if (lane < nw) scr[32 + lane] = w - (lane < nw ? scr[lane] : 0u);
     }
     __syncthreads();
-    uint32_t run = scr[32 + warp] + x - s;
+    uint32_t acc = scr[32 + warp] + x - s;
     for (int j = 0; j < per; ++j) {
         if (i0 + j < cnt) {
-            const uint32_t v = a[i0 + j];
-            a[i0 + j] = static_cast<uint16_t>(run);
-            run += v;
+            const int ai = i0 + j + (i0 + j) / group;
+            const uint32_t v = a[ai];
+            a[ai] = acc;
+            acc += v;
         }
     }
 }
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     float* const vals = reinterpret_cast<float*>(smem + a.sm_vals);        // entry -> value
     uint16_t* const sidx = reinterpret_cast<uint16_t*>(smem + a.sm_sidx);  // sorted position -> entry
     uint16_t* const pong = reinterpret_cast<uint16_t*>(smem + a.sm_pong);
-    uint16_t* const hist = reinterpret_cast<uint16_t*>(smem + a.sm_hist);
+    uint32_t* const hist = reinterpret_cast<uint32_t*>(smem + a.sm_hist);   // [digit][warp + 1 pad]
     float* const lv = reinterpret_cast<float*>(smem + a.sm_lv);            // entry -> log-cumsum
     uint32_t* const posv = reinterpret_cast<uint32_t*>(smem + a.sm_pos);   // entry -> position pack
     uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
@@ -228,8 +230,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     Bwd* const bscr = reinterpret_cast<Bwd*>(smem + a.sm_scr);
     uint32_t* const uscr = reinterpret_cast<uint32_t*>(smem + a.sm_scr + 64 * sizeof(Fwd));
 
+    // rows (token) of A (0) / QK (1) with at least one entry that has an earlier write entry in
+    // its group: only these rows have terms
+    __shared__ uint32_t rowmask[2][kMaxC / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = a.nwarps, nthr = blockDim.x;
+    if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
     const int64_t c = a.c0 + blockIdx.x;
     const int C = a.C, W = a.W, R = a.R, wr = a.wr, n = a.n, nk = a.nk, nq = a.nq, npad = a.npad;
     const int V = c >= a.first_partial ? a.valid_last : C;
@@ -323,7 +329,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             // the last pass writes sidx
             uint16_t* const dst = ((a.passes - 1 - pass) & 1) ? pong : sidx;
             const uint16_t* const src = ((a.passes - pass) & 1) ? pong : sidx;
-            for (int i = tid; i < nbins * nw; i += nthr) hist[i] = 0;
+            const int hs = nw + 1;   // padded row: lanes of different digits fall in different banks
+            for (int i = tid; i < nbins * hs; i += nthr) hist[i] = 0u;
             __syncthreads();
             uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 16
 #pragma unroll
@@ -342,21 +349,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     }
                 }
                 const uint32_t rin = __popc(peers & lt);
-                uint16_t* const h = hist + d * nw + warp;
+                uint32_t* const h = hist + d * hs + warp;
                 const uint32_t base = *h;
                 __syncwarp();
-                if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
+                if (rin == 0) *h = base + __popc(peers);
                 __syncwarp();
                 mer[k] = e | (base + rin) << 16;
             }
             __syncthreads();
-            block_exscan_u16(hist, nbins * nw, uscr, lane, warp, nw);
+            block_exscan_padded(hist, nbins * nw, nw, uscr, lane, warp, nw);
             __syncthreads();
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
                 const uint32_t e = mer[k] & 0xFFFFu;
                 const uint32_t d = (keys[e] >> sh) & dmask;
-                dst[hist[d * nw + warp] + (mer[k] >> 16)] = static_cast<uint16_t>(e);
+                dst[hist[d * hs + warp] + (mer[k] >> 16)] = static_cast<uint16_t>(e);
             }
             __syncthreads();
         }
@@ -444,7 +451,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const bool valid = (validm >> k) & 1u;
             posv[e] = own_b | jxv << 16;
             lv[e] = valid ? logv : 0.f;
-            kbv[e] = static_cast<uint16_t>(valid ? (b & 0xFFFFu) : 0u);
+            const uint32_t kbe = valid ? (b & 0xFFFFu) : 0u;
+            kbv[e] = static_cast<uint16_t>(kbe);
+            if (kbe != 0u) {
+                const uint32_t t = tok_of(e);
+                atomicOr(&rowmask[isq ? 1 : 0][t >> 5], 1u << (t & 31u));
+            }
         }
     }
     zero_slice(2);
@@ -577,14 +589,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
     const uint32_t le = lanemask_le();
     const bool vec4 = (C % 4) == 0;
-    for (int u = warp; u < 2 * C; u += nw) {
-        const int i = u >> 1;
-        const bool qk = u & 1;
-        float* const outp = qk ? a.out.QK : a.out.A;
-        if (outp == nullptr) continue;
+    // Only rows flagged in the scan (an entry with an earlier write entry in its group) have
+    // terms; the j-th flagged (triangle, row), in (triangle, row) order, goes to warp j % nw.
+    const int mwords = (C + 31) >> 5;
+    int ord = 0;
+    for (int u2 = 0; u2 < 2 * mwords; ++u2) {
+      const bool qk = u2 >= mwords;
+      const int wd = qk ? u2 - mwords : u2;
+      float* const outp = qk ? a.out.QK : a.out.A;
+      for (uint32_t bits = rowmask[qk ? 1 : 0][wd]; bits != 0u; bits &= bits - 1u) {
+        const int mine = (ord++ % nw) == warp;
+        if (!mine || outp == nullptr) continue;
+        const int i = wd * 32 + __ffs(bits) - 1;
         bool any = false;
         const int lanes = qk ? R : W;
-        if (i < V) {
+        {
             for (int ab = 0; ab < lanes; ++ab) {
                 const int e = i * wr + (qk ? W + ab : ab);
                 const uint32_t kb = kbv[e];
@@ -639,6 +658,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             for (int j = lane; j < C; j += 32) __stcs(row + j, rowbuf[j]);
         }
         __syncwarp();
+      }
     }
 }
 
