@@ -164,6 +164,32 @@ sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, cons
                               void* bank, const sdm_p1_out* out, int64_t step_begin,
                               int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);
 
+/* Bytes of the library-owned scratch used by sdm_forward_chunks_noalloc (16 MiB). */
+#define SDM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * The forward of sdm_forward_chunks for callers that cannot allocate device memory -- for example
+ * code inside a host framework that owns every device allocation, or a plugin interface that is
+ * handed only its input and output buffers. It takes no workspace: it uses a scratch array of
+ * SDM_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU that loads the library holds it
+ * until the process exits). It calls no cudaMalloc / cudaFree and no allocating library routine.
+ * The pages (sparse-delta-memory 2.0.0) have no counterpart of this entry point.
+ *   - Arguments and results are those of sdm_forward_chunks, without ws / ws_bytes.
+ *   - Shapes whose workspace (sdm_workspace_bytes) exceeds SDM_NOALLOC_SCRATCH_BYTES are rejected
+ *     with SDM_ERR_WORKSPACE before any launch; use sdm_forward_chunks with a caller workspace.
+ *   - status_out (nullable): one device int32 that receives the call's device status word
+ *     (SDM_DEV_* bits, 0 = fine), copied on `stream` after the kernels.
+ *   - The first call on a device looks up the scratch's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one scratch and clears its header first. Calls whose kernels overlap
+ *     on the GPU (different streams, or concurrent host threads) race on it: serialize them.
+ */
+sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const int32_t* k_idx,
+                                      const int32_t* q_idx, const void* k_val, const void* q_val,
+                                      const float* g, const void* dv, void* bank,
+                                      const sdm_p1_out* out, int64_t step_begin, int64_t step_end,
+                                      int32_t* status_out, sdm_stream_t stream);
+
 /*
  * Synchronizes `stream`, reads the workspace's device status word into *code_out (0 = fine,
  * else SDM_DEV_* bits) and, if `clear`, zeroes it. Returns SDM_ERR_DEVICE when the word is

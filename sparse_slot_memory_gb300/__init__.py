@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     device_status,
     dw,
     forward_chunks,
+    forward_chunks_noalloc,
     phase1,
     workspace_bytes,
 )

@@ -141,6 +141,19 @@ def forward_chunks(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, ou
     _check(st, "sdm_forward_chunks")
 
 
+def forward_chunks_noalloc(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, out, status=None, step_begin=0,
+                           step_end=None, stream=None):
+    """sdm_forward_chunks_noalloc: the forward on the library's own scratch (no workspace).
+    ``status`` (optional) is a CUDA int32 tensor of one element that receives the device status."""
+    step_end = shape.steps if step_end is None else step_end
+    o = _p1out(out)
+    st = _abi.load().sdm_forward_chunks_noalloc(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val),
+                                                _ptr(q_val), _ptr(g), _ptr(dv), _ptr(bank),
+                                                ctypes.byref(o) if out else None, step_begin, step_end, _ptr(status),
+                                                _stream(stream))
+    _check(st, "sdm_forward_chunks_noalloc")
+
+
 def device_status(ws, clear: bool = True, stream=None) -> int:
     code = _abi.c_i32(0)
     st = _abi.load().sdm_device_status(_ptr(ws), ctypes.byref(code), int(clear), _stream(stream))

@@ -2,6 +2,7 @@
 // workspace layout and the launches. Every check runs before any launch; nothing here allocates.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "sdm_internal.cuh"
 
@@ -280,6 +281,61 @@ extern "C" sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* 
     if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
         return st;
     return run_dw(shape, geo, dv, bank, step_begin, step_end, ws, cs);
+}
+
+// ---- the no-allocation forward ----------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory: a file-scope device array that every GPU
+// loading this library holds until the process exits. Its address is looked up once per device
+// (host code must not use the array's name as a device address) and then reused by every call.
+namespace {
+__device__ __align__(256) unsigned char g_noalloc_scratch[SDM_NOALLOC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+sdm_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SDM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SDM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SDM_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SDM_OK;
+}
+}  // namespace
+
+extern "C" sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                                                 const void* k_val, const void* q_val, const float* g, const void* dv,
+                                                 void* bank, const sdm_p1_out* out, int64_t step_begin,
+                                                 int64_t step_end, int32_t* status_out, sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if ((st = check_p1_args(geo, k_idx, q_idx, k_val, q_val, g, out)) != SDM_OK) return st;
+    if (dv == nullptr || bank == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(dv) || !aligned16(bank)) return SDM_ERR_ALIGN;
+    if (geo.ws_bytes > SDM_NOALLOC_SCRATCH_BYTES) return SDM_ERR_WORKSPACE;
+    if ((st = check_smem(geo)) != SDM_OK) return st;
+    void* ws = nullptr;
+    if ((st = noalloc_scratch(&ws)) != SDM_OK) return st;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // the scratch keeps the previous call's bytes: the status word and the work counter restart at 0
+    if (cudaMemsetAsync(ws, 0, kHdrBytes, cs) != cudaSuccess) return SDM_ERR_CUDA;
+    if (step_begin < step_end) {
+        if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
+            return st;
+        if ((st = run_dw(shape, geo, dv, bank, step_begin, step_end, ws, cs)) != SDM_OK) return st;
+    }
+    if (status_out != nullptr &&
+        cudaMemcpyAsync(status_out, static_cast<unsigned char*>(ws) + kHdrStatus, sizeof(int32_t),
+                        cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+        return SDM_ERR_CUDA;
+    return SDM_OK;
 }
 
 extern "C" sdm_status sdm_device_status(const void* ws, int32_t* code_out, int32_t clear, sdm_stream_t stream) {
