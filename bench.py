@@ -156,6 +156,8 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     if args.streams:
         w = scaled(w, P=args.streams)
+    if args.slots:
+        w = scaled(w, S=args.slots)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -362,6 +364,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--streams", type=int, default=0, help="override the workload's stream count (profiling runs)")
+    ap.add_argument("--slots", type=int, default=0, help="override the workload's slots per stream (profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

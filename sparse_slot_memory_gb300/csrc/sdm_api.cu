@@ -11,6 +11,7 @@ namespace {
 
  // DW work items (stream, slot bucket, column slice) aimed at per launch: ~3x the warps a GB300 holds.
 constexpr int64_t kDwTargetItems = 16384;
+constexpr int kMaxLogBuckets = 11;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -58,12 +59,13 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->npad = threads * kItems;
     g->nwarps = threads / 32;
     g->nsl = (s->hd + 127) / 128;
-    // DW slot buckets: 2^bshift consecutive slots each, about kDwTargetItems items per launch
+    // DW buckets per stream: about kDwTargetItems items per launch, at most 2^11 and no more
+    // buckets than 2^key_bits
     int64_t want = kDwTargetItems / (static_cast<int64_t>(s->P) * g->nsl);
     int lb = 0;
-    while ((int64_t(1) << lb) < want) ++lb;
-    g->bshift = kb > lb ? kb - lb : 0;
-    g->B = static_cast<int>((s->S + (int64_t(1) << g->bshift) - 1) >> g->bshift);
+    while ((int64_t(1) << lb) < want && lb < kMaxLogBuckets && lb < kb) ++lb;
+    g->logB = lb;
+    g->B = 1 << lb;
     // workspace: header | DW records [N, C*W] | bucket bounds [P, B + 1, steps]
     g->krec_off = kHdrBytes;
     g->bb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->nk * sizeof(int4), 256);
@@ -74,7 +76,7 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->sm_keys = off;
     off += np * 4;
     g->sm_vals = off;
-    off += np * 4;
+    off += np * (s->val_dtype == SDM_BF16 ? 2 : 4);
     g->sm_sidx = off;
     off += np * 2;
     g->sm_regd = off;
@@ -90,6 +92,8 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_kslot = off;
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
+    g->sm_bcnt = off;
+    off += round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16);
     g->sm_scr = off;
     off += 64 * 16 + 64 * 4;
     // the sort's digit counters [2^digit_bits][warps + 1] (uint32) reuse the position-pack region
@@ -146,8 +150,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.g_lane_stride = s->gate_per_entry ? 1 : 0;
     a.wr_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.wr - 1) / g.wr);
     a.P = g.P;
-    a.B = g.B;
-    a.bshift = g.bshift;
+    a.logB = g.logB;
     a.steps = g.steps;
     a.sm_keys = static_cast<uint32_t>(g.sm_keys);
     a.sm_vals = static_cast<uint32_t>(g.sm_vals);
@@ -160,6 +163,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_rex = static_cast<uint32_t>(g.sm_rex);
     a.sm_tot = static_cast<uint32_t>(g.sm_tot);
     a.sm_kslot = static_cast<uint32_t>(g.sm_kslot);
+    a.sm_bcnt = static_cast<uint32_t>(g.sm_bcnt);
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
     const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;

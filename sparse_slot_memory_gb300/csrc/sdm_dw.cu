@@ -8,10 +8,10 @@
 // A float32 bank stores the fmaf result itself. Steps apply in order.
 //
 // GB300 design: ONE launch runs every step, with no synchronization between warps. Each
-// stream's slots are cut into buckets of 2^bshift consecutive slots; a work item is
-// (stream p, bucket b, 128-column slice) and one warp walks ALL steps of the item in order:
-// step t of stream p touches bucket b through the contiguous range [bb[t][b], bb[t][b+1]) of the
-// chunk's slot-sorted write row (Phase 1 writes these bounds). A bank row is written only by its
+// stream's slots fall into B buckets by a hash of the slot; a work item is (stream p, bucket b,
+// 128-column slice) and one warp walks ALL steps of the item in order: step t of stream p
+// touches bucket b through the contiguous record range [bb[t][b], bb[t][b+1]) of the chunk (Phase 1
+// writes the records of each bucket's slot groups together). A bank row is written only by its
 // bucket's warp, and a lane always handles the same 4 columns of every row, so a row rewritten
 // in a later step is re-read by the very thread that stored it: program order alone orders the
 // steps. Per group the arithmetic and order are those of a step-by-step DW, so the bits are

@@ -39,7 +39,7 @@ constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid e
 // Device status word bits (mirrors SDM_DEV_* in sdm.h).
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
 
-// DW record of one write entry in the chunk's sorted write row (16 bytes, one vector load):
+// DW record of one valid write entry (16 bytes, one vector load), grouped by slot bucket:
 //   x = token | LAST << 30 | FIRST << 31 | kRecInvalid, y = stream-local slot,
 //   z = f32 bits of sc = k * expf(rex), w = f32 bits of cpe (the value-type cpe widened).
 constexpr uint32_t kRecInvalid = 1u << 29;
@@ -55,12 +55,13 @@ struct Geometry {
     int64_t steps, N, S;
     int key_bits, passes, digit_bits;
     int threads, npad, nwarps;
-    int B, bshift;         // DW slot buckets per stream: bucket(s) = s >> bshift, B = ceil(S / 2^bshift)
+    int B, logB;           // DW buckets per stream, B = 2^logB: a slot group's bucket is a hash of its slot
     int nsl;               // DW column slices of 128 columns
     size_t krec_off, bb_off, ws_bytes;
     size_t smem_bytes;
     // Phase-1 shared-memory carve (byte offsets)
-    size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_scr;
+    size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt,
+        sm_scr;
 };
 
 struct P1Args {
@@ -71,7 +72,7 @@ struct P1Args {
     const float* g;
     sdm_p1_out out;
     int4* krec;
-    int32_t* bb;            // [P][B + 1][steps] first write-row index of each slot bucket, per chunk
+    int32_t* bb;            // [P][B + 1][steps] first record of each slot bucket, per chunk
     uint32_t* status;
     int C, W, R, wr, n, nk, nq, npad, nwarps;
     int key_bits, passes, digit_bits;
@@ -81,9 +82,10 @@ struct P1Args {
     int valid_last;
     int g_width, g_lane_stride;
     uint32_t wr_magic;      // ceil(2^32 / wr): e / wr == umulhi(e, wr_magic) for e * wr < 2^32
-    int P, B, bshift;
+    int P, logB;
     int64_t steps;
-    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_scr, sm_lv;
+    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt, sm_scr,
+        sm_lv;
 };
 
 struct DWArgs {

@@ -7,7 +7,7 @@
 // entry, cpe = exp(group total) in the value type, the flags, the packed positions and the sorted
 // rows; then the pair triangles A (write x earlier write of another token) and QK (read x
 // earlier write, own token included). It also writes the DW records of the chunk's sorted write
-// row and, per slot bucket, where the bucket starts in that row (the DW kernel's work split).
+// row, partitioned into hashed slot buckets (the DW kernel's work split), with each bucket's start.
 //
 // GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
 // memory from load to the last output byte:
@@ -17,7 +17,7 @@
 //      counters, one block scan of the counters, one scatter (no global round trips, no merge);
 //   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
 //      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
-//      the DW records / sorted rows in sorted order, then the slot-bucket bounds;
+//      the sorted rows in sorted order, then the DW records partitioned into hashed slot buckets;
 //   3. every entry-order output written from shared memory by consecutive threads;
 //   4. pair triangles: A and QK are zero-filled in slices between the earlier phases (the stores
 //      drain while the sort and scans compute); then one warp per (row, triangle) walks: 32
@@ -216,7 +216,7 @@ template <typename ValT>
 __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + a.sm_keys);   // entry -> key word
-    float* const vals = reinterpret_cast<float*>(smem + a.sm_vals);        // entry -> value
+    ValT* const vals = reinterpret_cast<ValT*>(smem + a.sm_vals);          // entry -> value
     uint16_t* const sidx = reinterpret_cast<uint16_t*>(smem + a.sm_sidx);  // sorted position -> entry
     uint16_t* const pong = reinterpret_cast<uint16_t*>(smem + a.sm_pong);
     uint32_t* const hist = reinterpret_cast<uint32_t*>(smem + a.sm_hist);   // [digit][warp + 1 pad]
@@ -225,7 +225,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
     float* const rexv = reinterpret_cast<float*>(smem + a.sm_rex);         // write entry o -> rex
     float* const cpev = reinterpret_cast<float*>(smem + a.sm_tot);         // write entry o -> cpe (value type)
-    uint32_t* const kslot = reinterpret_cast<uint32_t*>(smem + a.sm_kslot); // write-row index -> key word
+    // write-row index -> entry | (FIRST: group size, then the group's record base) << 16
+    uint32_t* const krpos = reinterpret_cast<uint32_t*>(smem + a.sm_kslot);
+    uint32_t* const bcnt = reinterpret_cast<uint32_t*>(smem + a.sm_bcnt);  // [B + 1] sizes / offsets | [B] fill
     Fwd* const fscr = reinterpret_cast<Fwd*>(smem + a.sm_scr);
     Bwd* const bscr = reinterpret_cast<Bwd*>(smem + a.sm_scr);
     uint32_t* const uscr = reinterpret_cast<uint32_t*>(smem + a.sm_scr + 64 * sizeof(Fwd));
@@ -274,11 +276,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     const int t = o / lanes, ln = o - t * lanes;
                     const int e = t * wr + (isq ? W : 0) + ln;
                     uint32_t key = kmax | kKeyInvalid;
-                    float v = 0.f;
+                    ValT v = from_f<ValT>(0.f);
                     if (t < V) {
                         if (id[u] >= 0 && static_cast<int64_t>(id[u]) < a.S) {
                             key = static_cast<uint32_t>(id[u]);
-                            v = to_f(vv[u]);
+                            v = vv[u];
                         } else {
                             bad = true;
                         }
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         for (int e = n + tid; e < npad; e += nthr) {
             keys[e] = kmax | kKeyInvalid;
-            vals[e] = 0.f;
+            vals[e] = from_f<ValT>(0.f);
         }
         if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
     }
@@ -512,14 +514,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 const float cpe_f = valid ? to_f(from_f<ValT>(expf(run.tot))) : 1.0f;
                 rexv[o] = rex;
                 cpev[o] = cpe_f;
-                const float sc = valid ? __fmul_rn(vals[e], expf(rex)) : 0.f;
-                const uint32_t w0 = t | (valid ? ((before == 0 ? kFirst : 0u) | (after == 0 ? kLast : 0u))
-                                              : (kFirst | kLast | kRecInvalid));
-                const uint32_t slot = valid ? (key & 0x7FFFFFFFu) : 0u;
-                st_stream(a.krec + kbase + jx, make_int4(static_cast<int>(w0), static_cast<int>(slot),
-                                                         __float_as_int(sc), __float_as_int(cpe_f)));
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
-                kslot[jx] = valid ? key : 0xFFFFFFFFu;
+                krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
             }
         }
     }
@@ -531,18 +527,52 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     __syncthreads();
 
     zero_slice(3);
-    // DW slot buckets: bb[p][b][ti] = the first write-row index whose slot is >= b << bshift (the
-    // write row is sorted by slot; invalid entries, key 0xFFFFFFFF, come last), for b in [0, B].
+    // ---- DW work split: the chunk's slot groups (valid write entries) are partitioned into B
+    // buckets by a hash of the slot, each group's records contiguous and in sorted order; the order
+    // of groups inside a bucket does not matter (different slots). bb[p][b][ti] = the bucket's first
+    // record, bb[p][B][ti] = the chunk's valid write entries. Hashing spreads the hot slots of a
+    // skewed stream over different DW warps.
     {
+        const int B = 1 << a.logB;
+        uint32_t* const off = bcnt;          // [B + 1]
+        uint32_t* const fill = bcnt + B + 1; // [B]
+        auto bucket_of = [&](uint32_t key) -> uint32_t {
+            return a.logB == 0 ? 0u : (key * 0x9E3779B1u) >> (32 - a.logB);
+        };
+        for (int b = tid; b <= B; b += nthr) off[b] = 0u;
+        for (int b = tid; b < B; b += nthr) fill[b] = 0u;
+        __syncthreads();
+        for (int j = tid; j < nk; j += nthr) {
+            const uint32_t kp = krpos[j];
+            if (kp >> 16) atomicAdd(&off[bucket_of(keys[kp & 0xFFFFu])], kp >> 16);
+        }
+        __syncthreads();
+        block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
+        __syncthreads();
         const int64_t p = c % a.P, ti = c / a.P;
-        for (int b = tid; b <= a.B; b += nthr) {
-            const uint64_t thr = static_cast<uint64_t>(b) << a.bshift;
-            int lo = 0, hi = nk;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (static_cast<uint64_t>(kslot[mid]) < thr) lo = mid + 1; else hi = mid;
+        for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
+        for (int j = tid; j < nk; j += nthr) {
+            const uint32_t kp = krpos[j];
+            if (kp >> 16) {
+                const uint32_t b = bucket_of(keys[kp & 0xFFFFu]);
+                krpos[j] = (kp & 0xFFFFu) | (off[b] + atomicAdd(&fill[b], kp >> 16)) << 16;
             }
-            a.bb[(p * (a.B + 1) + b) * a.steps + ti] = lo;
+        }
+        __syncthreads();
+        const int64_t kbase = c * nk;
+        for (int j = tid; j < nk; j += nthr) {
+            const uint32_t e = krpos[j] & 0xFFFFu;
+            const uint32_t key = keys[e];
+            if (key >> 31) continue;   // invalid entries have no record
+            const uint32_t kb = kbv[e];
+            const uint32_t rec = (krpos[j - kb] >> 16) + kb;
+            const uint32_t t = tok_of(e);
+            const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
+            const bool last = ((posv[e] >> kPosAfterShift) & kPosCountMax) == 0u;
+            const uint32_t w0 = t | (kb == 0u ? kFirst : 0u) | (last ? kLast : 0u);
+            const float sc = __fmul_rn(to_f(vals[e]), expf(rexv[o]));
+            st_stream(a.krec + kbase + rec, make_int4(static_cast<int>(w0), static_cast<int>(key), __float_as_int(sc),
+                                                      __float_as_int(cpev[o])));
         }
     }
 
@@ -560,7 +590,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             if (a.out.log_k) st_stream(a.out.log_k + kbase + o, lg);
             if (a.out.rex) st_stream(a.out.rex + kbase + o, rexv[o]);
             if (cpe_o) st_stream(cpe_o + kbase + o, from_f<ValT>(cpev[o]));
-            if (keff_o) st_stream(keff_o + kbase + o, from_f<ValT>(valid ? vals[e] * expf(lg) : 0.f));
+            if (keff_o) st_stream(keff_o + kbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
             if (a.out.is_last)
                 st_stream(a.out.is_last + kbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
             if (a.out.is_only) st_stream(a.out.is_only + kbase + o, static_cast<int8_t>(size == 1u));
@@ -575,7 +605,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const bool valid = size != 0u;
             const float lg = lv[e];
             if (a.out.log_q) st_stream(a.out.log_q + qbase + o, lg);
-            if (qw_o) st_stream(qw_o + qbase + o, from_f<ValT>(valid ? vals[e] * expf(lg) : 0.f));
+            if (qw_o) st_stream(qw_o + qbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
             if (a.out.q_last)
                 st_stream(a.out.q_last + qbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
             if (a.out.q_only) st_stream(a.out.q_only + qbase + o, static_cast<int8_t>(size == 1u));
@@ -614,7 +644,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     any = true;
                 }
                 const int r = static_cast<int>(posv[e] & kPosMask);
-                const float ve = vals[e], lge = lv[e];
+                const float ve = to_f(vals[e]), lge = lv[e];
                 uint32_t met = 0;
                 for (int top = r - 1; met < kb && top >= 0; top -= 32) {
                     const int p = top - lane;
@@ -632,7 +662,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     const int tf = incl ? static_cast<int>(tok_of(f)) : -1;
                     float v = 0.f;
                     if (incl && isk && (qk || tf != i)) {
-                        v = __fmul_rn(__fmul_rn(ve, vals[f]), expf(__fsub_rn(lge, lv[f])));
+                        v = __fmul_rn(__fmul_rn(ve, to_f(vals[f])), expf(__fsub_rn(lge, lv[f])));
                     }
                     // segmented suffix sums over lanes of equal token (tokens are non-increasing
                     // along the lanes): a fixed shuffle tree
