@@ -51,7 +51,7 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     int kb = 1;
     while ((int64_t(1) << kb) < s->S) ++kb;
     g->key_bits = kb;
-    g->passes = (kb + 7) / 8;
+    g->passes = (kb + kMaxDigitBits - 1) / kMaxDigitBits;
     g->digit_bits = (kb + g->passes - 1) / g->passes;
     int threads = static_cast<int>((n + kItems - 1) / kItems);
     threads = static_cast<int>(round_up(static_cast<size_t>(threads), 32));
@@ -94,12 +94,14 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_bcnt = off;
     off += round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16);
+    g->sm_zero = off;
+    off += kZeroBufBytes;
     g->sm_scr = off;
     off += 64 * 16 + 64 * 4;
-    // the sort's digit counters [2^digit_bits][warps + 1] (uint32) reuse the position-pack region
+    // the sort's digit counters [2^digit_bits][warps + 1] (uint16) reuse the position-pack region
     // onwards, idle until the scans
     g->sm_hist = g->sm_pos;
-    const size_t hist_end = g->sm_hist + (size_t(1) << g->digit_bits) * (g->nwarps + 1) * 4;
+    const size_t hist_end = g->sm_hist + round_up((size_t(1) << g->digit_bits) * (g->nwarps + 1) * 2, 16);
     if (hist_end > g->sm_scr) off += hist_end - g->sm_scr;
     g->smem_bytes = round_up(off, 128);
     return SDM_OK;
@@ -149,6 +151,8 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.g_width = s->gate_per_entry ? g.W : 1;
     a.g_lane_stride = s->gate_per_entry ? 1 : 0;
     a.wr_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.wr - 1) / g.wr);
+    a.w_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.W - 1) / g.W);
+    a.r_magic = static_cast<uint32_t>(((uint64_t(1) << 32) + g.R - 1) / g.R);
     a.P = g.P;
     a.logB = g.logB;
     a.steps = g.steps;
@@ -164,6 +168,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_tot = static_cast<uint32_t>(g.sm_tot);
     a.sm_kslot = static_cast<uint32_t>(g.sm_kslot);
     a.sm_bcnt = static_cast<uint32_t>(g.sm_bcnt);
+    a.sm_zero = static_cast<uint32_t>(g.sm_zero);
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
     const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;

@@ -17,9 +17,11 @@
 // steps. Per group the arithmetic and order are those of a step-by-step DW, so the bits are
 // the same. Items are claimed from one counter (load balance across uneven buckets).
 // Rows move as 8-byte (bf16) / 16-byte (f32) lane vectors: 256 / 512 contiguous bytes per warp
-// access. The next step's records are loaded while the current step runs; per sub-batch every
+// access. Records arrive in shared memory by cp.async two steps ahead; per sub-batch every
 // token-row and base-row load is issued before the dependent FMAs.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "sdm_internal.cuh"
 
@@ -30,6 +32,12 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kDwThreads = 256;
 constexpr int kDwWarps = kDwThreads / 32;
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // A lane's 4 columns of a row, kept in the storage type until used: 8 bytes (bf16) / 16 bytes (f32).
 template <typename T>
 struct Raw4;
@@ -66,11 +74,14 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
 }
 
 template <typename BankT, typename DvT>
-__global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
+__global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
     constexpr int kSub = (sizeof(BankT) == 2 && sizeof(DvT) == 2) ? 8 : 4;   // entries per sub-batch
-    __shared__ int4 recs_s[kDwWarps][32];
+    // per warp two record buffers (the current step's, the next step's arriving by cp.async);
+    // slots past 32 are read by the unrolled loads but never used
+    __shared__ __align__(16) int4 recs_s[kDwWarps][3][40];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int4* const rs = recs_s[warp];
+    int4* const rsb = recs_s[warp][0];
+    int buf = 0;   // the current step's record buffer; the next two steps' follow it (mod 3)
     BankT* const bank = static_cast<BankT*>(a.bank);
     const DvT* const dv = static_cast<const DvT*>(a.dv);
     const int64_t nsteps = a.step_end - a.step_begin;
@@ -86,6 +97,8 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
         const int col = sl * 128 + lane * 4;
         const bool active = col < a.hd;
         const int64_t brow0 = static_cast<int64_t>(p) * a.S;
+        BankT* const bank_lane = bank + brow0 * a.hd + col;   // this lane's columns of the stream's row 0
+        const uint32_t hdu = static_cast<uint32_t>(a.hd);
         const int32_t* const bb0 = a.bb + (static_cast<int64_t>(p) * (a.B + 1) + b) * a.steps;
         const int32_t* const bb1 = bb0 + a.steps;
         for (int64_t t0 = 0; t0 < nsteps; t0 += 32) {
@@ -101,53 +114,57 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
                 const uint32_t m = from >= 32 ? 0u : (nonempty & (kFull << from));
                 return m ? __ffs(m) - 1 : tn;
             };
+            // Records of the first 32 entries of each non-empty step arrive by cp.async, two steps
+            // ahead (three buffers): while step t runs, the next step's records are already in
+            // shared memory and the step after next is on its way.
+            auto request = [&](int ts, int bi) {
+                const int s0 = __shfl_sync(kFull, s0l, ts), s1 = __shfl_sync(kFull, s1l, ts);
+                const int64_t c = (a.step_begin + t0 + ts) * a.P + p;
+                if (lane < s1 - s0) cp_async16(rsb + bi * 40 + lane, a.krec + c * a.nk + s0 + lane);
+                cp_async_commit();
+            };
             int t = next_nonempty(0);
-            // the records of the first non-empty step, prefetched into a register
-            int4 pre = make_int4(0, 0, 0, 0);
-            if (t < tn) {
-                const int s0 = __shfl_sync(kFull, s0l, t), s1 = __shfl_sync(kFull, s1l, t);
-                const int64_t c = (a.step_begin + t0 + t) * a.P + p;
-                if (lane < s1 - s0) pre = __ldg(a.krec + c * a.nk + s0 + lane);
-            }
+            int tnext = t < tn ? next_nonempty(t + 1) : tn;
+            __syncwarp();
+            if (t < tn) request(t, buf);
+            if (tnext < tn) request(tnext, buf == 2 ? 0 : buf + 1);
+            cp_async_wait_all();
+            __syncwarp();
             while (t < tn) {
+                const int tnext2 = tnext < tn ? next_nonempty(tnext + 1) : tn;
+                const int bnext = buf == 2 ? 0 : buf + 1, bnext2 = bnext == 2 ? 0 : bnext + 1;
+                if (tnext2 < tn) request(tnext2, bnext2);
                 const int s0 = __shfl_sync(kFull, s0l, t), s1 = __shfl_sync(kFull, s1l, t);
                 const int64_t c = (a.step_begin + t0 + t) * a.P + p;
                 const int4* const rec = a.krec + c * a.nk;
                 const int64_t drow0 = c * a.C;
-                const int tnext = next_nonempty(t + 1);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                int4* const rs = rsb + buf * 40;
                 for (int bs = s0; bs < s1; bs += 32) {
                     const int cnt = min(32, s1 - bs);
-                    __syncwarp();
-                    if (bs == s0) {
-                        rs[lane] = pre;
-                    } else if (lane < cnt) {
-                        rs[lane] = __ldg(rec + bs + lane);
+                    if (bs != s0) {   // steps with more than 32 entries: the rest synchronously
+                        __syncwarp();
+                        if (lane < cnt) rs[lane] = __ldg(rec + bs + lane);
+                        __syncwarp();
                     }
-                    __syncwarp();
-                    if (bs + 32 >= s1) {   // last batch of this step: prefetch the next step's records
-                        pre = make_int4(0, 0, 0, 0);
-                        if (tnext < tn) {
-                            const int n0 = __shfl_sync(kFull, s0l, tnext), n1 = __shfl_sync(kFull, s1l, tnext);
-                            const int64_t cn = (a.step_begin + t0 + tnext) * a.P + p;
-                            if (lane < n1 - n0) pre = __ldg(a.krec + cn * a.nk + n0 + lane);
-                        }
-                    }
-                    for (int m = 0; m < cnt; m += kSub) {
-                        Raw4<DvT> dvv[kSub];
-                        Raw4<BankT> bv[kSub];
+                    const DvT* const dv_lane = dv + drow0 * a.hd + col;
+                    // One sub-batch of K entries: every token-row and base-row load first (one
+                    // 32x32->64 multiply-add per row address), then the FMA chain in order.
+                    auto sub = [&](int m, auto kw) {
+                        constexpr int K = decltype(kw)::value;
+                        Raw4<DvT> dvv[K];
+                        Raw4<BankT> bv[K];
 #pragma unroll
-                        for (int k = 0; k < kSub; ++k) {
-                            const int4 r = rs[min(m + k, cnt - 1)];
+                        for (int k = 0; k < K; ++k) {
+                            const int4 r = rs[m + k];
                             const uint32_t w0 = static_cast<uint32_t>(r.x);
-                            const bool in = m + k < cnt && active && !(w0 & kRecInvalid);
-                            dvv[k].zero();
-                            bv[k].zero();
-                            if (in) dvv[k].ld_nc(dv + (drow0 + (w0 & kRecTokMask)) * a.hd + col);
-                            if (in && (w0 & kLast)) bv[k].ld_cg(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col);
+                            if (m + k < cnt && active) {
+                                dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
+                                if (w0 & kLast) bv[k].ld_cg(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu);
+                            }
                         }
 #pragma unroll
-                        for (int k = 0; k < kSub; ++k) {
+                        for (int k = 0; k < K; ++k) {
                             if (m + k < cnt) {
                                 const int4 r = rs[m + k];
                                 const uint32_t w0 = static_cast<uint32_t>(r.x);
@@ -155,21 +172,35 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
                                 if (w0 & kLast) {
-                                    if (!(w0 & kRecInvalid) && active) {
+                                    if (active) {
                                         const float cp = __int_as_float(r.w);
                                         float o[4];
 #pragma unroll
                                         for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
-                                        st4(bank + (brow0 + static_cast<uint32_t>(r.y)) * a.hd + col, o);
+                                        st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
                                     }
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) acc[i] = 0.f;
                                 }
                             }
                         }
+                    };
+                    // full sub-batches of kSub, a tail of at most kSub / 2 in a half-width one
+                    for (int m = 0; m < cnt;) {
+                        if (cnt - m > kSub / 2) {
+                            sub(m, std::integral_constant<int, kSub>());
+                            m += kSub;
+                        } else {
+                            sub(m, std::integral_constant<int, kSub / 2>());
+                            m += kSub / 2;
+                        }
                     }
                 }
                 t = tnext;
+                tnext = tnext2;
+                buf = bnext;
+                cp_async_wait_all();   // the new next step's records
+                __syncwarp();
             }
         }
     }

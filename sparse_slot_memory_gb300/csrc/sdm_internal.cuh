@@ -35,6 +35,8 @@ constexpr int kItems = 8;               // sorted positions per thread in the Ph
 constexpr int kMaxThreads = 1024;
 constexpr int kMaxRow = kItems * kMaxThreads;   // entries of one chunk held on chip
 constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid entry
+constexpr int kMaxDigitBits = 8;                // radix digit of the Phase-1 sort
+constexpr int kZeroBufBytes = 4096;             // zero source of the A / QK bulk zero fill
 
 // Device status word bits (mirrors SDM_DEV_* in sdm.h).
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
@@ -61,7 +63,7 @@ struct Geometry {
     size_t smem_bytes;
     // Phase-1 shared-memory carve (byte offsets)
     size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt,
-        sm_scr;
+        sm_zero, sm_scr;
 };
 
 struct P1Args {
@@ -82,10 +84,11 @@ struct P1Args {
     int valid_last;
     int g_width, g_lane_stride;
     uint32_t wr_magic;      // ceil(2^32 / wr): e / wr == umulhi(e, wr_magic) for e * wr < 2^32
+    uint32_t w_magic, r_magic;   // the same for W and R (entry-order output index -> token)
     int P, logB;
     int64_t steps;
-    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt, sm_scr,
-        sm_lv;
+    uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt, sm_zero,
+        sm_scr, sm_lv;
 };
 
 struct DWArgs {

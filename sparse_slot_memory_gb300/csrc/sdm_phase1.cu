@@ -12,15 +12,16 @@
 // GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
 // memory from load to the last output byte:
 //   0. load ids and values (coalesced) into entry-indexed arrays;
-//   1. stable LSD radix sort of entry indices by slot: per pass, warps rank their 256 positions
-//      (lanes of equal digit found with one ballot per digit bit) against per-warp digit
-//      counters, one block scan of the counters, one scatter (no global round trips, no merge);
+//   1. stable LSD radix sort of entry indices by slot in passes of up to 8-bit digits (three passes
+//      for 2^20 slots): warps rank their 256 positions (lanes of equal digit found with one ballot
+//      per digit bit) against per-warp 16-bit digit counters (padded rows: conflict-free), one
+//      block scan of the counters, one scatter (no global round trips, no merge);
 //   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
 //      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
 //      the sorted rows in sorted order, then the DW records partitioned into hashed slot buckets;
 //   3. every entry-order output written from shared memory by consecutive threads;
-//   4. pair triangles: A and QK are zero-filled in slices between the earlier phases (the stores
-//      drain while the sort and scans compute); then one warp per (row, triangle) walks: 32
+//   4. pair triangles: A and QK are zero-filled by TMA bulk stores issued at the start (they drain
+//      while the sort and scans compute); then one warp per (row, triangle) walks: 32
 //      earlier positions per step, lanes of one cell summed by a fixed shuffle tree, one lane adds
 //      the cell's partial to the warp's row buffer; only rows with terms are rewritten.
 #include <cuda_bf16.h>
@@ -117,7 +118,7 @@ __device__ __forceinline__ Bwd shfl_down_b(const Bwd& v, int d) {
 
 // Exclusive prefix (aggregate of every earlier thread) of the threads' aggregates, forward.
 // scr: 64 elements of scratch. Contains two block barriers.
-__device__ Fwd fwd_block_prefix(Fwd x, Fwd* scr, int lane, int warp, int nw) {
+__device__ __noinline__ Fwd fwd_block_prefix(Fwd x, Fwd* scr, int lane, int warp, int nw) {
     const Fwd zero = {0.f, 0.f, 0u, 0u};
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -144,7 +145,7 @@ __device__ Fwd fwd_block_prefix(Fwd x, Fwd* scr, int lane, int warp, int nw) {
 }
 
 // Exclusive prefix in the reversed order (aggregate of every later thread).
-__device__ Bwd bwd_block_prefix(Bwd x, Bwd* scr, int lane, int warp, int nw) {
+__device__ __noinline__ Bwd bwd_block_prefix(Bwd x, Bwd* scr, int lane, int warp, int nw) {
     const Bwd zero = {0.f, 0.f, 0u, 0.f};
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -172,12 +173,29 @@ __device__ Bwd bwd_block_prefix(Bwd x, Bwd* scr, int lane, int warp, int nw) {
 
 // In-place exclusive scan (block-wide) of cnt counters stored with one padding word after every
 // `group` of them: logical index i lives at a[i + i / group].
-__device__ void block_exscan_padded(uint32_t* a, int cnt, int group, uint32_t* scr, int lane, int warp, int nw) {
+// In-place exclusive scan (block-wide) of cnt counters stored with one padding slot after every
+// `group` of them: logical index i lives at a[i + i / group]. Each thread takes a contiguous run of
+// logical indices and walks the padded addresses incrementally (one division per thread).
+template <typename T>
+__device__ __noinline__ void block_exscan_padded(T* a, int cnt, int group, uint32_t* scr, int lane, int warp, int nw) {
     const int per = (cnt + blockDim.x - 1) / blockDim.x;
     const int i0 = threadIdx.x * per;
+    const int n_mine = max(0, min(per, cnt - i0));
+    const int r0 = i0 / group;
+    const int start = i0 + r0;               // padded address of i0
+    const int left0 = group - (i0 - r0 * group);   // entries left in the first row
     uint32_t s = 0;
-    for (int j = 0; j < per; ++j)
-        if (i0 + j < cnt) s += a[i0 + j + (i0 + j) / group];
+    {
+        int addr = start, left = left0;
+        for (int j = 0; j < n_mine; ++j) {
+            s += a[addr];
+            ++addr;
+            if (--left == 0) {
+                ++addr;   // skip the padding slot
+                left = group;
+            }
+        }
+    }
     uint32_t x = s;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -197,13 +215,40 @@ __device__ void block_exscan_padded(uint32_t* a, int cnt, int group, uint32_t* s
     }
     __syncthreads();
     uint32_t acc = scr[32 + warp] + x - s;
-    for (int j = 0; j < per; ++j) {
-        if (i0 + j < cnt) {
-            const int ai = i0 + j + (i0 + j) / group;
-            const uint32_t v = a[ai];
-            a[ai] = acc;
+    {
+        int addr = start, left = left0;
+        for (int j = 0; j < n_mine; ++j) {
+            const uint32_t v = a[addr];
+            a[addr] = static_cast<T>(acc);
             acc += v;
+            ++addr;
+            if (--left == 0) {
+                ++addr;
+                left = group;
+            }
         }
+    }
+}
+
+// TMA bulk store (shared -> global) of `bytes` (a multiple of 16; both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(ssrc));
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(s), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// A / QK of chunk c set to zero by the block with plain stores (the triangles are not a whole
+// number of 16-byte units, so the TMA bulk fill does not apply). Out of line: rarely used.
+__device__ __noinline__ void zero_triangles(float* A, float* QK, int64_t c, int64_t cells) {
+    for (int m = 0; m < 2; ++m) {
+        float* const base = m == 0 ? A : QK;
+        if (base == nullptr) continue;
+        float* const chunk = base + c * cells;
+        for (int64_t i = threadIdx.x; i < cells; i += blockDim.x) __stcs(chunk + i, 0.f);
     }
 }
 
@@ -219,7 +264,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     ValT* const vals = reinterpret_cast<ValT*>(smem + a.sm_vals);          // entry -> value
     uint16_t* const sidx = reinterpret_cast<uint16_t*>(smem + a.sm_sidx);  // sorted position -> entry
     uint16_t* const pong = reinterpret_cast<uint16_t*>(smem + a.sm_pong);
-    uint32_t* const hist = reinterpret_cast<uint32_t*>(smem + a.sm_hist);   // [digit][warp + 1 pad]
+    uint16_t* const hist = reinterpret_cast<uint16_t*>(smem + a.sm_hist);   // [digit][warp + 1 pad]
     float* const lv = reinterpret_cast<float*>(smem + a.sm_lv);            // entry -> log-cumsum
     uint32_t* const posv = reinterpret_cast<uint32_t*>(smem + a.sm_pos);   // entry -> position pack
     uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
@@ -238,6 +283,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
+    // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
+    // use by the sort's barriers
+    const int nbk = 1 << a.logB;
+    for (int b = tid; b < 2 * nbk + 1; b += nthr) bcnt[b] = 0u;
+    // A and QK start as zeros written by the TMA engine from a zeroed shared buffer (when the chunk's
+    // triangles are a whole number of 16-byte units); the rows with terms are rewritten at the end.
+    const int64_t cells = static_cast<int64_t>(a.C) * a.C;
+    const bool bulk_zero = (cells & 3) == 0 && (a.out.A != nullptr || a.out.QK != nullptr);
+    uint4* const zbuf = reinterpret_cast<uint4*>(smem + a.sm_zero);
+    if (bulk_zero) {
+        for (int i = tid; i < kZeroBufBytes / 16; i += nthr) zbuf[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_async_shared();   // the zeros are visible to the bulk copies issued after the next barrier
+    }
+    auto bucket_of = [&](uint32_t key) -> uint32_t {
+        return a.logB == 0 ? 0u : (key * 0x9E3779B1u) >> (32 - a.logB);
+    };
     const int64_t c = a.c0 + blockIdx.x;
     const int C = a.C, W = a.W, R = a.R, wr = a.wr, n = a.n, nk = a.nk, nq = a.nq, npad = a.npad;
     const int V = c >= a.first_partial ? a.valid_last : C;
@@ -273,7 +334,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     const bool isq = i >= nk;
                     const int o = isq ? i - nk : i;
                     const int lanes = isq ? R : W;
-                    const int t = o / lanes, ln = o - t * lanes;
+                    const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), isq ? a.r_magic : a.w_magic));
+                    const int ln = o - t * lanes;
                     const int e = t * wr + (isq ? W : 0) + ln;
                     uint32_t key = kmax | kKeyInvalid;
                     ValT v = from_f<ValT>(0.f);
@@ -296,29 +358,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
     }
-    // A and QK are zero-filled in four slices issued between the compute phases below, so their
-    // stores drain while the sort and the scans run; rows with terms are rewritten at the end
-    // (after block barriers, which order the two stores to a cell).
-    auto zero_slice = [&](int slice) {
-        const int64_t cells = static_cast<int64_t>(C) * C;
+    if (!bulk_zero && (a.out.A != nullptr || a.out.QK != nullptr)) zero_triangles(a.out.A, a.out.QK, c, cells);
+    __syncthreads();
+    if (bulk_zero && warp == 0) {   // the 32 lanes of warp 0 issue the pieces round-robin
         float* mats[2] = {a.out.A, a.out.QK};
+        const int64_t bytes = cells * 4;
+        const int64_t pieces = (bytes + kZeroBufBytes - 1) / kZeroBufBytes;
         for (int m = 0; m < 2; ++m) {
-            float* const base = mats[m];
-            if (base == nullptr) continue;
-            float* const chunk = base + c * cells;
-            if ((cells & 3) == 0) {
-                const int64_t n4 = cells >> 2;
-                const int64_t lo = n4 * slice / 4, hi = n4 * (slice + 1) / 4;
-                for (int64_t i = lo + tid; i < hi; i += nthr)
-                    __stcs(reinterpret_cast<float4*>(chunk) + i, make_float4(0.f, 0.f, 0.f, 0.f));
-            } else {
-                const int64_t lo = cells * slice / 4, hi = cells * (slice + 1) / 4;
-                for (int64_t i = lo + tid; i < hi; i += nthr) __stcs(chunk + i, 0.f);
+            if (mats[m] == nullptr) continue;
+            char* const dst = reinterpret_cast<char*>(mats[m] + c * cells);
+            for (int64_t i = lane; i < pieces; i += 32) {
+                const int64_t o = i * kZeroBufBytes;
+                bulk_store(dst + o, zbuf, static_cast<uint32_t>(bytes - o < kZeroBufBytes ? bytes - o : kZeroBufBytes));
             }
         }
-    };
-    zero_slice(0);
-    __syncthreads();
+        bulk_commit();
+    }
 
     // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits) ---------------------
     {
@@ -332,7 +387,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             uint16_t* const dst = ((a.passes - 1 - pass) & 1) ? pong : sidx;
             const uint16_t* const src = ((a.passes - pass) & 1) ? pong : sidx;
             const int hs = nw + 1;   // padded row: lanes of different digits fall in different banks
-            for (int i = tid; i < nbins * hs; i += nthr) hist[i] = 0u;
+            {
+                uint32_t* const h32 = reinterpret_cast<uint32_t*>(hist);
+                for (int i = tid; i < (nbins * hs + 1) / 2; i += nthr) h32[i] = 0u;
+            }
             __syncthreads();
             uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 16
 #pragma unroll
@@ -342,19 +400,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 const uint32_t d = (keys[e] >> sh) & dmask;
                 // lanes holding the same digit: one ballot per digit bit
                 uint32_t peers = kFull;
-#pragma unroll
-                for (int bit = 0; bit < 8; ++bit) {
-                    if (bit < nb) {
-                        const bool on = (d >> bit) & 1u;
-                        const uint32_t bal = __ballot_sync(kFull, on);
-                        peers &= on ? bal : ~bal;
-                    }
+#pragma unroll 1
+                for (int bit = 0; bit < nb; ++bit) {
+                    const bool on = (d >> bit) & 1u;
+                    const uint32_t bal = __ballot_sync(kFull, on);
+                    peers &= on ? bal : ~bal;
                 }
                 const uint32_t rin = __popc(peers & lt);
-                uint32_t* const h = hist + d * hs + warp;
+                uint16_t* const h = hist + d * hs + warp;
                 const uint32_t base = *h;
                 __syncwarp();
-                if (rin == 0) *h = base + __popc(peers);
+                if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
                 __syncwarp();
                 mer[k] = e | (base + rin) << 16;
             }
@@ -374,7 +430,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             __syncthreads();
         }
     }
-    zero_slice(1);
 
     // ---- 2. segmented scans over the sorted row -------------------------------------------------
     const int r0 = tid * kItems;
@@ -432,13 +487,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // in posv until the reverse pass replaces it with the position pack
     {
         Fwd agg = {0.f, 0.f, 0u, 0u};
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < kItems; ++k) {
             const Fwd it = {x[k], 0.f, cnt_of(k), all_of(k) | (((headm >> k) & 1u) << 31)};
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < kItems; ++k) {
             const uint32_t ownc = cnt_of(k), owna = all_of(k);
             const Fwd it = {x[k], 0.f, ownc, owna | (((headm >> k) & 1u) << 31)};
@@ -461,13 +516,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
         }
     }
-    zero_slice(2);
     __syncthreads();   // the scratch is reused by the reverse scan
 
     // reverse: rex, peers after, group total; then every per-entry result
     {
         Bwd agg = {0.f, 0.f, 0u, 0.f};
-#pragma unroll
+#pragma unroll 1
         for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
             const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
@@ -475,8 +529,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
         const int64_t kbase = c * nk, qbase = c * nq;
-#pragma unroll
-        for (int k = kItems - 1; k >= 0; --k) {
+#pragma unroll 1
+        for (int k = kItems - 1; k >= 0; --k) {   // not unrolled: the body is large (code size)
             const bool tail = (tailm >> k) & 1u;
             const Bwd ex = run;
             const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
@@ -516,6 +570,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 cpev[o] = cpe_f;
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
+                if (valid && before == 0) atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
             }
         }
     }
@@ -526,27 +581,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     __syncthreads();
 
-    zero_slice(3);
     // ---- DW work split: the chunk's slot groups (valid write entries) are partitioned into B
     // buckets by a hash of the slot, each group's records contiguous and in sorted order; the order
     // of groups inside a bucket does not matter (different slots). bb[p][b][ti] = the bucket's first
     // record, bb[p][B][ti] = the chunk's valid write entries. Hashing spreads the hot slots of a
     // skewed stream over different DW warps.
     {
-        const int B = 1 << a.logB;
-        uint32_t* const off = bcnt;          // [B + 1]
+        const int B = nbk;
+        uint32_t* const off = bcnt;          // [B + 1]: sizes counted by the reverse scan
         uint32_t* const fill = bcnt + B + 1; // [B]
-        auto bucket_of = [&](uint32_t key) -> uint32_t {
-            return a.logB == 0 ? 0u : (key * 0x9E3779B1u) >> (32 - a.logB);
-        };
-        for (int b = tid; b <= B; b += nthr) off[b] = 0u;
-        for (int b = tid; b < B; b += nthr) fill[b] = 0u;
-        __syncthreads();
-        for (int j = tid; j < nk; j += nthr) {
-            const uint32_t kp = krpos[j];
-            if (kp >> 16) atomicAdd(&off[bucket_of(keys[kp & 0xFFFFu])], kp >> 16);
-        }
-        __syncthreads();
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
         const int64_t p = c % a.P, ti = c / a.P;
@@ -582,7 +625,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
         ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);
         for (int o = tid; o < nk; o += nthr) {
-            const int t = o / W, e = t * wr + (o - t * W);
+            const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.w_magic)), e = t * wr + (o - t * W);
             const uint32_t pk = posv[e];
             const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
             const bool valid = size != 0u;
@@ -599,7 +642,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         const int64_t qbase = c * nq;
         ValT* const qw_o = static_cast<ValT*>(a.out.q_w);
         for (int o = tid; o < nq; o += nthr) {
-            const int t = o / R, e = t * wr + W + (o - t * R);
+            const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
             const uint32_t pk = posv[e];
             const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
             const bool valid = size != 0u;
@@ -615,6 +658,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 4. pair triangles --------------------------------------------------------------------------
     if (a.out.A == nullptr && a.out.QK == nullptr) return;
+    if (bulk_zero && warp == 0) {
+        bulk_wait_all();        // this lane's zero pieces are written (and the zero buffer is no longer read)
+        fence_async_global();   // ... and ordered before the generic stores of the rows below
+    }
     __syncthreads();   // the key array becomes the row buffers
     float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
     const uint32_t le = lanemask_le();
