@@ -74,8 +74,8 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
 }
 
 template <typename BankT, typename DvT>
-__global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
-    constexpr int kSub = (sizeof(BankT) == 2 && sizeof(DvT) == 2) ? 8 : 4;   // entries per sub-batch
+__global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
+    constexpr int kSub = 4;   // entries per sub-batch (4 blocks of 8 warps per SM hide the latency)
     // per warp two record buffers (the current step's, the next step's arriving by cp.async);
     // slots past 32 are read by the unrolled loads but never used
     __shared__ __align__(16) int4 recs_s[kDwWarps][3][40];
