@@ -95,15 +95,19 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->sm_bcnt = off;
     off += round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16);
     g->sm_zero = off;
-    off += kZeroBufBytes;
-    g->sm_scr = off;
-    off += 64 * 16 + 64 * 4;
     // the sort's digit counters [2^digit_bits][warps + 1] (uint16) reuse the position-pack region
     // onwards, idle until the scans
     g->sm_hist = g->sm_pos;
     const size_t hist_end = g->sm_hist + round_up((size_t(1) << g->digit_bits) * (g->nwarps + 1) * 2, 16);
-    if (hist_end > g->sm_scr) off += hist_end - g->sm_scr;
-    g->smem_bytes = round_up(off, 128);
+    for (int zb : {kZeroBufBig, kZeroBufSmall}) {
+        size_t o = off + zb;
+        g->sm_scr = o;
+        o += 64 * 16 + 64 * 4;
+        if (hist_end > g->sm_scr) o += hist_end - g->sm_scr;
+        g->zero_bytes = zb;
+        g->smem_bytes = round_up(o, 128);
+        if (g->smem_bytes + 1024 <= kSmemOptin) break;   // room for the static arrays too
+    }
     return SDM_OK;
 }
 
@@ -169,6 +173,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_kslot = static_cast<uint32_t>(g.sm_kslot);
     a.sm_bcnt = static_cast<uint32_t>(g.sm_bcnt);
     a.sm_zero = static_cast<uint32_t>(g.sm_zero);
+    a.zero_bytes = g.zero_bytes;
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
     const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;

@@ -36,7 +36,12 @@ constexpr int kMaxThreads = 1024;
 constexpr int kMaxRow = kItems * kMaxThreads;   // entries of one chunk held on chip
 constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid entry
 constexpr int kMaxDigitBits = 8;                // radix digit of the Phase-1 sort
-constexpr int kZeroBufBytes = 4096;             // zero source of the A / QK bulk zero fill
+// zero source of the A / QK bulk zero fill: 16 KB pieces where the chunk's shared memory has room,
+// else 4 KB; the pieces are issued in kZeroStages portions spread over the Phase-1 phases
+constexpr int kZeroBufBig = 16384;
+constexpr int kZeroBufSmall = 4096;
+constexpr int kZeroStages = 8;
+constexpr size_t kSmemOptin = 232448;          // opt-in shared memory per block on sm_103a
 
 // Device status word bits (mirrors SDM_DEV_* in sdm.h).
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
@@ -61,6 +66,7 @@ struct Geometry {
     int nsl;               // DW column slices of 128 columns
     size_t krec_off, bb_off, ws_bytes;
     size_t smem_bytes;
+    int zero_bytes;        // bulk zero-fill piece (and zero buffer) size
     // Phase-1 shared-memory carve (byte offsets)
     size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt,
         sm_zero, sm_scr;
@@ -87,6 +93,7 @@ struct P1Args {
     uint32_t w_magic, r_magic;   // the same for W and R (entry-order output index -> token)
     int P, logB;
     int64_t steps;
+    int zero_bytes;         // bulk zero-fill piece size (the zero buffer's size)
     uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt, sm_zero,
         sm_scr, sm_lv;
 };

@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const bool bulk_zero = (cells & 3) == 0 && (a.out.A != nullptr || a.out.QK != nullptr);
     uint4* const zbuf = reinterpret_cast<uint4*>(smem + a.sm_zero);
     if (bulk_zero) {
-        for (int i = tid; i < kZeroBufBytes / 16; i += nthr) zbuf[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < a.zero_bytes / 16; i += nthr) zbuf[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_async_shared();   // the zeros are visible to the bulk copies issued after the next barrier
     }
     auto bucket_of = [&](uint32_t key) -> uint32_t {
@@ -360,20 +360,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     if (!bulk_zero && (a.out.A != nullptr || a.out.QK != nullptr)) zero_triangles(a.out.A, a.out.QK, c, cells);
     __syncthreads();
-    if (bulk_zero && warp == 0) {   // the 32 lanes of warp 0 issue the pieces round-robin
-        float* mats[2] = {a.out.A, a.out.QK};
-        const int64_t bytes = cells * 4;
-        const int64_t pieces = (bytes + kZeroBufBytes - 1) / kZeroBufBytes;
-        for (int m = 0; m < 2; ++m) {
-            if (mats[m] == nullptr) continue;
-            char* const dst = reinterpret_cast<char*>(mats[m] + c * cells);
-            for (int64_t i = lane; i < pieces; i += 32) {
-                const int64_t o = i * kZeroBufBytes;
-                bulk_store(dst + o, zbuf, static_cast<uint32_t>(bytes - o < kZeroBufBytes ? bytes - o : kZeroBufBytes));
+    // The zero pieces of both triangles go out in kZeroStages portions, one at the start of each
+    // phase (issued by the lanes of warp 0): issuing them all at once stalls warp 0, and with it
+    // the block, until the store engine has taken most of them.
+    int zero_next = 0;   // the next portion to issue (warp 0)
+    auto zero_upto = [&](int k) {
+        if (!bulk_zero || warp != 0) return;
+        const int64_t bytes = cells * 4, zb = a.zero_bytes;
+        const int64_t pieces = (bytes + zb - 1) / zb;
+        for (; zero_next <= k; ++zero_next) {
+            const int64_t i0 = 2 * pieces * zero_next / kZeroStages, i1 = 2 * pieces * (zero_next + 1) / kZeroStages;
+            for (int64_t i = i0 + lane; i < i1; i += 32) {
+                const int m = i < pieces ? 0 : 1;
+                float* const mat = m == 0 ? a.out.A : a.out.QK;
+                if (mat == nullptr) continue;
+                const int64_t o = (i - m * pieces) * zb;
+                bulk_store(reinterpret_cast<char*>(mat + c * cells) + o, zbuf,
+                           static_cast<uint32_t>(bytes - o < zb ? bytes - o : zb));
             }
+            bulk_commit();
         }
-        bulk_commit();
-    }
+    };
+    zero_upto(0);
 
     // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits) ---------------------
     {
@@ -392,6 +400,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 for (int i = tid; i < (nbins * hs + 1) / 2; i += nthr) h32[i] = 0u;
             }
             __syncthreads();
+            if (pass < 3) zero_upto(1 + pass);
             uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 16
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
@@ -493,6 +502,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
+        zero_upto(4);
 #pragma unroll 1
         for (int k = 0; k < kItems; ++k) {
             const uint32_t ownc = cnt_of(k), owna = all_of(k);
@@ -528,6 +538,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == kItems - 1 ? it : bcomb(agg, it);
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
+        zero_upto(5);
         const int64_t kbase = c * nk, qbase = c * nq;
 #pragma unroll 1
         for (int k = kItems - 1; k >= 0; --k) {   // not unrolled: the body is large (code size)
@@ -592,6 +603,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         uint32_t* const fill = bcnt + B + 1; // [B]
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
+        zero_upto(6);
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
         for (int j = tid; j < nk; j += nthr) {
@@ -621,6 +633,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 3. entry-order outputs -------------------------------------------------------------------
     {
+        zero_upto(kZeroStages - 1);
         const int64_t kbase = c * nk;
         ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
         ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);
@@ -667,24 +680,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const uint32_t le = lanemask_le();
     const bool vec4 = (C % 4) == 0;
     // Only rows flagged in the scan (an entry with an earlier write entry in its group) have
-    // terms; the j-th flagged (triangle, row), in (triangle, row) order, goes to warp j % nw.
-    const int mwords = (C + 31) >> 5;
-    int ord = 0;
-    for (int u2 = 0; u2 < 2 * mwords; ++u2) {
-      const bool qk = u2 >= mwords;
-      const int wd = qk ? u2 - mwords : u2;
-      float* const outp = qk ? a.out.QK : a.out.A;
-      for (uint32_t bits = rowmask[qk ? 1 : 0][wd]; bits != 0u; bits &= bits - 1u) {
-        const int mine = (ord++ % nw) == warp;
-        if (!mine || outp == nullptr) continue;
-        const int i = wd * 32 + __ffs(bits) - 1;
+    // terms; the j-th flagged (triangle, row), in (triangle, row) order, goes to warp j % nw. Lane
+    // u < 2 * mwords holds flag word u (A rows, then QK rows); a warp prefix of the words' counts
+    // locates pair j without any walk over the others.
+    const int mwords = (C + 31) >> 5;   // <= 8: the flag words fit the lanes
+    const uint32_t fw = lane < 2 * mwords ? rowmask[lane >= mwords ? 1 : 0][lane >= mwords ? lane - mwords : lane] : 0u;
+    uint32_t fincl = __popc(fw);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, fincl, d);
+        if (lane >= d) fincl += y;
+    }
+    const uint32_t fexcl = fincl - __popc(fw);
+    const uint32_t nflag = __shfl_sync(kFull, fincl, 31);
+    for (uint32_t jf = static_cast<uint32_t>(warp); jf < nflag; jf += static_cast<uint32_t>(nw)) {
+        const int u = __ffs(__ballot_sync(kFull, jf >= fexcl && jf < fincl)) - 1;   // the word holding pair jf
+        uint32_t bits = __shfl_sync(kFull, fw, u);
+        for (uint32_t q = __shfl_sync(kFull, fexcl, u); q < jf; ++q) bits &= bits - 1u;
+        const bool qk = u >= mwords;
+        float* const outp = qk ? a.out.QK : a.out.A;
+        if (outp == nullptr) continue;
+        const int i = (qk ? u - mwords : u) * 32 + __ffs(bits) - 1;
         bool any = false;
         const int lanes = qk ? R : W;
-        {
-            for (int ab = 0; ab < lanes; ++ab) {
-                const int e = i * wr + (qk ? W + ab : ab);
+        for (int ab0 = 0; ab0 < lanes; ab0 += 32) {
+            // the row's entries with an earlier write entry in their group, one ballot per 32
+            const int eab = i * wr + (qk ? W : 0) + ab0 + lane;
+            uint32_t with = __ballot_sync(kFull, ab0 + lane < lanes && kbv[eab] != 0u);
+            for (; with != 0u; with &= with - 1u) {
+                const int e = i * wr + (qk ? W : 0) + ab0 + __ffs(with) - 1;
                 const uint32_t kb = kbv[e];
-                if (kb == 0u) continue;   // no earlier write entry in its group: no term
                 if (!any) {
                     for (int j = lane; j < C; j += 32) rowbuf[j] = 0.f;
                     __syncwarp();
@@ -735,7 +760,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             for (int j = lane; j < C; j += 32) __stcs(row + j, rowbuf[j]);
         }
         __syncwarp();
-      }
     }
 }
 
