@@ -17,8 +17,11 @@
 // steps. Per group the arithmetic and order are those of a step-by-step DW, so the bits are
 // the same. Items are claimed from one counter (load balance across uneven buckets).
 // Rows move as 8-byte (bf16) / 16-byte (f32) lane vectors: 256 / 512 contiguous bytes per warp
-// access. Records arrive in shared memory by cp.async two steps ahead; per sub-batch every
-// token-row and base-row load is issued before the dependent FMAs.
+// access. The item's records of up to 32 steps are taken as one sequence in step order, in
+// windows of 32 that arrive in shared memory by cp.async two windows ahead; per sub-batch of up
+// to 4 records every token-row and base-row load is issued before the dependent FMAs. A
+// sub-batch never holds two records of one slot (those are of different steps): it is cut
+// before the second, whose base row is then loaded after the first one's store.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -76,15 +79,16 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
 template <typename BankT, typename DvT>
 __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
     constexpr int kSub = 4;   // entries per sub-batch (4 blocks of 8 warps per SM hide the latency)
-    // per warp two record buffers (the current step's, the next step's arriving by cp.async);
-    // slots past 32 are read by the unrolled loads but never used
+    // per warp three window buffers of 32 records (+ 8 slots read by the unrolled loads, never
+    // used) and each record's first dv row (its chunk * C)
     __shared__ __align__(16) int4 recs_s[kDwWarps][3][40];
+    __shared__ long long drow_s[kDwWarps][3][40];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int4* const rsb = recs_s[warp][0];
-    int buf = 0;   // the current step's record buffer; the next two steps' follow it (mod 3)
+    const uint32_t lt = (1u << lane) - 1u;
     BankT* const bank = static_cast<BankT*>(a.bank);
     const DvT* const dv = static_cast<const DvT*>(a.dv);
     const int64_t nsteps = a.step_end - a.step_begin;
+    const uint32_t hdu = static_cast<uint32_t>(a.hd);
     for (;;) {
         uint32_t it = 0;
         if (lane == 0) it = atomicAdd(a.claim, 1u);
@@ -96,110 +100,115 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
         const int p = static_cast<int>(rest / static_cast<uint32_t>(a.B));
         const int col = sl * 128 + lane * 4;
         const bool active = col < a.hd;
-        const int64_t brow0 = static_cast<int64_t>(p) * a.S;
-        BankT* const bank_lane = bank + brow0 * a.hd + col;   // this lane's columns of the stream's row 0
-        const uint32_t hdu = static_cast<uint32_t>(a.hd);
+        BankT* const bank_lane = bank + static_cast<int64_t>(p) * a.S * a.hd + col;   // stream row 0, own columns
+        const DvT* const dv_lane = dv + col;
         const int32_t* const bb0 = a.bb + (static_cast<int64_t>(p) * (a.B + 1) + b) * a.steps;
         const int32_t* const bb1 = bb0 + a.steps;
         for (int64_t t0 = 0; t0 < nsteps; t0 += 32) {
-            // this item's range in each of the next (up to) 32 steps: lane t holds step t0 + t
+            // The item's records of (up to) 32 steps, concatenated in step order: lane t holds
+            // step t0 + t's range, cum the inclusive prefix of the counts.
             const int tn = static_cast<int>(nsteps - t0 < 32 ? nsteps - t0 : 32);
-            int s0l = 0, s1l = 0;
+            int s0l = 0, cntl = 0;
             if (lane < tn) {
                 s0l = __ldg(bb0 + a.step_begin + t0 + lane);
-                s1l = __ldg(bb1 + a.step_begin + t0 + lane);
+                cntl = __ldg(bb1 + a.step_begin + t0 + lane) - s0l;
             }
-            const uint32_t nonempty = __ballot_sync(kFull, s1l > s0l);
-            auto next_nonempty = [&](int from) {
-                const uint32_t m = from >= 32 ? 0u : (nonempty & (kFull << from));
-                return m ? __ffs(m) - 1 : tn;
-            };
-            // Records of the first 32 entries of each non-empty step arrive by cp.async, two steps
-            // ahead (three buffers): while step t runs, the next step's records are already in
-            // shared memory and the step after next is on its way.
-            auto request = [&](int ts, int bi) {
-                const int s0 = __shfl_sync(kFull, s0l, ts), s1 = __shfl_sync(kFull, s1l, ts);
-                const int64_t c = (a.step_begin + t0 + ts) * a.P + p;
-                if (lane < s1 - s0) cp_async16(rsb + bi * 40 + lane, a.krec + c * a.nk + s0 + lane);
+            int cum = cntl;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(kFull, cum, d);
+                if (lane >= d) cum += y;
+            }
+            const int total = __shfl_sync(kFull, cum, 31);
+            if (total == 0) continue;
+            const int64_t cl = (a.step_begin + t0 + lane) * a.P + p;   // lane t's chunk
+            const long long rbase = cl * a.nk + s0l - (cum - cntl);    // record of position g: rbase + g
+            const long long dbase = static_cast<long long>(cl) * a.C;
+            const int nwin = (total + 31) >> 5;
+            // window w (positions 32w..) into buffer s: lane j fetches position 32w + j by cp.async
+            auto fetch = [&](int w, int s) {
+                const int g = w * 32 + lane;
+                int ts = 0;   // the step holding g: the number of steps whose inclusive count is <= g
+#pragma unroll
+                for (int d = 16; d >= 1; d >>= 1) {
+                    const int c = __shfl_sync(kFull, cum, ts + d - 1);
+                    if (c <= g) ts += d;
+                }
+                const long long rb = __shfl_sync(kFull, rbase, ts);
+                const long long db = __shfl_sync(kFull, dbase, ts);
+                if (g < total) {
+                    cp_async16(&recs_s[warp][s][lane], a.krec + rb + g);
+                    drow_s[warp][s][lane] = db;
+                }
                 cp_async_commit();
             };
-            int t = next_nonempty(0);
-            int tnext = t < tn ? next_nonempty(t + 1) : tn;
             __syncwarp();
-            if (t < tn) request(t, buf);
-            if (tnext < tn) request(tnext, buf == 2 ? 0 : buf + 1);
+            fetch(0, 0);
+            if (nwin > 1) fetch(1, 1);
             cp_async_wait_all();
             __syncwarp();
-            while (t < tn) {
-                const int tnext2 = tnext < tn ? next_nonempty(tnext + 1) : tn;
-                const int bnext = buf == 2 ? 0 : buf + 1, bnext2 = bnext == 2 ? 0 : bnext + 1;
-                if (tnext2 < tn) request(tnext2, bnext2);
-                const int s0 = __shfl_sync(kFull, s0l, t), s1 = __shfl_sync(kFull, s1l, t);
-                const int64_t c = (a.step_begin + t0 + t) * a.P + p;
-                const int4* const rec = a.krec + c * a.nk;
-                const int64_t drow0 = c * a.C;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                int4* const rs = rsb + buf * 40;
-                for (int bs = s0; bs < s1; bs += 32) {
-                    const int cnt = min(32, s1 - bs);
-                    if (bs != s0) {   // steps with more than 32 entries: the rest synchronously
-                        __syncwarp();
-                        if (lane < cnt) rs[lane] = __ldg(rec + bs + lane);
-                        __syncwarp();
-                    }
-                    const DvT* const dv_lane = dv + drow0 * a.hd + col;
-                    // One sub-batch of K entries: every token-row and base-row load first (one
-                    // 32x32->64 multiply-add per row address), then the FMA chain in order.
-                    auto sub = [&](int m, auto kw) {
-                        constexpr int K = decltype(kw)::value;
-                        Raw4<DvT> dvv[K];
-                        Raw4<BankT> bv[K];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int w = 0; w < nwin; ++w) {
+                const int s = w % 3;
+                if (w + 2 < nwin) fetch(w + 2, (w + 2) % 3);
+                const int n = min(32, total - w * 32);
+                const int4* const rs = recs_s[warp][s];
+                const long long* const ds = drow_s[warp][s];
+                // A record whose slot is also the LAST slot of an earlier record of the window (an
+                // earlier step) must load its base row after that record's store: prev = the
+                // nearest such record.
+                uint32_t key = 0x80000000u | static_cast<uint32_t>(lane);
+                if (lane < n && (static_cast<uint32_t>(rs[lane].x) & kLast)) key = static_cast<uint32_t>(rs[lane].y);
+                const uint32_t same = __match_any_sync(kFull, key) & lt;
+                const int prev = same ? 31 - __clz(same) : -1;
+                // One sub-batch of up to K records [m, m + cnt): every token-row and base-row load
+                // first, then the FMA chain in order.
+                auto sub = [&](int m, int cnt, auto kw) {
+                    constexpr int K = decltype(kw)::value;
+                    Raw4<DvT> dvv[K];
+                    Raw4<BankT> bv[K];
 #pragma unroll
-                        for (int k = 0; k < K; ++k) {
+                    for (int k = 0; k < K; ++k) {
+                        const int4 r = rs[m + k];
+                        const uint32_t w0 = static_cast<uint32_t>(r.x);
+                        if (k < cnt && active) {
+                            dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(ds[m + k] + (w0 & kRecTokMask)) * hdu);
+                            if (w0 & kLast) bv[k].ld_cg(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < K; ++k) {
+                        if (k < cnt) {
                             const int4 r = rs[m + k];
                             const uint32_t w0 = static_cast<uint32_t>(r.x);
-                            if (m + k < cnt && active) {
-                                dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
-                                if (w0 & kLast) bv[k].ld_cg(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu);
-                            }
-                        }
+                            const float sc = __int_as_float(r.z);
 #pragma unroll
-                        for (int k = 0; k < K; ++k) {
-                            if (m + k < cnt) {
-                                const int4 r = rs[m + k];
-                                const uint32_t w0 = static_cast<uint32_t>(r.x);
-                                const float sc = __int_as_float(r.z);
+                            for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
+                            if (w0 & kLast) {
+                                if (active) {
+                                    const float cp = __int_as_float(r.w);
+                                    float o[4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
-                                if (w0 & kLast) {
-                                    if (active) {
-                                        const float cp = __int_as_float(r.w);
-                                        float o[4];
-#pragma unroll
-                                        for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
-                                        st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
-                                    }
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+                                    for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
+                                    st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
                                 }
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) acc[i] = 0.f;
                             }
-                        }
-                    };
-                    // full sub-batches of kSub, a tail of at most kSub / 2 in a half-width one
-                    for (int m = 0; m < cnt;) {
-                        if (cnt - m > kSub / 2) {
-                            sub(m, std::integral_constant<int, kSub>());
-                            m += kSub;
-                        } else {
-                            sub(m, std::integral_constant<int, kSub / 2>());
-                            m += kSub / 2;
                         }
                     }
+                };
+                for (int m = 0; m < n;) {
+                    int e = min(m + kSub, n);
+                    const uint32_t cut = __ballot_sync(kFull, lane > m && lane < e && prev >= m);
+                    if (cut) e = __ffs(cut) - 1;
+                    if (e - m > kSub / 2)
+                        sub(m, e - m, std::integral_constant<int, kSub>());
+                    else
+                        sub(m, e - m, std::integral_constant<int, kSub / 2>());
+                    m = e;
                 }
-                t = tnext;
-                tnext = tnext2;
-                buf = bnext;
-                cp_async_wait_all();   // the new next step's records
+                cp_async_wait_all();   // window w + 1 (and the one after it, if issued)
                 __syncwarp();
             }
         }
