@@ -106,7 +106,7 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
         if (hist_end > g->sm_scr) o += hist_end - g->sm_scr;
         g->zero_bytes = zb;
         g->smem_bytes = round_up(o, 128);
-        if (g->smem_bytes + 1024 <= kSmemOptin) break;   // room for the static arrays too
+        if (g->smem_bytes + 4096 <= kSmemOptin) break;   // room for the static arrays too
     }
     return SDM_OK;
 }

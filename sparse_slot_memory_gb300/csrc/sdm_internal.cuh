@@ -41,6 +41,11 @@ constexpr int kMaxDigitBits = 8;                // radix digit of the Phase-1 so
 constexpr int kZeroBufBig = 16384;
 constexpr int kZeroBufSmall = 4096;
 constexpr int kZeroStages = 8;
+// dense pair path: slot groups with at least kHotMin write entries, at most kHotMax per chunk,
+// whose log-cumsums span at most kHotSpan
+constexpr uint32_t kHotMin = 16;
+constexpr int kHotMax = 16;
+constexpr float kHotSpan = 80.f;
 constexpr size_t kSmemOptin = 232448;          // opt-in shared memory per block on sm_103a
 
 // Device status word bits (mirrors SDM_DEV_* in sdm.h).

@@ -280,9 +280,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // rows (token) of A (0) / QK (1) with at least one entry that has an earlier write entry in
     // its group: only these rows have terms
     __shared__ uint32_t rowmask[2][kMaxC / 32];
+    // sorted positions of the first write entry of each slot group with >= kHotMin write entries:
+    // the candidates for the dense pair path
+    __shared__ uint32_t hotmask[kMaxRow / 32];
+    __shared__ int hot_n;
+    // per (triangle, token): the dense groups with a term in the token's A (0) / QK (1) row
+    __shared__ uint32_t hotrow[2][kMaxC];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
+    for (int i = tid; i < kMaxRow / 32; i += blockDim.x) hotmask[i] = 0u;
+    for (int i = tid; i < 2 * kMaxC; i += blockDim.x) hotrow[i / kMaxC][i % kMaxC] = 0u;
     // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
     // use by the sort's barriers
     const int nbk = 1 << a.logB;
@@ -582,6 +590,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
                 if (valid && before == 0) atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
+                if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
             }
         }
     }
@@ -679,6 +688,118 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
     const uint32_t le = lanemask_le();
     const bool vec4 = (C % 4) == 0;
+
+    // Dense path of hot slot groups. Inside a group the entries run in token order, every write
+    // entry of token j before every entry of token i > j and, within a token, its write entries
+    // before its read entries. So the group adds to A[i][j] (j < i) and QK[i][j] (j <= i)
+    //   sum_a sum_b v_a v_b exp(L_a - L_b) = UK[i] * WK[j]   (QK: UQ[i] * WK[j]),
+    //   UK[i] = sum over token i's write entries a of v_a exp(L_a - ref), UQ the same over its
+    //   read entries, WK[j] = sum over token j's write entries b of v_b exp(ref - L_b),
+    // a rank-1 term per group. ref = L_first - 40 keeps both factors within e^{+-40} when the
+    // group's log-cumsums span at most kHotSpan; a wider group keeps the exact walk. The first
+    // (in position order) groups with at least kHotMin write entries take this path, as many as
+    // the free shared memory holds; their entries are marked (kb bit 15) and skip the walk.
+    struct HotMeta {
+        int r0, r1, ok;
+        float ref;
+    };
+    HotMeta* const meta = reinterpret_cast<HotMeta*>(smem + a.sm_rex);   // rex .. zero buffer: free now
+    float* const hvec = reinterpret_cast<float*>(smem + a.sm_rex + kHotMax * sizeof(HotMeta));
+    const int hot_cap = min(kHotMax, (static_cast<int>(a.sm_scr - a.sm_rex) - kHotMax * static_cast<int>(sizeof(HotMeta))) /
+                                         (12 * C));
+    if (warp == 0) {   // the first hot_cap candidates in position order
+        const int nwords = npad >> 5;
+        uint32_t cnt = 0;
+        for (int q = 0; q < 8; ++q) {
+            const int wi = lane * 8 + q;
+            if (wi < nwords) cnt += __popc(hotmask[wi]);
+        }
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, d);
+            if (lane >= d) incl += y;
+        }
+        int idx = static_cast<int>(incl - cnt);
+        for (int q = 0; q < 8 && idx < hot_cap; ++q) {
+            const int wi = lane * 8 + q;
+            for (uint32_t m = wi < nwords ? hotmask[wi] : 0u; m != 0u && idx < hot_cap; m &= m - 1u)
+                meta[idx++].r0 = wi * 32 + __ffs(m) - 1;
+        }
+        if (lane == 31) hot_n = min(static_cast<int>(incl), hot_cap);
+    }
+    __syncthreads();
+    const int nhot = hot_n;
+    for (int h = warp; h < nhot; h += nw) {   // one warp builds a group's vectors
+        const int hr0 = meta[h].r0;
+        const uint32_t hkey = keys[sidx[hr0]];
+        const float l0 = lv[sidx[hr0]];
+        int hr1 = hr0;   // the group's last position: same key
+        for (int base = hr0 + 1;; base += 32) {
+            const int pos = base + lane;
+            const uint32_t m = __ballot_sync(kFull, pos < npad && keys[sidx[pos]] == hkey);
+            if (m != kFull) {
+                hr1 = base + __ffs(~m) - 2;
+                break;
+            }
+        }
+        const bool ok = __fsub_rn(l0, lv[sidx[hr1]]) <= kHotSpan;
+        const float ref = __fsub_rn(l0, 40.f);
+        if (lane == 0) {
+            meta[h].r1 = hr1;
+            meta[h].ok = ok ? 1 : 0;
+            meta[h].ref = ref;
+        }
+        if (!ok) continue;
+        float* const uk = hvec + h * 3 * C;
+        float* const uq = uk + C;
+        float* const wk = uq + C;
+        for (int j = lane; j < 3 * C; j += 32) uk[j] = 0.f;
+        __syncwarp();
+        for (int base = hr0; base <= hr1; base += 32) {
+            const int pos = base + lane;
+            float vk = 0.f, vq = 0.f, vw = 0.f;
+            int tf = -1;
+            if (pos <= hr1) {
+                const uint32_t f = sidx[pos];
+                tf = static_cast<int>(tok_of(f));
+                const float vf = to_f(vals[f]), lf = lv[f];
+                const float u = __fmul_rn(vf, expf(__fsub_rn(lf, ref)));
+                if (is_q_of(f)) {
+                    vq = u;
+                } else {
+                    vk = u;
+                    vw = __fmul_rn(vf, expf(__fsub_rn(ref, lf)));
+                }
+                kbv[f] = static_cast<uint16_t>(kbv[f] | 0x8000u);   // handled densely
+            }
+            // per-token sums over the lanes (tokens are non-decreasing along the lanes): a fixed
+            // shuffle tree, the token's first lane adds them to the vectors
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float ok_ = __shfl_down_sync(kFull, vk, d);
+                const float oq = __shfl_down_sync(kFull, vq, d);
+                const float ow = __shfl_down_sync(kFull, vw, d);
+                const int ot = __shfl_down_sync(kFull, tf, d);
+                if (lane + d < 32 && ot == tf) {
+                    vk = __fadd_rn(vk, ok_);
+                    vq = __fadd_rn(vq, oq);
+                    vw = __fadd_rn(vw, ow);
+                }
+            }
+            const int tprev = __shfl_up_sync(kFull, tf, 1);
+            if (tf >= 0 && (lane == 0 || tprev != tf)) {
+                uk[tf] = __fadd_rn(uk[tf], vk);
+                uq[tf] = __fadd_rn(uq[tf], vq);
+                wk[tf] = __fadd_rn(wk[tf], vw);
+                const uint32_t hb = 1u << h;   // kHotMax <= 32
+                if (vk != 0.f) atomicOr(&hotrow[0][tf], hb);
+                if (vq != 0.f) atomicOr(&hotrow[1][tf], hb);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
     // Only rows flagged in the scan (an entry with an earlier write entry in its group) have
     // terms; the j-th flagged (triangle, row), in (triangle, row) order, goes to warp j % nw. Lane
     // u < 2 * mwords holds flag word u (A rows, then QK rows); a warp prefix of the words' counts
@@ -706,7 +827,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         for (int ab0 = 0; ab0 < lanes; ab0 += 32) {
             // the row's entries with an earlier write entry in their group, one ballot per 32
             const int eab = i * wr + (qk ? W : 0) + ab0 + lane;
-            uint32_t with = __ballot_sync(kFull, ab0 + lane < lanes && kbv[eab] != 0u);
+            uint32_t with = __ballot_sync(kFull, ab0 + lane < lanes && static_cast<uint32_t>(kbv[eab]) - 1u < 0x7FFFu);
             for (; with != 0u; with &= with - 1u) {
                 const int e = i * wr + (qk ? W : 0) + ab0 + __ffs(with) - 1;
                 const uint32_t kb = kbv[e];
@@ -736,21 +857,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     if (incl && isk && (qk || tf != i)) {
                         v = __fmul_rn(__fmul_rn(ve, to_f(vals[f])), expf(__fsub_rn(lge, lv[f])));
                     }
-                    // segmented suffix sums over lanes of equal token (tokens are non-increasing
-                    // along the lanes): a fixed shuffle tree
+                    const uint32_t terms = __ballot_sync(kFull, v != 0.f);
+                    if ((terms & (terms - 1u)) == 0u) {   // at most one term: it is the cell's sum
+                        if (v != 0.f) rowbuf[tf] = __fadd_rn(rowbuf[tf], v);
+                    } else {
+                        // segmented suffix sums over lanes of equal token (tokens are non-increasing
+                        // along the lanes): a fixed shuffle tree
 #pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const float ov = __shfl_down_sync(kFull, v, d);
-                        const int ot = __shfl_down_sync(kFull, tf, d);
-                        if (lane + d < 32 && ot == tf) v = __fadd_rn(v, ov);
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const float ov = __shfl_down_sync(kFull, v, d);
+                            const int ot = __shfl_down_sync(kFull, tf, d);
+                            if (lane + d < 32 && ot == tf) v = __fadd_rn(v, ov);
+                        }
+                        const int tprev = __shfl_up_sync(kFull, tf, 1);
+                        if (tf >= 0 && (lane == 0 || tprev != tf)) rowbuf[tf] = __fadd_rn(rowbuf[tf], v);
                     }
-                    const int tprev = __shfl_up_sync(kFull, tf, 1);
-                    if (tf >= 0 && (lane == 0 || tprev != tf)) rowbuf[tf] = __fadd_rn(rowbuf[tf], v);
                     __syncwarp();
                     met += __popc(bk);
                 }
             }
         }
+        // the rank-1 terms of the dense groups with an entry of this token, in group order
+        for (uint32_t hm = hotrow[qk ? 1 : 0][i]; hm != 0u; hm &= hm - 1u) {
+            const int h = __ffs(hm) - 1;
+            const float* const uk = hvec + h * 3 * C;
+            const float coef = qk ? uk[C + i] : uk[i];
+            if (!any) {
+                for (int j = lane; j < C; j += 32) rowbuf[j] = 0.f;
+                any = true;
+            }
+            const int jend = qk ? i + 1 : i;   // columns j < jend
+            for (int j = lane; j < jend; j += 32) rowbuf[j] = fmaf(coef, uk[2 * C + j], rowbuf[j]);
+        }
+        __syncwarp();
         if (!any) continue;   // the row stays as the zero fill left it
         float* const row = outp + (c * C + i) * static_cast<int64_t>(C);
         if (vec4) {
