@@ -877,17 +877,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 }
             }
         }
-        // the rank-1 terms of the dense groups with an entry of this token, in group order
-        for (uint32_t hm = hotrow[qk ? 1 : 0][i]; hm != 0u; hm &= hm - 1u) {
-            const int h = __ffs(hm) - 1;
-            const float* const uk = hvec + h * 3 * C;
-            const float coef = qk ? uk[C + i] : uk[i];
-            if (!any) {
-                for (int j = lane; j < C; j += 32) rowbuf[j] = 0.f;
-                any = true;
+        // the rank-1 terms of the dense groups with an entry of this token, in group order, added
+        // to the row held in registers (column lane + 32 q)
+        uint32_t hm = hotrow[qk ? 1 : 0][i];
+        if (hm != 0u) {
+            __syncwarp();
+            float racc[kMaxC / 32];
+#pragma unroll
+            for (int q = 0; q < kMaxC / 32; ++q) {
+                const int j = lane + 32 * q;
+                racc[q] = (any && j < C) ? rowbuf[j] : 0.f;
             }
             const int jend = qk ? i + 1 : i;   // columns j < jend
-            for (int j = lane; j < jend; j += 32) rowbuf[j] = fmaf(coef, uk[2 * C + j], rowbuf[j]);
+            for (; hm != 0u; hm &= hm - 1u) {
+                const float* const uk = hvec + (__ffs(hm) - 1) * 3 * C;
+                const float coef = qk ? uk[C + i] : uk[i];
+#pragma unroll
+                for (int q = 0; q < kMaxC / 32; ++q) {
+                    const int j = lane + 32 * q;
+                    if (j < jend) racc[q] = fmaf(coef, uk[2 * C + j], racc[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kMaxC / 32; ++q) {
+                const int j = lane + 32 * q;
+                if (j < C) rowbuf[j] = racc[q];
+            }
+            any = true;
         }
         __syncwarp();
         if (!any) continue;   // the row stays as the zero fill left it
