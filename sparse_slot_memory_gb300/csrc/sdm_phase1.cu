@@ -504,14 +504,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // in posv until the reverse pass replaces it with the position pack
     {
         Fwd agg = {0.f, 0.f, 0u, 0u};
-#pragma unroll 1
+#pragma unroll
         for (int k = 0; k < kItems; ++k) {
             const Fwd it = {x[k], 0.f, cnt_of(k), all_of(k) | (((headm >> k) & 1u) << 31)};
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
         zero_upto(4);
-#pragma unroll 1
+#pragma unroll
         for (int k = 0; k < kItems; ++k) {
             const uint32_t ownc = cnt_of(k), owna = all_of(k);
             const Fwd it = {x[k], 0.f, ownc, owna | (((headm >> k) & 1u) << 31)};
@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // reverse: rex, peers after, group total; then every per-entry result
     {
         Bwd agg = {0.f, 0.f, 0u, 0.f};
-#pragma unroll 1
+#pragma unroll
         for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
             const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
@@ -548,13 +548,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
         zero_upto(5);
         const int64_t kbase = c * nk, qbase = c * nq;
+        // Not unrolled (the body is large): item k's gate and entry are taken from the top of
+        // x[] / ke[], which shift up one place per iteration (register moves, no local memory).
 #pragma unroll 1
-        for (int k = kItems - 1; k >= 0; --k) {   // not unrolled: the body is large (code size)
+        for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
             const Bwd ex = run;
-            const Bwd it = {x[k], 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[ke[k]] : 0.f};
+            const float xk = x[kItems - 1];
+            const uint32_t e = ke[kItems - 1];
+#pragma unroll
+            for (int q = kItems - 1; q > 0; --q) {
+                x[q] = x[q - 1];
+                ke[q] = ke[q - 1];
+            }
+            const Bwd it = {xk, 0.f, cnt_of(k) | ((tail ? 1u : 0u) << 31), tail ? lv[e] : 0.f};
             run = bcomb(run, it);
-            const uint32_t e = ke[k];
             if (e >= static_cast<uint32_t>(n)) continue;
             const int r = r0 + k;
             const uint32_t key = keys[e];
