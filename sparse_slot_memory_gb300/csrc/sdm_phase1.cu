@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
             __syncthreads();
             if (pass < 3) zero_upto(1 + pass);
-            uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 16
+            uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 13 | digit << 21
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
                 const int p = warp * (32 * kItems) + k * 32 + lane;
@@ -429,16 +429,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 __syncwarp();
                 if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
                 __syncwarp();
-                mer[k] = e | (base + rin) << 16;
+                mer[k] = e | (base + rin) << 13 | d << 21;   // entry | rank (< 256) | digit
             }
             __syncthreads();
             block_exscan_padded(hist, nbins * nw, nw, uscr, lane, warp, nw);
             __syncthreads();
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
-                const uint32_t e = mer[k] & 0xFFFFu;
-                const uint32_t d = (keys[e] >> sh) & dmask;
-                dst[hist[d * hs + warp] + (mer[k] >> 16)] = static_cast<uint16_t>(e);
+                const uint32_t e = mer[k] & 0x1FFFu;
+                dst[hist[(mer[k] >> 21) * hs + warp] + ((mer[k] >> 13) & 0xFFu)] = static_cast<uint16_t>(e);
             }
             __syncthreads();
         }
