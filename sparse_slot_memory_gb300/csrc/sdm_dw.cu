@@ -77,8 +77,8 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
 }
 
 template <typename BankT, typename DvT>
-__global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
-    constexpr int kSub = 4;   // entries per sub-batch (4 blocks of 8 warps per SM hide the latency)
+__global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
+    constexpr int kSub = 8;   // entries per sub-batch (3 blocks of 8 warps per SM, 80 registers)
     // per warp three window buffers of 32 records (+ 8 slots read by the unrolled loads, never
     // used) and each record's first dv row (its chunk * C)
     __shared__ __align__(16) int4 recs_s[kDwWarps][3][40];
@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
                             if (w0 & kLast) bv[k].ld_cg(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu);
                         }
                     }
+                    asm volatile("" ::: "memory");   // the records are read again below, not held in registers
 #pragma unroll
                     for (int k = 0; k < K; ++k) {
                         if (k < cnt) {
