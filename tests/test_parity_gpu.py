@@ -27,6 +27,13 @@ CASES = {
     "c1_w1_r1": scaled(WORKLOADS["tiny"], P=3, T=5, C=1, S=16, hd=4, W=1, R=1, name="c1_w1_r1"),
     "bf16_hd4_ragged": scaled(WORKLOADS["uniform_c128"], P=2, T=100, C=48, S=64, hd=4, W=3, R=7,
                               name="bf16_hd4_ragged"),
+    # ~32 write entries per slot and chunk over 64 slots: more hot groups than the dense pair path
+    # takes (the rest keep the exact walk)
+    "many_hot": scaled(WORKLOADS["zipf_c256"], P=1, T=512, S=64, hd=8, idx="uniform", name="many_hot"),
+    # strongly decaying gates (logsigmoid(N(-3, 1))) over 4 slots: the groups' log-cumsums span far
+    # more than the dense path's exponent range, so they keep the exact walk
+    "wide_span": scaled(WORKLOADS["uniform_c128"], P=1, T=256, S=4, hd=8, W=4, R=4, gate_mu=-3.0,
+                        name="wide_span"),
 }
 
 
