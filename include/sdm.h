@@ -96,6 +96,8 @@ typedef struct {
  *              | min(peers before, 4095) << 18 | LAST << 30 | FIRST << 31; invalid: | 3 << 30.
  *   repeats: one int64 to which the count of repeated write entries (a token's write entry on
  *            a slot its previous write entry of the group already holds) is ADDED.
+ *   ngroups [N] int32: the chunk's valid write groups (slots with at least one valid write
+ *            entry), i.e. the rows of its dense compact snapshot (sdm_dw_saving).
  * Position pack: r | min(after, 127) << 17 | min(before + 1 + min(after, 127), 127) << 24 for a
  * valid entry (r = position in the chunk's sorted row, before / after = valid entries of the
  * same kind and slot before / after it), r alone for an invalid entry. Invalid entries:
@@ -119,6 +121,7 @@ typedef struct {
     int32_t* sorted_k;
     int32_t* sorted_q;
     int64_t* repeats;
+    int32_t* ngroups;
 } sdm_p1_out;
 
 /*
@@ -163,6 +166,28 @@ sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, cons
                               const void* k_val, const void* q_val, const float* g, const void* dv,
                               void* bank, const sdm_p1_out* out, int64_t step_begin,
                               int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);
+
+/*
+ * The saving forward's DW (mover_fx_cuda.py, module docstring; mover_da2_cuda.py, the WR mode of the
+ * DW walk): sdm_dw, and in addition every valid write group's base row -- the bank row before this
+ * step's write, as raw bytes of the bank type -- goes to the dense compact snapshot
+ *   snap [N, C*W, hd] (bank dtype, 16-byte aligned, caller-owned), row c * (C*W) + g,
+ * g = the group's dense ordinal in chunk c: the number of the chunk's valid write groups (slots with
+ * at least one valid write entry) before it in sorted order, i.e. slots ascending. Rows g >=
+ * ngroups[c] (sdm_p1_out.ngroups) are not written. The records must come from sdm_phase1 of this
+ * library version (they carry the ordinals). Bank results are those of sdm_dw, bit for bit.
+ * Errors: those of sdm_dw; snap NULL -> SDM_ERR_ARG, misaligned -> SDM_ERR_ALIGN.
+ */
+sdm_status sdm_dw_saving(const sdm_shape* shape, const void* dv, void* bank, void* snap,
+                         int64_t step_begin, int64_t step_end, void* ws, size_t ws_bytes,
+                         sdm_stream_t stream);
+
+/* sdm_phase1 then sdm_dw_saving on `stream` (arguments as sdm_forward_chunks, plus snap). */
+sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const int32_t* k_idx,
+                                     const int32_t* q_idx, const void* k_val, const void* q_val,
+                                     const float* g, const void* dv, void* bank, void* snap,
+                                     const sdm_p1_out* out, int64_t step_begin, int64_t step_end,
+                                     void* ws, size_t ws_bytes, sdm_stream_t stream);
 
 /* Bytes of the library-owned scratch used by sdm_forward_chunks_noalloc (16 MiB). */
 #define SDM_NOALLOC_SCRATCH_BYTES (16u << 20)

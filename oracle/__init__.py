@@ -147,13 +147,25 @@ def dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, *, S, V, val_dtype, bank_d
         raise ValueError("oracle: a valid slot id is outside [0, S)")
 
 
+def snapshot_slots(k_idx_c, *, S, V):
+    """The dense compact snapshot's row order of one chunk (mover_da2_cuda.py, the WR mode of the DW
+    walk; mover_fx_cuda.py module docstring): a valid write group's row is its dense ordinal, the
+    number of the chunk's valid write groups before it in sorted order. Groups are slots with at
+    least one valid write entry (token t < V, id in [0, S)); sorted order is slot order. Returns the
+    slots by ordinal."""
+    ids = np.asarray(k_idx_c)[:V].ravel().astype(np.int64)
+    return np.unique(ids[(ids >= 0) & (ids < S)])
+
+
 def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, dv_dtype, bank_dtype,
-              step_begin=0, step_end=None, round_cpe=True, round_bank=True, track=False):
+              step_begin=0, step_end=None, round_cpe=True, round_bank=True, track=False, snaps=None):
     """DW of every step in [step_begin, step_end) of one stream, in step order.
 
     ``inputs`` holds chunk-major arrays of P streams (as synth.make_inputs returns); ``p_local`` is
     the stream's index among them. ``bank`` is that stream's [S, hd] float64 rows (updated in place).
     With ``track`` returns (alt, amb, touched, mag) for tolerance bookkeeping.
+    With ``snaps`` (a list) appends, per chunk, its snapshot slots and their rows before the chunk's
+    DW (and, with ``track``, the same bookkeeping for those rows).
     """
     step_end = steps if step_end is None else step_end
     hd = bank.shape[1]
@@ -165,6 +177,11 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
         c = ti * P + p_local
         V = valid_last if ti == steps - 1 else C
         dv = as_f64(inputs["dv"][c * C:(c + 1) * C], dv_dtype).reshape(C, hd)
+        if snaps is not None:   # the saving forward: the groups' base rows before this step
+            sl = snapshot_slots(inputs["k_idx"][c], S=S, V=V)
+            snaps.append({"c": c, "slots": sl, "rows": bank[sl].copy(),
+                          **({"alt": alt[sl].copy(), "amb": amb[sl].copy(), "touched": touched[sl].copy(),
+                              "mag": mag[sl].copy()} if track else {})})
         dw_chunk(bank, inputs["k_idx"][c], inputs["q_idx"][c], inputs["k_val"][c], inputs["q_val"][c],
                  inputs["g"][c], dv, S=S, V=V, val_dtype=val_dtype, bank_dtype=bank_dtype,
                  round_cpe=round_cpe, round_bank=round_bank, alt=alt, amb=amb, touched=touched, mag=mag)

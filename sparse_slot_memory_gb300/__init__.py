@@ -11,10 +11,13 @@ from .api import (  # noqa: F401
     SdmError,
     ShapeSpec,
     alloc_outputs,
+    alloc_snapshot,
     alloc_workspace,
     device_status,
     dw,
+    dw_saving,
     forward_chunks,
+    forward_chunks_saving,
     forward_chunks_noalloc,
     phase1,
     workspace_bytes,

@@ -15,7 +15,8 @@ SDM_DEV_BAD_SLOT = 0x1
 
 # every symbol include/sdm.h declares
 EXPORTS = ("sdm_workspace_bytes", "sdm_workspace_init", "sdm_phase1", "sdm_dw", "sdm_forward_chunks",
-           "sdm_forward_chunks_noalloc", "sdm_device_status", "sdm_status_string")
+           "sdm_dw_saving", "sdm_forward_chunks_saving", "sdm_forward_chunks_noalloc", "sdm_device_status",
+           "sdm_status_string")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -26,7 +27,7 @@ class Shape(ctypes.Structure):
 
 
 P1_FIELDS = ("log_k", "rex", "cpe", "k_eff", "is_last", "is_only", "pos_k", "log_q", "q_w", "pos_q", "q_last",
-             "q_only", "A", "QK", "sorted_k", "sorted_q", "repeats")
+             "q_only", "A", "QK", "sorted_k", "sorted_q", "repeats", "ngroups")
 
 
 class P1Out(ctypes.Structure):
@@ -56,6 +57,11 @@ def load(path: str = LIB):
     lib.sdm_dw.argtypes = [sp, c_p, c_p, c_i64, c_i64, c_p, c_sz, c_p]
     lib.sdm_forward_chunks.restype = c_i32
     lib.sdm_forward_chunks.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_sz, c_p]
+    lib.sdm_dw_saving.restype = c_i32
+    lib.sdm_dw_saving.argtypes = [sp, c_p, c_p, c_p, c_i64, c_i64, c_p, c_sz, c_p]
+    lib.sdm_forward_chunks_saving.restype = c_i32
+    lib.sdm_forward_chunks_saving.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_sz,
+                                              c_p]
     lib.sdm_forward_chunks_noalloc.restype = c_i32
     lib.sdm_forward_chunks_noalloc.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_p]
     lib.sdm_device_status.restype = c_i32

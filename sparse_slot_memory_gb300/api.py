@@ -99,6 +99,7 @@ def alloc_outputs(shape: ShapeSpec, device="cuda", fields=_abi.P1_FIELDS) -> dic
         "pos_q": ((N, C, R), torch.int32), "q_last": ((N, C, R), torch.int8), "q_only": ((N, C, R), torch.int8),
         "A": ((N, C, C), torch.float32), "QK": ((N, C, C), torch.float32),
         "sorted_k": ((N, C * W), torch.int32), "sorted_q": ((N, C * R), torch.int32), "repeats": ((2,), torch.int64),
+        "ngroups": ((N,), torch.int32),
     }
     out = {}
     for f in fields:
@@ -139,6 +140,31 @@ def forward_chunks(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, ou
                                         _ptr(g), _ptr(dv), _ptr(bank), ctypes.byref(o) if out else None, step_begin,
                                         step_end, _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "sdm_forward_chunks")
+
+
+def alloc_snapshot(shape: ShapeSpec, device="cuda") -> torch.Tensor:
+    """The dense compact snapshot of the saving forward: [N, C*W, hd] rows of the bank type."""
+    return torch.empty((shape.N, shape.C * shape.W, shape.hd), dtype=_TORCH_DT[shape.bank_dtype], device=device)
+
+
+def dw_saving(shape: ShapeSpec, dv, bank, snap, ws, step_begin=0, step_end=None, stream=None):
+    """sdm_dw_saving: the DW, also writing each group's pre-write base row to ``snap``."""
+    step_end = shape.steps if step_end is None else step_end
+    st = _abi.load().sdm_dw_saving(ctypes.byref(shape.c()), _ptr(dv), _ptr(bank), _ptr(snap), step_begin, step_end,
+                                   _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "sdm_dw_saving")
+
+
+def forward_chunks_saving(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, snap, out, ws, step_begin=0,
+                          step_end=None, stream=None):
+    """sdm_forward_chunks_saving: Phase 1, then the DW writing the dense compact snapshot."""
+    step_end = shape.steps if step_end is None else step_end
+    o = _p1out(out)
+    st = _abi.load().sdm_forward_chunks_saving(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val),
+                                               _ptr(q_val), _ptr(g), _ptr(dv), _ptr(bank), _ptr(snap),
+                                               ctypes.byref(o) if out else None, step_begin, step_end, _ptr(ws),
+                                               ws.numel(), _stream(stream))
+    _check(st, "sdm_forward_chunks_saving")
 
 
 def forward_chunks_noalloc(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, out, status=None, step_begin=0,

@@ -106,7 +106,7 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
         if (hist_end > g->sm_scr) o += hist_end - g->sm_scr;
         g->zero_bytes = zb;
         g->smem_bytes = round_up(o, 128);
-        if (g->smem_bytes + 4096 <= kSmemOptin) break;   // room for the static arrays too
+        if (g->smem_bytes + 6144 <= kSmemOptin) break;   // room for the static arrays too
     }
     return SDM_OK;
 }
@@ -179,8 +179,8 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
 }
 
-sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* bank, int64_t b, int64_t e, void* ws,
-                  cudaStream_t stream) {
+sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* bank, void* snap, int64_t b, int64_t e,
+                  void* ws, cudaStream_t stream) {
     unsigned char* const w = static_cast<unsigned char*>(ws);
     // the work counter starts at zero for every launch (the status word is kept)
     if (cudaMemsetAsync(w + kHdrClaim, 0, sizeof(uint32_t), stream) != cudaSuccess) return SDM_ERR_CUDA;
@@ -190,9 +190,11 @@ sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* b
     a.bb = reinterpret_cast<const int32_t*>(w + g.bb_off);
     a.dv = dv;
     a.bank = bank;
+    a.snap = snap;
     a.claim = reinterpret_cast<uint32_t*>(w + kHdrClaim);
     a.P = g.P;
     a.C = g.C;
+    a.W = g.W;
     a.nk = g.nk;
     a.B = g.B;
     a.nsl = g.nsl;
@@ -214,7 +216,7 @@ sdm_status check_p1_args(const Geometry& g, const int32_t* k_idx, const int32_t*
     if (out != nullptr) {
         const void* ptrs[] = {out->log_k, out->rex, out->cpe, out->k_eff, out->is_last, out->is_only,
                               out->pos_k, out->log_q, out->q_w, out->pos_q, out->q_last, out->q_only,
-                              out->A, out->QK, out->sorted_k, out->sorted_q, out->repeats};
+                              out->A, out->QK, out->sorted_k, out->sorted_q, out->repeats, out->ngroups};
         for (const void* p : ptrs)
             if (p != nullptr && !aligned16(p)) return SDM_ERR_ALIGN;
     }
@@ -274,7 +276,7 @@ extern "C" sdm_status sdm_dw(const sdm_shape* shape, const void* dv, void* bank,
     if (!aligned16(dv) || !aligned16(bank)) return SDM_ERR_ALIGN;
     if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
     if (step_begin == step_end) return SDM_OK;
-    return run_dw(shape, geo, dv, bank, step_begin, step_end, ws, reinterpret_cast<cudaStream_t>(stream));
+    return run_dw(shape, geo, dv, bank, nullptr, step_begin, step_end, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
@@ -294,7 +296,41 @@ extern "C" sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* 
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
         return st;
-    return run_dw(shape, geo, dv, bank, step_begin, step_end, ws, cs);
+    return run_dw(shape, geo, dv, bank, nullptr, step_begin, step_end, ws, cs);
+}
+
+// ---- the saving forward: DW also writes the dense compact snapshot ------------------------------
+extern "C" sdm_status sdm_dw_saving(const sdm_shape* shape, const void* dv, void* bank, void* snap, int64_t step_begin,
+                                    int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if (dv == nullptr || bank == nullptr || snap == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(dv) || !aligned16(bank) || !aligned16(snap)) return SDM_ERR_ALIGN;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    return run_dw(shape, geo, dv, bank, snap, step_begin, step_end, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                                                const void* k_val, const void* q_val, const float* g, const void* dv,
+                                                void* bank, void* snap, const sdm_p1_out* out, int64_t step_begin,
+                                                int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if ((st = check_p1_args(geo, k_idx, q_idx, k_val, q_val, g, out)) != SDM_OK) return st;
+    if (dv == nullptr || bank == nullptr || snap == nullptr) return SDM_ERR_ARG;
+    if (!aligned16(dv) || !aligned16(bank) || !aligned16(snap)) return SDM_ERR_ALIGN;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if ((st = check_smem(geo)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
+        return st;
+    return run_dw(shape, geo, dv, bank, snap, step_begin, step_end, ws, cs);
 }
 
 // ---- the no-allocation forward ----------------------------------------------------------------
@@ -343,7 +379,7 @@ extern "C" sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const i
     if (step_begin < step_end) {
         if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
             return st;
-        if ((st = run_dw(shape, geo, dv, bank, step_begin, step_end, ws, cs)) != SDM_OK) return st;
+        if ((st = run_dw(shape, geo, dv, bank, nullptr, step_begin, step_end, ws, cs)) != SDM_OK) return st;
     }
     if (status_out != nullptr &&
         cudaMemcpyAsync(status_out, static_cast<unsigned char*>(ws) + kHdrStatus, sizeof(int32_t),

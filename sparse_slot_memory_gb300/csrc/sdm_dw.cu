@@ -64,6 +64,12 @@ struct Raw4<__nv_bfloat16> {
     }
 };
 
+// the row's raw bytes (the dense snapshot is a copy of the base row)
+__device__ __forceinline__ void st_raw(float* p, const Raw4<float>& r) { *reinterpret_cast<float4*>(p) = r.v; }
+__device__ __forceinline__ void st_raw(__nv_bfloat16* p, const Raw4<__nv_bfloat16>& r) {
+    *reinterpret_cast<uint2*>(p) = r.v;
+}
+
 __device__ __forceinline__ void st4(float* p, const float (&o)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
 }
@@ -76,7 +82,8 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
     *reinterpret_cast<uint2*>(p) = u;
 }
 
-template <typename BankT, typename DvT>
+// SNAP: the saving forward (a.snap is the dense compact snapshot)
+template <typename BankT, typename DvT, bool SNAP>
 __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
     constexpr int kSub = 8;   // entries per sub-batch (3 blocks of 8 warps per SM, 80 registers)
     // per warp three window buffers of 32 records (+ 8 slots read by the unrolled loads, never
@@ -148,6 +155,7 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
             cp_async_wait_all();
             __syncwarp();
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t gord = 0;   // the current group's dense ordinal (from its FIRST record)
             for (int w = 0; w < nwin; ++w) {
                 const int s = w % 3;
                 if (w + 2 < nwin) fetch(w + 2, (w + 2) % 3);
@@ -183,9 +191,14 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                             const int4 r = rs[m + k];
                             const uint32_t w0 = static_cast<uint32_t>(r.x);
                             const float sc = __int_as_float(r.z);
+                            if (SNAP && (w0 & kFirst)) gord = (w0 >> kRecOrdShift) & kRecOrdMask;
 #pragma unroll
                             for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
                             if (w0 & kLast) {
+                                if (SNAP && active)   // saving forward: the base row, raw
+                                    st_raw(static_cast<BankT*>(a.snap) +
+                                               (static_cast<uint64_t>(ds[m + k]) * a.W + gord) * hdu + col,
+                                           bv[k]);
                                 if (active) {
                                     const float cp = __int_as_float(r.w);
                                     float o[4];
@@ -216,22 +229,27 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
     }
 }
 
-template <typename BankT, typename DvT>
-cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
+template <typename BankT, typename DvT, bool SNAP>
+cudaError_t launch_t1(const DWArgs& a, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dw_kernel<BankT, DvT>, kDwThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dw_kernel<BankT, DvT, SNAP>, kDwThreads, 0);
     if (e != cudaSuccess) return e;
     per_sm = per_sm < 1 ? 1 : per_sm;
     int64_t blocks = static_cast<int64_t>(sms) * per_sm;
     const int64_t need_blocks = (a.items + kDwWarps - 1) / kDwWarps;
     if (blocks > need_blocks) blocks = need_blocks;
     if (blocks < 1) blocks = 1;
-    dw_kernel<BankT, DvT><<<static_cast<unsigned>(blocks), kDwThreads, 0, stream>>>(a);
+    dw_kernel<BankT, DvT, SNAP><<<static_cast<unsigned>(blocks), kDwThreads, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+template <typename BankT, typename DvT>
+cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
+    return a.snap != nullptr ? launch_t1<BankT, DvT, true>(a, stream) : launch_t1<BankT, DvT, false>(a, stream);
 }
 
 }  // namespace

@@ -52,10 +52,15 @@ constexpr size_t kSmemOptin = 232448;          // opt-in shared memory per block
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
 
 // DW record of one valid write entry (16 bytes, one vector load), grouped by slot bucket:
-//   x = token | LAST << 30 | FIRST << 31 | kRecInvalid, y = stream-local slot,
+//   x = token | group ordinal << 16 (FIRST records) | LAST << 30 | FIRST << 31 | kRecInvalid,
+//   y = stream-local slot,
 //   z = f32 bits of sc = k * expf(rex), w = f32 bits of cpe (the value-type cpe widened).
 constexpr uint32_t kRecInvalid = 1u << 29;
 constexpr uint32_t kRecTokMask = 0xFFFFu;
+// the group's dense ordinal in its chunk (valid write groups before it in sorted order), carried by
+// the group's FIRST record: the row of the dense compact snapshot
+constexpr int kRecOrdShift = 16;
+constexpr uint32_t kRecOrdMask = 0x1FFFu;
 
 // Workspace header (bytes): [0] status word, [4] the DW work counter.
 constexpr size_t kHdrStatus = 0;
@@ -108,8 +113,9 @@ struct DWArgs {
     const int32_t* bb;  // [P][B + 1][steps]
     const void* dv;
     void* bank;
+    void* snap;         // dense compact snapshot [N, C*W, hd] (bank type) or null
     uint32_t* claim;    // work counter
-    int P, C, nk, B, nsl, hd;
+    int P, C, W, nk, B, nsl, hd;
     int64_t S, steps;
     int64_t step_begin, step_end;
     int64_t items;      // P * B * nsl

@@ -286,11 +286,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     __shared__ int hot_n;
     // per (triangle, token): the dense groups with a term in the token's A (0) / QK (1) row
     __shared__ uint32_t hotrow[2][kMaxC];
+    // write-row positions of the valid write groups' first entries (bit per position) and, per
+    // 32-bit word, the groups before it: a group's dense ordinal in the chunk
+    __shared__ uint32_t khead[kMaxRow / 32], kheadp[kMaxRow / 32 + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
     for (int i = tid; i < kMaxRow / 32; i += blockDim.x) hotmask[i] = 0u;
     for (int i = tid; i < 2 * kMaxC; i += blockDim.x) hotrow[i / kMaxC][i % kMaxC] = 0u;
+    for (int i = tid; i < kMaxRow / 32; i += blockDim.x) khead[i] = 0u;
     // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
     // use by the sort's barriers
     const int nbk = 1 << a.logB;
@@ -596,7 +600,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 cpev[o] = cpe_f;
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
-                if (valid && before == 0) atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
+                if (valid && before == 0) {
+                    atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
+                    atomicOr(&khead[jx >> 5], 1u << (jx & 31u));
+                }
                 if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
             }
         }
@@ -620,6 +627,32 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
         zero_upto(6);
+        if (warp == 0) {   // groups before each word of the write row (lane: 8 words)
+            const int nwords = (nk + 31) >> 5;
+            uint32_t cnt = 0;
+            for (int q = 0; q < 8; ++q) {
+                const int wi = lane * 8 + q;
+                if (wi < nwords) cnt += __popc(khead[wi]);
+            }
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, d);
+                if (lane >= d) incl += y;
+            }
+            uint32_t run = incl - cnt;
+            for (int q = 0; q < 8; ++q) {
+                const int wi = lane * 8 + q;
+                if (wi < nwords) {
+                    kheadp[wi] = run;
+                    run += __popc(khead[wi]);
+                }
+            }
+            if (lane == 31) {
+                kheadp[nwords] = incl;
+                if (a.out.ngroups != nullptr) a.out.ngroups[c] = static_cast<int32_t>(incl);
+            }
+        }
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
         for (int j = tid; j < nk; j += nthr) {
@@ -640,7 +673,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const uint32_t t = tok_of(e);
             const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
             const bool last = ((posv[e] >> kPosAfterShift) & kPosCountMax) == 0u;
-            const uint32_t w0 = t | (kb == 0u ? kFirst : 0u) | (last ? kLast : 0u);
+            uint32_t w0 = t | (last ? kLast : 0u);
+            if (kb == 0u)   // FIRST: the group's dense ordinal
+                w0 |= kFirst | (kheadp[j >> 5] + __popc(khead[j >> 5] & ((1u << (j & 31)) - 1u))) << kRecOrdShift;
             const float sc = __fmul_rn(to_f(vals[e]), expf(rexv[o]));
             st_stream(a.krec + kbase + rec, make_int4(static_cast<int>(w0), static_cast<int>(key), __float_as_int(sc),
                                                       __float_as_int(cpev[o])));

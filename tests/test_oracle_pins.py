@@ -25,7 +25,7 @@ import numpy as np
 import pytest
 
 import oracle
-from synth import WORKLOADS, f32_to_bf16_bits, make_inputs, scaled
+from synth import WORKLOADS, f32_to_bf16_bits, make_bank_stream, make_inputs, scaled
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -417,3 +417,45 @@ def test_planted_mistake_is_caught(name, tmp_path):
     lib = oracle.load_variant(so)
     assert not _pins_pass(lib), f"planted mistake '{name}' was not caught by the pins"
     shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+def test_snapshot_order_hand_example():
+    """The dense snapshot's rows follow the chunk's valid write groups in slot order: ids of invalid
+    tokens (t >= V), -1 and ids outside [0, S) form no group (mover_da2_cuda.py, WR mode)."""
+    k = np.array([[3, 7, 3], [11, -1, 0], [5, 5, 5]], np.int32)
+    assert oracle.snapshot_slots(k, S=10, V=2).tolist() == [0, 3, 7]
+    assert oracle.snapshot_slots(k, S=10, V=3).tolist() == [0, 3, 5, 7]
+
+
+@pytest.mark.parametrize("case", ["tiny_scaled", "zipf_small"])
+def test_snapshot_order_matches_sorted_row_groups(case):
+    """The dense ordinal of a group (valid write groups before it in the sorted write row, from the
+    oracle's Phase-1 sorted_k FIRST flags) is the slot's rank in snapshot_slots."""
+    w = {"tiny_scaled": scaled(WORKLOADS["tiny"], T=256), "zipf_small": scaled(WORKLOADS["zipf_c256"], P=1, T=512)}[case]
+    x = make_inputs(w)
+    orc = oracle.phase1(x["k_idx"], x["q_idx"], x["k_val"], x["q_val"], x["g"], S=w.S, val_dtype=w.val_dtype,
+                        valid_last=w.valid_last, first_partial=(w.steps - 1) * w.P)
+    for c in range(w.N):
+        V = w.valid_last if c >= (w.steps - 1) * w.P else w.C
+        el = orc["sorted_k"][c].astype(np.int64) & 0xFFFFFFFF
+        first = ((el >> 31) & 1 == 1) & ((el >> 17) & 1 == 0)
+        e = el[first] & 0x3FFFF
+        t, lane = e >> 9, e & 0xFF
+        heads = x["k_idx"][c][t, lane]
+        assert heads.tolist() == oracle.snapshot_slots(x["k_idx"][c], S=w.S, V=V).tolist()
+
+
+def test_snapshot_rows_are_the_pre_step_bank():
+    """The captured rows of step t are the stream's rows after the DW of steps [0, t)."""
+    w = scaled(WORKLOADS["tiny"], T=512, S=256)
+    x = make_inputs(w)
+    init = make_bank_stream(w, 0).astype(np.float64)
+    kw = dict(S=w.S, C=w.C, P=w.P, steps=w.steps, valid_last=w.valid_last, val_dtype=w.val_dtype,
+              dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype)
+    snaps = []
+    oracle.dw_stream(init.copy(), x, 0, snaps=snaps, **kw)
+    for t in (0, 3, w.steps - 1):
+        b = init.copy()
+        oracle.dw_stream(b, x, 0, step_end=t, **kw)
+        sn = snaps[t]
+        assert sn["c"] == t and np.array_equal(sn["rows"], b[sn["slots"]])
