@@ -165,7 +165,8 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
     the stream's index among them. ``bank`` is that stream's [S, hd] float64 rows (updated in place).
     With ``track`` returns (alt, amb, touched, mag) for tolerance bookkeeping.
     With ``snaps`` (a list) appends, per chunk, its snapshot slots and their rows before the chunk's
-    DW (and, with ``track``, the same bookkeeping for those rows).
+    DW (and, with ``track``, the same bookkeeping for those rows plus ``peak``, the largest |value|
+    each row has held so far).
     """
     step_end = steps if step_end is None else step_end
     hd = bank.shape[1]
@@ -173,6 +174,7 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
     amb = np.zeros(S, np.int32) if track else None
     touched = np.zeros(S, np.int32) if track else None
     mag = np.zeros_like(bank) if track else None
+    peak = np.abs(bank) if (snaps is not None and track) else None   # largest |value| each row has held
     for ti in range(step_begin, step_end):
         c = ti * P + p_local
         V = valid_last if ti == steps - 1 else C
@@ -181,10 +183,12 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
             sl = snapshot_slots(inputs["k_idx"][c], S=S, V=V)
             snaps.append({"c": c, "slots": sl, "rows": bank[sl].copy(),
                           **({"alt": alt[sl].copy(), "amb": amb[sl].copy(), "touched": touched[sl].copy(),
-                              "mag": mag[sl].copy()} if track else {})})
+                              "mag": mag[sl].copy(), "peak": peak[sl].copy()} if track else {})})
         dw_chunk(bank, inputs["k_idx"][c], inputs["q_idx"][c], inputs["k_val"][c], inputs["q_val"][c],
                  inputs["g"][c], dv, S=S, V=V, val_dtype=val_dtype, bank_dtype=bank_dtype,
                  round_cpe=round_cpe, round_bank=round_bank, alt=alt, amb=amb, touched=touched, mag=mag)
+        if peak is not None:
+            np.maximum(peak, np.abs(bank), out=peak)
     if track:
         return alt, amb, touched, mag
     return None

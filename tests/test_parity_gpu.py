@@ -239,3 +239,22 @@ def test_host_checks_before_launch():
     with pytest.raises(sdm.SdmError) as e:
         sdm.dw(shape, d["dv"], bank, ws, 2, 1)
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("name", ["uniform_c128", "zipf_c256", "few_slots", "one_slot"])
+def test_one_launch_equals_per_step_launches(name):
+    """One DW launch over every step (windows of records spanning steps, sub-batches cut before a
+    repeated slot) gives the bits of one launch per step (each step's loads after the previous
+    step's stores): the per-step definition, in program order."""
+    w, x, shape, d, ws = _setup(name)
+    run_phase1(shape, d, ws, fields=("repeats",))
+    P, S, hd = x["P"], w.S, w.hd
+    init = _init_bank(w, P).reshape(P * S, hd)
+    b1 = _bank_dev(init, w.bank_dtype)
+    b2 = _bank_dev(init, w.bank_dtype)
+    sdm.dw(shape, d["dv"], b1, ws)
+    for t in range(w.steps):
+        sdm.dw(shape, d["dv"], b2, ws, t, t + 1)
+    torch.cuda.synchronize()
+    assert sdm.device_status(ws) == 0
+    assert torch.equal(b1, b2)

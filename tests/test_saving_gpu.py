@@ -90,13 +90,22 @@ def test_saving_forward_snapshot(name):
             assert ng[c] == G, f"chunk {c}: {ng[c]} groups, oracle {G}"
             assert np.array_equal(snap_raw[c, G:], sent_raw[c, G:]), f"chunk {c}: rows past ngroups written"
             got, exact = snap_h[c, :G], sn["rows"]
-            k = np.maximum(sn["touched"], 1)[:, None].astype(np.float64)
+            # The rows after k earlier writes: each write rounds once on either side (GPU and oracle
+            # may land one unit of the last place apart, a unit of the value written then, which can
+            # be larger than the row's current one) and carries the earlier difference scaled by
+            # cpe <= 1; so k units at the row's largest magnitude so far, plus the f32 accumulation.
+            k = sn["touched"][:, None].astype(np.float64)
             if w.bank_dtype == "bf16":
-                tol = k * (ulp_bf16(exact) + 2.0 ** -17 * sn["mag"])
+                tol = k * (2.0 ** -7 * sn["peak"] + 2.0 ** -17 * sn["mag"])
             else:
-                tol = k * (1e-5 * sn["mag"]) + 1e-30
+                tol = k * (1e-5 * np.maximum(sn["peak"], sn["mag"])) + 1e-30
             ok = (np.abs(got - exact) <= tol) | ((sn["amb"][:, None] > 0) & (np.abs(got - sn["alt"]) <= tol))
-            assert ok.all(), f"chunk {c}: {int((~ok).sum())} snapshot elements beyond tolerance"
+            if not ok.all():
+                i, j = np.argwhere(~ok)[0]
+                raise AssertionError(f"chunk {c}: {int((~ok).sum())} snapshot elements beyond tolerance, first "
+                                     f"[{i},{j}] slot {sn['slots'][i]}: gpu {got[i, j]!r} oracle {exact[i, j]!r} "
+                                     f"alt {sn['alt'][i, j]!r} amb {sn['amb'][i]} touched {sn['touched'][i]} "
+                                     f"mag {sn['mag'][i, j]!r} tol {tol[i, j]!r}")
 
 
 @pytest.mark.parametrize("name", ["uniform_c128", "zipf_c256", "few_slots"])
