@@ -122,9 +122,10 @@ def count_groups(x, w):
     return total
 
 
-def algorithmic_bytes(w, x, groups):
+def algorithmic_bytes(w, x, groups, saving=False):
     """Bytes per forward (SURVEY section 8(d) accounting): inputs read once, outputs written once,
-    dv rows read once, per slot group one base-row read and one row write."""
+    dv rows read once, per slot group one base-row read and one row write (the saving forward:
+    and one snapshot row write)."""
     vt = 2 if w.val_dtype == "bf16" else 4
     dvt = 2 if w.dv_dtype == "bf16" else 4
     bt = 2 if w.bank_dtype == "bf16" else 4
@@ -132,7 +133,7 @@ def algorithmic_bytes(w, x, groups):
     tok = N * C
     p1_in = tok * (W * (4 + vt) + R * (4 + vt) + 4)
     p1_out = tok * (W * (4 + 4 + vt + vt + 1 + 1 + 4) + R * (4 + vt + 4 + 1 + 1)) + N * C * C * 4 * 2
-    dw = tok * w.hd * dvt + groups * w.hd * bt * 2
+    dw = tok * w.hd * dvt + groups * w.hd * bt * (3 if saving else 2)
     return {"phase1": p1_in + p1_out, "dw": dw, "total": p1_in + p1_out + dw}
 
 
@@ -177,10 +178,20 @@ def run_ours(args):
     ws = sdm.alloc_workspace(shape)
     out = sdm.alloc_outputs(shape)
     stream = torch.cuda.current_stream()
+    # the saving forward also writes the dense compact snapshot (one base row per group)
+    snap = sdm.alloc_snapshot(shape) if args.saving else None
+
+    def dw():
+        if snap is None:
+            sdm.dw(shape, d["dv"], bank, ws)
+        else:
+            sdm.dw_saving(shape, d["dv"], bank, snap, ws)
+
+    p1 = sdm.phase1 if snap is None else sdm.phase1_saving
 
     def step():
-        sdm.phase1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
-        sdm.dw(shape, d["dv"], bank, ws)
+        p1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
+        dw()
 
     for _ in range(args.warmup):
         step()
@@ -198,9 +209,9 @@ def run_ours(args):
         t0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            sdm.phase1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
+            p1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
             ev[i][1].record(stream)
-            sdm.dw(shape, d["dv"], bank, ws)
+            dw()
             ev[i][2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
@@ -230,7 +241,11 @@ def run_ours(args):
             for k, v in pin.items():
                 dst = d[k].view(torch.int16) if dts[k] == "bf16" else d[k]
                 dst.copy_(v, non_blocking=True)
-            sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws)
+            if snap is None:
+                sdm.forward_chunks(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, out, ws)
+            else:
+                sdm.forward_chunks_saving(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank,
+                                          snap, out, ws)
             for k, v in out.items():
                 outs_h[k].copy_(v, non_blocking=True)
 
@@ -255,7 +270,7 @@ def run_ours(args):
                "note": "inputs H2D from pinned host memory and every Phase-1 output D2H each step; the bank is resident state"}
 
     groups = count_groups(x, w)
-    ab = algorithmic_bytes(w, x, groups)
+    ab = algorithmic_bytes(w, x, groups, saving=args.saving)
     peak, peak_kind = peaks()
     dom = "dw" if dw_ms >= p1_ms else "phase1"
     dom_ms = dw_ms if dom == "dw" else p1_ms
@@ -270,7 +285,7 @@ def run_ours(args):
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.val_dtype, "data": "synthetic (seeded generators of the workload's distributions)",
-            "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+            "config": {"workload": w.name + ("+saving" if args.saving else ""), **{k: v for k, v in w.describe().items() if k != "workload"},
                        "tokens_per_step_per_gpu": tokens, "parallelism": f"replicas x{world} (independent streams)",
                        "l2": "inputs larger than L2 (8 GiB bank)"},
             "hbm_gbs_total": ab["total"] / (ms / 1e3) / 1e9,
@@ -365,6 +380,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--streams", type=int, default=0, help="override the workload's stream count (profiling runs)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slots per stream (profiling runs)")
+    ap.add_argument("--saving", action="store_true", help="time the saving forward (DW writes the dense snapshot)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

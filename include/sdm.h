@@ -97,7 +97,8 @@ typedef struct {
  *   repeats: one int64 to which the count of repeated write entries (a token's write entry on
  *            a slot its previous write entry of the group already holds) is ADDED.
  *   ngroups [N] int32: the chunk's valid write groups (slots with at least one valid write
- *            entry), i.e. the rows of its dense compact snapshot (sdm_dw_saving).
+ *            entry), i.e. the rows of its dense compact snapshot; written only by the saving
+ *            forward's Phase 1 (sdm_phase1_saving, sdm_forward_chunks_saving).
  * Position pack: r | min(after, 127) << 17 | min(before + 1 + min(after, 127), 127) << 24 for a
  * valid entry (r = position in the chunk's sorted row, before / after = valid entries of the
  * same kind and slot before / after it), r alone for an invalid entry. Invalid entries:
@@ -168,21 +169,31 @@ sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* k_idx, cons
                               int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream);
 
 /*
+ * Phase 1 of the saving forward: sdm_phase1, and in addition each group's FIRST DW record carries
+ * the group's dense ordinal (below) and out->ngroups is written. Its records serve sdm_dw_saving
+ * (and sdm_dw); the records of sdm_phase1 serve sdm_dw only. Errors: those of sdm_phase1.
+ */
+sdm_status sdm_phase1_saving(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                             const void* k_val, const void* q_val, const float* g,
+                             const sdm_p1_out* out, int64_t step_begin, int64_t step_end, void* ws,
+                             size_t ws_bytes, sdm_stream_t stream);
+
+/*
  * The saving forward's DW (mover_fx_cuda.py, module docstring; mover_da2_cuda.py, the WR mode of the
  * DW walk): sdm_dw, and in addition every valid write group's base row -- the bank row before this
  * step's write, as raw bytes of the bank type -- goes to the dense compact snapshot
  *   snap [N, C*W, hd] (bank dtype, 16-byte aligned, caller-owned), row c * (C*W) + g,
  * g = the group's dense ordinal in chunk c: the number of the chunk's valid write groups (slots with
  * at least one valid write entry) before it in sorted order, i.e. slots ascending. Rows g >=
- * ngroups[c] (sdm_p1_out.ngroups) are not written. The records must come from sdm_phase1 of this
- * library version (they carry the ordinals). Bank results are those of sdm_dw, bit for bit.
+ * ngroups[c] (sdm_p1_out.ngroups) are not written. The records must come from sdm_phase1_saving
+ * (they carry the ordinals). Bank results are those of sdm_dw, bit for bit.
  * Errors: those of sdm_dw; snap NULL -> SDM_ERR_ARG, misaligned -> SDM_ERR_ALIGN.
  */
 sdm_status sdm_dw_saving(const sdm_shape* shape, const void* dv, void* bank, void* snap,
                          int64_t step_begin, int64_t step_end, void* ws, size_t ws_bytes,
                          sdm_stream_t stream);
 
-/* sdm_phase1 then sdm_dw_saving on `stream` (arguments as sdm_forward_chunks, plus snap). */
+/* sdm_phase1_saving then sdm_dw_saving on `stream` (arguments as sdm_forward_chunks, plus snap). */
 sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const int32_t* k_idx,
                                      const int32_t* q_idx, const void* k_val, const void* q_val,
                                      const float* g, const void* dv, void* bank, void* snap,

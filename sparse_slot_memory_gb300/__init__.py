@@ -20,5 +20,6 @@ from .api import (  # noqa: F401
     forward_chunks_saving,
     forward_chunks_noalloc,
     phase1,
+    phase1_saving,
     workspace_bytes,
 )

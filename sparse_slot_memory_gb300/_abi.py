@@ -15,7 +15,7 @@ SDM_DEV_BAD_SLOT = 0x1
 
 # every symbol include/sdm.h declares
 EXPORTS = ("sdm_workspace_bytes", "sdm_workspace_init", "sdm_phase1", "sdm_dw", "sdm_forward_chunks",
-           "sdm_dw_saving", "sdm_forward_chunks_saving", "sdm_forward_chunks_noalloc", "sdm_device_status",
+           "sdm_phase1_saving", "sdm_dw_saving", "sdm_forward_chunks_saving", "sdm_forward_chunks_noalloc", "sdm_device_status",
            "sdm_status_string")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -57,6 +57,8 @@ def load(path: str = LIB):
     lib.sdm_dw.argtypes = [sp, c_p, c_p, c_i64, c_i64, c_p, c_sz, c_p]
     lib.sdm_forward_chunks.restype = c_i32
     lib.sdm_forward_chunks.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_sz, c_p]
+    lib.sdm_phase1_saving.restype = c_i32
+    lib.sdm_phase1_saving.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_sz, c_p]
     lib.sdm_dw_saving.restype = c_i32
     lib.sdm_dw_saving.argtypes = [sp, c_p, c_p, c_p, c_i64, c_i64, c_p, c_sz, c_p]
     lib.sdm_forward_chunks_saving.restype = c_i32

@@ -89,7 +89,11 @@ def alloc_workspace(shape: ShapeSpec, device="cuda", stream=None) -> torch.Tenso
     return ws
 
 
-def alloc_outputs(shape: ShapeSpec, device="cuda", fields=_abi.P1_FIELDS) -> dict:
+# every Phase-1 output but ngroups (written only by the saving forward's Phase 1)
+PLAIN_FIELDS = tuple(f for f in _abi.P1_FIELDS if f != "ngroups")
+
+
+def alloc_outputs(shape: ShapeSpec, device="cuda", fields=PLAIN_FIELDS) -> dict:
     N, C, W, R = shape.N, shape.C, shape.W, shape.R
     vt = _TORCH_DT[shape.val_dtype]
     spec = {
@@ -145,6 +149,17 @@ def forward_chunks(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, ou
 def alloc_snapshot(shape: ShapeSpec, device="cuda") -> torch.Tensor:
     """The dense compact snapshot of the saving forward: [N, C*W, hd] rows of the bank type."""
     return torch.empty((shape.N, shape.C * shape.W, shape.hd), dtype=_TORCH_DT[shape.bank_dtype], device=device)
+
+
+def phase1_saving(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws, step_begin=0, step_end=None,
+                  stream=None):
+    """sdm_phase1_saving: Phase 1 whose records carry the groups' dense ordinals (for dw_saving)."""
+    step_end = shape.steps if step_end is None else step_end
+    o = _p1out(out)
+    st = _abi.load().sdm_phase1_saving(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val),
+                                       _ptr(g), ctypes.byref(o), step_begin, step_end, _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "sdm_phase1_saving")
 
 
 def dw_saving(shape: ShapeSpec, dv, bank, snap, ws, step_begin=0, step_end=None, stream=None):

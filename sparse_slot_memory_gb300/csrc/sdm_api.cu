@@ -123,7 +123,7 @@ sdm_status check_range(const Geometry& g, int64_t b, int64_t e) {
 
 sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_idx, const int32_t* q_idx,
                       const void* k_val, const void* q_val, const float* gate, const sdm_p1_out* out,
-                      int64_t b, int64_t e, void* ws, cudaStream_t stream) {
+                      int64_t b, int64_t e, void* ws, cudaStream_t stream, int ordinals = 0) {
     P1Args a;
     memset(&a, 0, sizeof(a));
     a.k_idx = k_idx;
@@ -175,7 +175,8 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_zero = static_cast<uint32_t>(g.sm_zero);
     a.zero_bytes = g.zero_bytes;
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
-    const cudaError_t err = launch_phase1(a, s->val_dtype == SDM_BF16, (e - b) * g.P, g.threads, g.smem_bytes, stream);
+    const cudaError_t err =
+        launch_phase1(a, s->val_dtype == SDM_BF16, ordinals, (e - b) * g.P, g.threads, g.smem_bytes, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
 }
 
@@ -300,6 +301,22 @@ extern "C" sdm_status sdm_forward_chunks(const sdm_shape* shape, const int32_t* 
 }
 
 // ---- the saving forward: DW also writes the dense compact snapshot ------------------------------
+extern "C" sdm_status sdm_phase1_saving(const sdm_shape* shape, const int32_t* k_idx, const int32_t* q_idx,
+                                        const void* k_val, const void* q_val, const float* g, const sdm_p1_out* out,
+                                        int64_t step_begin, int64_t step_end, void* ws, size_t ws_bytes,
+                                        sdm_stream_t stream) {
+    Geometry geo;
+    sdm_status st = geometry(shape, &geo);
+    if (st != SDM_OK) return st;
+    if ((st = check_range(geo, step_begin, step_end)) != SDM_OK) return st;
+    if ((st = check_p1_args(geo, k_idx, q_idx, k_val, q_val, g, out)) != SDM_OK) return st;
+    if ((st = check_ws(geo, ws, ws_bytes)) != SDM_OK) return st;
+    if ((st = check_smem(geo)) != SDM_OK) return st;
+    if (step_begin == step_end) return SDM_OK;
+    return run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws,
+                      reinterpret_cast<cudaStream_t>(stream), 1);
+}
+
 extern "C" sdm_status sdm_dw_saving(const sdm_shape* shape, const void* dv, void* bank, void* snap, int64_t step_begin,
                                     int64_t step_end, void* ws, size_t ws_bytes, sdm_stream_t stream) {
     Geometry geo;
@@ -328,7 +345,7 @@ extern "C" sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const in
     if ((st = check_smem(geo)) != SDM_OK) return st;
     if (step_begin == step_end) return SDM_OK;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs)) != SDM_OK)
+    if ((st = run_phase1(shape, geo, k_idx, q_idx, k_val, q_val, g, out, step_begin, step_end, ws, cs, 1)) != SDM_OK)
         return st;
     return run_dw(shape, geo, dv, bank, snap, step_begin, step_end, ws, cs);
 }

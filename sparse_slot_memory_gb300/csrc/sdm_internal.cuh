@@ -122,7 +122,7 @@ struct DWArgs {
 };
 
 // Launchers (return a cudaError_t from the launch).
-cudaError_t launch_phase1(const P1Args& a, int val_bf16, int64_t nchunks, int threads, size_t smem,
+cudaError_t launch_phase1(const P1Args& a, int val_bf16, int ordinals, int64_t nchunks, int threads, size_t smem,
                           cudaStream_t stream);
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream);
 cudaError_t phase1_smem_limit(int device, size_t* bytes);

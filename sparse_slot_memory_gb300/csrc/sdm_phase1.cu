@@ -257,7 +257,9 @@ __device__ __forceinline__ void st_stream(T* p, T v) {
     __stcs(p, v);
 }
 
-template <typename ValT>
+// ORD: the saving forward's Phase 1 -- each group's FIRST record also carries its dense ordinal
+// and out.ngroups is written (a separate instantiation: the plain forward's kernel is unchanged)
+template <typename ValT, bool ORD>
 __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + a.sm_keys);   // entry -> key word
@@ -286,15 +288,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     __shared__ int hot_n;
     // per (triangle, token): the dense groups with a term in the token's A (0) / QK (1) row
     __shared__ uint32_t hotrow[2][kMaxC];
-    // write-row positions of the valid write groups' first entries (bit per position) and, per
-    // 32-bit word, the groups before it: a group's dense ordinal in the chunk
-    __shared__ uint32_t khead[kMaxRow / 32], kheadp[kMaxRow / 32 + 1];
+    // write-row positions of the valid write groups' first entries, a bit per position: the dense
+    // ordinal of a group = the heads before it
+    __shared__ uint32_t khead[kMaxRow / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
     for (int i = tid; i < kMaxRow / 32; i += blockDim.x) hotmask[i] = 0u;
     for (int i = tid; i < 2 * kMaxC; i += blockDim.x) hotrow[i / kMaxC][i % kMaxC] = 0u;
-    for (int i = tid; i < kMaxRow / 32; i += blockDim.x) khead[i] = 0u;
     // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
     // use by the sort's barriers
     const int nbk = 1 << a.logB;
@@ -600,10 +601,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 cpev[o] = cpe_f;
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
-                if (valid && before == 0) {
-                    atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
-                    atomicOr(&khead[jx >> 5], 1u << (jx & 31u));
-                }
+                if (valid && before == 0) atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
                 if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
             }
         }
@@ -627,36 +625,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
         zero_upto(6);
-        if (warp == 0) {   // groups before each word of the write row (lane: 8 words)
-            const int nwords = (nk + 31) >> 5;
-            uint32_t cnt = 0;
-            for (int q = 0; q < 8; ++q) {
-                const int wi = lane * 8 + q;
-                if (wi < nwords) cnt += __popc(khead[wi]);
-            }
-            uint32_t incl = cnt;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, incl, d);
-                if (lane >= d) incl += y;
-            }
-            uint32_t run = incl - cnt;
-            for (int q = 0; q < 8; ++q) {
-                const int wi = lane * 8 + q;
-                if (wi < nwords) {
-                    kheadp[wi] = run;
-                    run += __popc(khead[wi]);
-                }
-            }
-            if (lane == 31) {
-                kheadp[nwords] = incl;
-                if (a.out.ngroups != nullptr) a.out.ngroups[c] = static_cast<int32_t>(incl);
-            }
-        }
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
-        for (int j = tid; j < nk; j += nthr) {
-            const uint32_t kp = krpos[j];
+        // a warp takes 32 consecutive write-row positions (ORD: the ballot of group heads is a word of
+        // khead)
+        for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
+            const int j = j0 + lane;
+            const uint32_t kp = j < nk ? krpos[j] : 0u;
+            if constexpr (ORD) {
+                const uint32_t hb = __ballot_sync(kFull, (kp >> 16) != 0u);
+                if (lane == 0) khead[j0 >> 5] = hb;
+            }
             if (kp >> 16) {
                 const uint32_t b = bucket_of(keys[kp & 0xFFFFu]);
                 krpos[j] = (kp & 0xFFFFu) | (off[b] + atomicAdd(&fill[b], kp >> 16)) << 16;
@@ -664,7 +643,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         __syncthreads();
         const int64_t kbase = c * nk;
-        for (int j = tid; j < nk; j += nthr) {
+        if constexpr (ORD) {
+            if (warp == 0 && a.out.ngroups != nullptr) {   // the chunk's valid write groups
+                const int nwords = (nk + 31) >> 5;
+                uint32_t cnt = 0;
+                for (int wi = lane; wi < nwords; wi += 32) cnt += __popc(khead[wi]);
+                cnt = __reduce_add_sync(kFull, cnt);
+                if (lane == 0) a.out.ngroups[c] = static_cast<int32_t>(cnt);
+            }
+        }
+        for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
+            uint32_t gpre = 0;   // ORD: groups before this warp's word (the dense ordinal of a group starting in it)
+            if constexpr (ORD) {
+                for (int wi = lane; wi < (j0 >> 5); wi += 32) gpre += __popc(khead[wi]);
+                gpre = __reduce_add_sync(kFull, gpre);
+            }
+            const int j = j0 + lane;
+            if (j >= nk) continue;
             const uint32_t e = krpos[j] & 0xFFFFu;
             const uint32_t key = keys[e];
             if (key >> 31) continue;   // invalid entries have no record
@@ -674,8 +669,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
             const bool last = ((posv[e] >> kPosAfterShift) & kPosCountMax) == 0u;
             uint32_t w0 = t | (last ? kLast : 0u);
-            if (kb == 0u)   // FIRST: the group's dense ordinal
-                w0 |= kFirst | (kheadp[j >> 5] + __popc(khead[j >> 5] & ((1u << (j & 31)) - 1u))) << kRecOrdShift;
+            if (kb == 0u) {
+                w0 |= kFirst;
+                if constexpr (ORD)   // the group's dense ordinal
+                    w0 |= (gpre + __popc(khead[j0 >> 5] & ((1u << lane) - 1u))) << kRecOrdShift;
+            }
             const float sc = __fmul_rn(to_f(vals[e]), expf(rexv[o]));
             st_stream(a.krec + kbase + rec, make_int4(static_cast<int>(w0), static_cast<int>(key), __float_as_int(sc),
                                                       __float_as_int(cpev[o])));
@@ -962,22 +960,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
 }  // namespace
 
-cudaError_t launch_phase1(const P1Args& a, int val_bf16, int64_t nchunks, int threads, size_t smem,
+template <typename ValT, bool ORD>
+cudaError_t launch_p1(const P1Args& a, int64_t nchunks, int threads, size_t smem, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(p1_kernel<ValT, ORD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    p1_kernel<ValT, ORD><<<dim3(static_cast<unsigned>(nchunks)), threads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_phase1(const P1Args& a, int val_bf16, int ordinals, int64_t nchunks, int threads, size_t smem,
                           cudaStream_t stream) {
     if (nchunks <= 0) return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(nchunks));
-    if (val_bf16) {
-        cudaError_t e = cudaFuncSetAttribute(p1_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        p1_kernel<__nv_bfloat16><<<grid, threads, smem, stream>>>(a);
-    } else {
-        cudaError_t e = cudaFuncSetAttribute(p1_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        p1_kernel<float><<<grid, threads, smem, stream>>>(a);
-    }
-    return cudaGetLastError();
+    if (val_bf16)
+        return ordinals ? launch_p1<__nv_bfloat16, true>(a, nchunks, threads, smem, stream)
+                        : launch_p1<__nv_bfloat16, false>(a, nchunks, threads, smem, stream);
+    return ordinals ? launch_p1<float, true>(a, nchunks, threads, smem, stream)
+                    : launch_p1<float, false>(a, nchunks, threads, smem, stream);
 }
 
 cudaError_t phase1_smem_limit(int device, size_t* bytes) {
