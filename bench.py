@@ -37,7 +37,10 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload, kernel and the
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "large:dw:536242ae44ac": 1178298624 + 981054464,        # profiles/dram_traffic_large.md
+    "large:phase1:536242ae44ac": 55952128 + 718865664,
+}
 
 
 def src_hash() -> str:
