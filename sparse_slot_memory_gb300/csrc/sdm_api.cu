@@ -67,9 +67,15 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->logB = lb;
     g->B = 1 << lb;
     // workspace: header | DW records [N, C*W] | bucket bounds [P, B + 1, steps]
+    g->maxL = g->nk / kLongMin > 0 ? g->nk / kLongMin : 1;
+    g->rstride = g->nk + g->maxL;
+    if (N > (int64_t(1) << 31) / g->maxL) return SDM_ERR_SHAPE;   // long-group sum rows are int32-indexed
     g->krec_off = kHdrBytes;
-    g->bb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->nk * sizeof(int4), 256);
-    g->ws_bytes = g->bb_off + round_up(static_cast<size_t>(s->P) * (g->B + 1) * s->steps * sizeof(int32_t), 256);
+    g->bb_off = g->krec_off + round_up(static_cast<size_t>(N) * g->rstride * sizeof(int4), 256);
+    g->lcnt_off = g->bb_off + round_up(static_cast<size_t>(s->P) * (g->B + 1) * s->steps * sizeof(int32_t), 256);
+    g->ldesc_off = g->lcnt_off + round_up(static_cast<size_t>(N) * sizeof(int32_t), 256);
+    g->lacc_off = g->ldesc_off + round_up(static_cast<size_t>(N) * g->maxL * sizeof(int32_t), 256);
+    g->ws_bytes = g->lacc_off + round_up(static_cast<size_t>(N) * g->maxL * s->hd * sizeof(float), 256);
     // Phase-1 shared memory: keys | vals | sidx | (pong + hist) or log-cumsums | pos | kb | rex | cpe | scratch
     const size_t np = static_cast<size_t>(g->npad);
     size_t off = 0;
@@ -135,6 +141,10 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     unsigned char* const w = static_cast<unsigned char*>(ws);
     a.krec = reinterpret_cast<int4*>(w + g.krec_off);
     a.bb = reinterpret_cast<int32_t*>(w + g.bb_off);
+    a.lcnt = reinterpret_cast<int32_t*>(w + g.lcnt_off);
+    a.ldesc = reinterpret_cast<int32_t*>(w + g.ldesc_off);
+    a.maxL = g.maxL;
+    a.rstride = g.rstride;
     a.status = reinterpret_cast<uint32_t*>(w + kHdrStatus);
     a.C = g.C;
     a.W = g.W;
@@ -189,6 +199,7 @@ sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* b
     memset(&a, 0, sizeof(a));
     a.krec = reinterpret_cast<const int4*>(w + g.krec_off);
     a.bb = reinterpret_cast<const int32_t*>(w + g.bb_off);
+    a.lacc = reinterpret_cast<const float*>(w + g.lacc_off);
     a.dv = dv;
     a.bank = bank;
     a.snap = snap;
@@ -197,6 +208,8 @@ sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* b
     a.C = g.C;
     a.W = g.W;
     a.nk = g.nk;
+    a.maxL = g.maxL;
+    a.rstride = g.rstride;
     a.B = g.B;
     a.nsl = g.nsl;
     a.hd = g.hd;
@@ -205,6 +218,21 @@ sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* b
     a.step_begin = b;
     a.step_end = e;
     a.items = static_cast<int64_t>(g.P) * g.B * g.nsl;
+    LongArgs la;   // the long groups' sums first (the DW takes them at their reference records)
+    memset(&la, 0, sizeof(la));
+    la.krec = a.krec;
+    la.lcnt = reinterpret_cast<const int32_t*>(w + g.lcnt_off);
+    la.ldesc = reinterpret_cast<const int32_t*>(w + g.ldesc_off);
+    la.dv = dv;
+    la.lacc = reinterpret_cast<float*>(w + g.lacc_off);
+    la.C = g.C;
+    la.maxL = g.maxL;
+    la.rstride = g.rstride;
+    la.hd = g.hd;
+    la.nsl = g.nsl;
+    la.c0 = b * g.P;
+    la.nchunks = (e - b) * g.P;
+    if (launch_long(la, s->dv_dtype == SDM_BF16, stream) != cudaSuccess) return SDM_ERR_CUDA;
     const cudaError_t err = launch_dw(a, s->dv_dtype == SDM_BF16, s->bank_dtype == SDM_BF16, stream);
     return err == cudaSuccess ? SDM_OK : SDM_ERR_CUDA;
 }

@@ -82,6 +82,55 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+// Long groups (at least kLongMin write entries in one chunk, e.g. the hot slots of a skewed
+// stream): one warp per (group, 128-column slice) sums the group's tail records in order,
+// acc = fmaf(sc_m, dv[tok_m], acc) from 0 -- the very chain of the DW walk -- with the token rows of
+// 16 records in flight at a time. The DW walk meets the group as one reference record and takes the
+// sum there, so a hot slot's terms no longer form one long chain inside its bucket's warp: all long
+// groups of all steps are summed in parallel.
+template <typename DvT>
+__global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t c = a.c0 + blockIdx.x;   // one block per chunk
+    const int nl = a.lcnt[c];
+    const DvT* const dv = static_cast<const DvT*>(a.dv);
+    const uint32_t hdu = static_cast<uint32_t>(a.hd);
+    for (int item = warp; item < nl * a.nsl; item += kDwWarps) {
+        const int li = item / a.nsl, sl = item - li * a.nsl;
+        const int col = sl * 128 + lane * 4;
+        const bool active = col < a.hd;
+        const int4* const rec = a.krec + c * a.rstride;
+        const DvT* const dv_lane = dv + static_cast<int64_t>(c) * a.C * a.hd + col;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // records from the group's first tail record to its LAST (never past the chunk's records)
+        for (int base = a.ldesc[c * a.maxL + li]; base < a.rstride; base += 16) {
+            int4 r = make_int4(0, 0, 0, 0);
+            const bool in = lane < 16 && base + lane < a.rstride;
+            if (in) r = __ldcg(rec + base + lane);
+            const uint32_t lastm = __ballot_sync(kFull, in && (static_cast<uint32_t>(r.x) & kLast));
+            const int n = lastm ? __ffs(lastm) : 16;   // the group's records in this batch
+            Raw4<DvT> dvv[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t w0 = __shfl_sync(kFull, static_cast<uint32_t>(r.x), k);
+                if (k < n && active && base + k < a.rstride) dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float sc = __int_as_float(__shfl_sync(kFull, r.z, k));
+                if (k < n && base + k < a.rstride) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
+                }
+            }
+            if (lastm != 0u) break;
+        }
+        if (active)
+            __stcg(reinterpret_cast<float4*>(a.lacc + (static_cast<int64_t>(c) * a.maxL + li) * a.hd + col),
+                   make_float4(acc[0], acc[1], acc[2], acc[3]));
+    }
+}
+
 // SNAP: the saving forward (a.snap is the dense compact snapshot)
 template <typename BankT, typename DvT, bool SNAP>
 __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
@@ -129,7 +178,7 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
             const int total = __shfl_sync(kFull, cum, 31);
             if (total == 0) continue;
             const int64_t cl = (a.step_begin + t0 + lane) * a.P + p;   // lane t's chunk
-            const long long rbase = cl * a.nk + s0l - (cum - cntl);    // record of position g: rbase + g
+            const long long rbase = cl * a.rstride + s0l - (cum - cntl);   // record of position g: rbase + g
             const long long dbase = static_cast<long long>(cl) * a.C;
             const int nwin = (total + 31) >> 5;
             // window w (positions 32w..) into buffer s: lane j fetches position 32w + j by cp.async
@@ -212,9 +261,35 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                         }
                     }
                 };
+                // A long group's reference record: base row, its precomputed sum, the row back (on its
+                // own: sub-batches stop before it).
+                auto long_ref = [&](int m) {
+                    const int4 r = rs[m];
+                    if (active) {
+                        BankT* const row = bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu;
+                        Raw4<BankT> bv;
+                        bv.ld_cg(row);
+                        const float4 la = __ldcg(reinterpret_cast<const float4*>(
+                            a.lacc + static_cast<uint64_t>(static_cast<uint32_t>(r.z)) * hdu + col));
+                        if constexpr (SNAP)
+                            st_raw(static_cast<BankT*>(a.snap) +
+                                       (static_cast<uint64_t>(ds[m]) * a.W + ((static_cast<uint32_t>(r.x) >> kRecOrdShift) & kRecOrdMask)) * hdu + col,
+                                   bv);
+                        const float cp = __int_as_float(r.w);
+                        const float o[4] = {fmaf(bv[0], cp, la.x), fmaf(bv[1], cp, la.y), fmaf(bv[2], cp, la.z),
+                                            fmaf(bv[3], cp, la.w)};
+                        st4(row, o);
+                    }
+                };
+                const uint32_t longm = __ballot_sync(kFull, lane < n && (static_cast<uint32_t>(rs[lane].x) & kRecLong));
                 for (int m = 0; m < n;) {
+                    if ((longm >> m) & 1u) {
+                        long_ref(m);
+                        ++m;
+                        continue;
+                    }
                     int e = min(m + kSub, n);
-                    const uint32_t cut = __ballot_sync(kFull, lane > m && lane < e && prev >= m);
+                    const uint32_t cut = __ballot_sync(kFull, lane > m && lane < e && (prev >= m || ((longm >> lane) & 1u)));
                     if (cut) e = __ffs(cut) - 1;
                     if (e - m > kSub / 2)
                         sub(m, e - m, std::integral_constant<int, kSub>());
@@ -253,6 +328,16 @@ cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream) {
+    if (a.nchunks <= 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(a.nchunks));
+    if (dv_bf16)
+        long_kernel<__nv_bfloat16><<<grid, kDwThreads, 0, stream>>>(a);
+    else
+        long_kernel<float><<<grid, kDwThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream) {
     if (a.items <= 0 || a.step_end <= a.step_begin) return cudaSuccess;

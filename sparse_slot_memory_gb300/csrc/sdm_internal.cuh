@@ -52,11 +52,19 @@ constexpr size_t kSmemOptin = 232448;          // opt-in shared memory per block
 constexpr uint32_t kDevBadSlot = SDM_DEV_BAD_SLOT;
 
 // DW record of one valid write entry (16 bytes, one vector load), grouped by slot bucket:
-//   x = token | group ordinal << 16 (FIRST records) | LAST << 30 | FIRST << 31 | kRecInvalid,
+//   x = token | group ordinal << 16 (FIRST records) | kRecLong | LAST << 30 | FIRST << 31,
 //   y = stream-local slot,
 //   z = f32 bits of sc = k * expf(rex), w = f32 bits of cpe (the value-type cpe widened).
-constexpr uint32_t kRecInvalid = 1u << 29;
 constexpr uint32_t kRecTokMask = 0xFFFFu;
+// A long group (at least kLongMin write entries in its chunk, e.g. a hot slot of a skewed stream)
+// takes ONE record in its slot bucket -- the reference record: x = the group's index among the
+// chunk's long groups | kRecLong | FIRST | LAST (| ordinal), y = slot, z = its row of the sums
+// (chunk * maxL + index), w = cpe -- while its own
+// records go to the chunk's tail (after the buckets' records), where the long-group kernel sums
+// them (the DW walk's very FMA chain) before the DW, which takes the sum at the reference record.
+constexpr uint32_t kRecLong = 1u << 29;
+constexpr int kLongMin = 32;
+constexpr int kMaxLong = kMaxRow / kLongMin;   // long groups per chunk at most
 // the group's dense ordinal in its chunk (valid write groups before it in sorted order), carried by
 // the group's FIRST record: the row of the dense compact snapshot
 constexpr int kRecOrdShift = 16;
@@ -74,7 +82,9 @@ struct Geometry {
     int threads, npad, nwarps;
     int B, logB;           // DW buckets per stream, B = 2^logB: a slot group's bucket is a hash of its slot
     int nsl;               // DW column slices of 128 columns
-    size_t krec_off, bb_off, ws_bytes;
+    size_t krec_off, bb_off, lcnt_off, ldesc_off, lacc_off, ws_bytes;
+    int maxL;              // long groups per chunk at most: max(1, C*W / kLongMin)
+    int rstride;           // records per chunk: C*W + maxL (a long group adds its reference record)
     size_t smem_bytes;
     int zero_bytes;        // bulk zero-fill piece (and zero buffer) size
     // Phase-1 shared-memory carve (byte offsets)
@@ -91,6 +101,9 @@ struct P1Args {
     sdm_p1_out out;
     int4* krec;
     int32_t* bb;            // [P][B + 1][steps] first record of each slot bucket, per chunk
+    int32_t* lcnt;          // [N] long groups of each chunk
+    int32_t* ldesc;         // [N][maxL] the first tail record of each long group
+    int maxL, rstride;
     uint32_t* status;
     int C, W, R, wr, n, nk, nq, npad, nwarps;
     int key_bits, passes, digit_bits;
@@ -114,8 +127,9 @@ struct DWArgs {
     const void* dv;
     void* bank;
     void* snap;         // dense compact snapshot [N, C*W, hd] (bank type) or null
+    const float* lacc;  // [N][maxL][hd] each long group's sum of terms
     uint32_t* claim;    // work counter
-    int P, C, W, nk, B, nsl, hd;
+    int P, C, W, nk, B, nsl, hd, maxL, rstride;
     int64_t S, steps;
     int64_t step_begin, step_end;
     int64_t items;      // P * B * nsl
@@ -125,6 +139,17 @@ struct DWArgs {
 cudaError_t launch_phase1(const P1Args& a, int val_bf16, int ordinals, int64_t nchunks, int threads, size_t smem,
                           cudaStream_t stream);
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream);
+// the long groups' sums of terms, for the chunks [c0, c0 + nchunks)
+struct LongArgs {
+    const int4* krec;
+    const int32_t* lcnt;
+    const int32_t* ldesc;
+    const void* dv;
+    float* lacc;
+    int C, maxL, rstride, hd, nsl;
+    int64_t c0, nchunks;
+};
+cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream);
 cudaError_t phase1_smem_limit(int device, size_t* bytes);
 
 }  // namespace sdm

@@ -291,7 +291,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // write-row positions of the valid write groups' first entries, a bit per position: the dense
     // ordinal of a group = the heads before it
     __shared__ uint32_t khead[kMaxRow / 32];
+    // long groups: count, tail fill, and per long group its head's write-row index and its
+    // reference record's place in its bucket
+    __shared__ uint32_t lcnt_s, ltail_s;
+    __shared__ uint16_t lhead_j[kMaxLong], lref[kMaxLong];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        lcnt_s = 0u;
+        ltail_s = 0u;
+    }
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
     for (int i = tid; i < kMaxRow / 32; i += blockDim.x) hotmask[i] = 0u;
@@ -601,7 +609,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 cpev[o] = cpe_f;
                 if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
-                if (valid && before == 0) atomicAdd(&bcnt[bucket_of(key)], after + 1u);   // the group's size
+                if (valid && before == 0)   // the group's records in its bucket: a long group has one
+                    atomicAdd(&bcnt[bucket_of(key)], after + 1u >= static_cast<uint32_t>(kLongMin) ? 1u : after + 1u);
                 if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
             }
         }
@@ -638,11 +647,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
             if (kp >> 16) {
                 const uint32_t b = bucket_of(keys[kp & 0xFFFFu]);
-                krpos[j] = (kp & 0xFFFFu) | (off[b] + atomicAdd(&fill[b], kp >> 16)) << 16;
+                const uint32_t size = kp >> 16;
+                uint32_t base;
+                if (size >= static_cast<uint32_t>(kLongMin)) {   // long: reference record + tail records
+                    const uint32_t li = atomicAdd(&lcnt_s, 1u);   // < C*W / kLongMin
+                    lhead_j[li] = static_cast<uint16_t>(j);
+                    lref[li] = static_cast<uint16_t>(off[b] + atomicAdd(&fill[b], 1u));
+                    base = off[B] + atomicAdd(&ltail_s, size);
+                    a.ldesc[c * a.maxL + li] = static_cast<int32_t>(base);
+                } else {
+                    base = off[b] + atomicAdd(&fill[b], size);
+                }
+                krpos[j] = (kp & 0xFFFFu) | base << 16;
             }
         }
         __syncthreads();
-        const int64_t kbase = c * nk;
+        const int64_t kbase = c * a.rstride;
+        // the long groups' reference records: {index | kRecLong | FIRST | LAST (| ordinal), slot, row of
+        // the sums, cpe}
+        for (int li = tid; li < static_cast<int>(lcnt_s); li += nthr) {
+            const int j = lhead_j[li];
+            const uint32_t e = krpos[j] & 0xFFFFu;
+            const uint32_t t = tok_of(e);
+            const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
+            uint32_t w0 = static_cast<uint32_t>(li) | kRecLong | kFirst | kLast;
+            if constexpr (ORD) {   // the group's dense ordinal: group heads before it
+                uint32_t g = __popc(khead[j >> 5] & ((1u << (j & 31)) - 1u));
+                for (int wi = 0; wi < (j >> 5); ++wi) g += __popc(khead[wi]);
+                w0 |= g << kRecOrdShift;
+            }
+            const int32_t lrow = static_cast<int32_t>(c * a.maxL + li);   // its row of the sums (< 2^31)
+            st_stream(a.krec + kbase + lref[li], make_int4(static_cast<int>(w0), static_cast<int>(keys[e]), lrow,
+                                                           __float_as_int(cpev[o])));
+        }
         if constexpr (ORD) {
             if (warp == 0 && a.out.ngroups != nullptr) {   // the chunk's valid write groups
                 const int nwords = (nk + 31) >> 5;
@@ -719,6 +756,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
 
     // ---- 4. pair triangles --------------------------------------------------------------------------
+    if (tid == 0) a.lcnt[c] = static_cast<int32_t>(lcnt_s);   // final since the DW split's barrier
     if (a.out.A == nullptr && a.out.QK == nullptr) return;
     if (bulk_zero && warp == 0) {
         bulk_wait_all();        // this lane's zero pieces are written (and the zero buffer is no longer read)
