@@ -291,10 +291,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // write-row positions of the valid write groups' first entries, a bit per position: the dense
     // ordinal of a group = the heads before it
     __shared__ uint32_t khead[kMaxRow / 32];
-    // long groups: count, tail fill, and per long group its head's write-row index and its
-    // reference record's place in its bucket
+    // long groups: count and tail fill
     __shared__ uint32_t lcnt_s, ltail_s;
-    __shared__ uint16_t lhead_j[kMaxLong], lref[kMaxLong];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         lcnt_s = 0u;
@@ -303,6 +301,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
     for (int i = tid; i < kMaxRow / 32; i += blockDim.x) hotmask[i] = 0u;
+    if constexpr (ORD)
+        for (int i = tid; i < kMaxRow / 32; i += blockDim.x) khead[i] = 0u;
     for (int i = tid; i < 2 * kMaxC; i += blockDim.x) hotrow[i / kMaxC][i % kMaxC] = 0u;
     // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
     // use by the sort's barriers
@@ -611,6 +611,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
                 if (valid && before == 0)   // the group's records in its bucket: a long group has one
                     atomicAdd(&bcnt[bucket_of(key)], after + 1u >= static_cast<uint32_t>(kLongMin) ? 1u : after + 1u);
+                if constexpr (ORD)   // the saving forward: group heads by write-row position
+                    if (valid && before == 0) atomicOr(&khead[jx >> 5], 1u << (jx & 31u));
                 if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
             }
         }
@@ -636,25 +638,32 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         zero_upto(6);
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
-        // a warp takes 32 consecutive write-row positions (ORD: the ballot of group heads is a word of
-        // khead)
+        // a warp takes 32 consecutive write-row positions
         for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
             const int j = j0 + lane;
             const uint32_t kp = j < nk ? krpos[j] : 0u;
-            if constexpr (ORD) {
-                const uint32_t hb = __ballot_sync(kFull, (kp >> 16) != 0u);
-                if (lane == 0) khead[j0 >> 5] = hb;
-            }
             if (kp >> 16) {
                 const uint32_t b = bucket_of(keys[kp & 0xFFFFu]);
                 const uint32_t size = kp >> 16;
                 uint32_t base;
-                if (size >= static_cast<uint32_t>(kLongMin)) {   // long: reference record + tail records
+                if (size >= static_cast<uint32_t>(kLongMin)) {
+                    // long: its reference record in the bucket {index | kRecLong | FIRST | LAST (| ordinal),
+                    // slot, row of the sums, cpe}; its own records in the chunk's tail
                     const uint32_t li = atomicAdd(&lcnt_s, 1u);   // < C*W / kLongMin
-                    lhead_j[li] = static_cast<uint16_t>(j);
-                    lref[li] = static_cast<uint16_t>(off[b] + atomicAdd(&fill[b], 1u));
+                    const uint32_t ref = off[b] + atomicAdd(&fill[b], 1u);
                     base = off[B] + atomicAdd(&ltail_s, size);
                     a.ldesc[c * a.maxL + li] = static_cast<int32_t>(base);
+                    const uint32_t e = kp & 0xFFFFu;
+                    const uint32_t t = tok_of(e);
+                    uint32_t w0 = li | kRecLong | kFirst | kLast;
+                    if constexpr (ORD) {   // the group's dense ordinal (khead is complete: reverse scan)
+                        uint32_t g = __popc(khead[j >> 5] & ((1u << (j & 31)) - 1u));
+                        for (int wi = 0; wi < (j >> 5); ++wi) g += __popc(khead[wi]);
+                        w0 |= g << kRecOrdShift;
+                    }
+                    st_stream(a.krec + c * a.rstride + ref,
+                              make_int4(static_cast<int>(w0), static_cast<int>(keys[e]), static_cast<int>(c * a.maxL + li),
+                                        __float_as_int(cpev[static_cast<int>(t) * W + static_cast<int>(e - t * wr)])));
                 } else {
                     base = off[b] + atomicAdd(&fill[b], size);
                 }
@@ -663,23 +672,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         __syncthreads();
         const int64_t kbase = c * a.rstride;
-        // the long groups' reference records: {index | kRecLong | FIRST | LAST (| ordinal), slot, row of
-        // the sums, cpe}
-        for (int li = tid; li < static_cast<int>(lcnt_s); li += nthr) {
-            const int j = lhead_j[li];
-            const uint32_t e = krpos[j] & 0xFFFFu;
-            const uint32_t t = tok_of(e);
-            const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
-            uint32_t w0 = static_cast<uint32_t>(li) | kRecLong | kFirst | kLast;
-            if constexpr (ORD) {   // the group's dense ordinal: group heads before it
-                uint32_t g = __popc(khead[j >> 5] & ((1u << (j & 31)) - 1u));
-                for (int wi = 0; wi < (j >> 5); ++wi) g += __popc(khead[wi]);
-                w0 |= g << kRecOrdShift;
-            }
-            const int32_t lrow = static_cast<int32_t>(c * a.maxL + li);   // its row of the sums (< 2^31)
-            st_stream(a.krec + kbase + lref[li], make_int4(static_cast<int>(w0), static_cast<int>(keys[e]), lrow,
-                                                           __float_as_int(cpev[o])));
-        }
         if constexpr (ORD) {
             if (warp == 0 && a.out.ngroups != nullptr) {   // the chunk's valid write groups
                 const int nwords = (nk + 31) >> 5;
