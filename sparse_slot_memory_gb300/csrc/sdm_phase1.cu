@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // the candidates for the dense pair path
     __shared__ uint32_t hotmask[kMaxRow / 32];
     __shared__ int hot_n;
+    __shared__ uint32_t row_claim;   // the next flagged (triangle, row) pair to take (phase 4)
     // per (triangle, token): the dense groups with a term in the token's A (0) / QK (1) row
     __shared__ uint32_t hotrow[2][kMaxC];
     // write-row positions of the valid write groups' first entries, a bit per position: the dense
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     if (tid == 0) {
         lcnt_s = 0u;
         ltail_s = 0u;
+        row_claim = 0u;
     }
     const int nw = a.nwarps, nthr = blockDim.x;
     if (tid < 2 * (kMaxC / 32)) rowmask[tid / (kMaxC / 32)][tid % (kMaxC / 32)] = 0u;
@@ -871,9 +873,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     __syncthreads();
     // Only rows flagged in the scan (an entry with an earlier write entry in its group) have
-    // terms; the j-th flagged (triangle, row), in (triangle, row) order, goes to warp j % nw. Lane
-    // u < 2 * mwords holds flag word u (A rows, then QK rows); a warp prefix of the words' counts
-    // locates pair j without any walk over the others.
+    // terms. Lane u < 2 * mwords holds flag word u (A rows, then QK rows); a warp prefix of the
+    // words' counts locates the j-th flagged (triangle, row) pair without any walk over the others.
     const int mwords = (C + 31) >> 5;   // <= 8: the flag words fit the lanes
     const uint32_t fw = lane < 2 * mwords ? rowmask[lane >= mwords ? 1 : 0][lane >= mwords ? lane - mwords : lane] : 0u;
     uint32_t fincl = __popc(fw);
@@ -884,7 +885,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     const uint32_t fexcl = fincl - __popc(fw);
     const uint32_t nflag = __shfl_sync(kFull, fincl, 31);
-    for (uint32_t jf = static_cast<uint32_t>(warp); jf < nflag; jf += static_cast<uint32_t>(nw)) {
+    // warps take the flagged pairs from a counter (rows differ in work: skewed chunks balance)
+    for (;;) {
+        uint32_t jf = 0;
+        if (lane == 0) jf = atomicAdd(&row_claim, 1u);
+        jf = __shfl_sync(kFull, jf, 0);
+        if (jf >= nflag) break;
         const int u = __ffs(__ballot_sync(kFull, jf >= fexcl && jf < fincl)) - 1;   // the word holding pair jf
         uint32_t bits = __shfl_sync(kFull, fw, u);
         for (uint32_t q = __shfl_sync(kFull, fexcl, u); q < jf; ++q) bits &= bits - 1u;
