@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
 NCU_TRAFFIC = {
-    "large:dw:536242ae44ac": 1178298624 + 981054464,        # profiles/dram_traffic_large.md
-    "large:phase1:536242ae44ac": 55952128 + 718865664,
+    "large:dw:17feffa56b22": 1178160640 + 981001984,        # profiles/dram_traffic_large.md
+    "large:phase1:17feffa56b22": 56588032 + 719801600,
 }
 
 
@@ -326,7 +326,7 @@ def run_ours(args):
                          "traffic": traffic, "total_frac": ab["total"] / (ms / 1e3) / 1e9 / peak},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 3 * args.steps,   # per forward: Phase 1, the long-group sums, the DW
             "clocks": clk.summary(),
             "impl": "ours",
         }
