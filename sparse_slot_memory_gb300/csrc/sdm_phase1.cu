@@ -425,7 +425,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             __syncthreads();
             if (pass < 3) zero_upto(1 + pass);
             uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 13 | digit << 21
-#pragma unroll
+            // Not unrolled (code size): each item's word enters at the top of mer[], which shifts down
+            // one place per iteration, so after kItems iterations mer[k] is item k's.
+#pragma unroll 1
             for (int k = 0; k < kItems; ++k) {
                 const int p = warp * (32 * kItems) + k * 32 + lane;
                 const uint32_t e = pass == 0 ? static_cast<uint32_t>(p) : src[p];
@@ -444,7 +446,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 __syncwarp();
                 if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
                 __syncwarp();
-                mer[k] = e | (base + rin) << 13 | d << 21;   // entry | rank (< 256) | digit
+#pragma unroll
+                for (int q = 0; q < kItems - 1; ++q) mer[q] = mer[q + 1];
+                mer[kItems - 1] = e | (base + rin) << 13 | d << 21;   // entry | rank (< 256) | digit
             }
             __syncthreads();
             block_exscan_padded(hist, nbins * nw, nw, uscr, lane, warp, nw);
@@ -525,10 +529,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
         zero_upto(4);
-#pragma unroll
+        // Not unrolled (code size): item k's gate and entry are taken from the bottom of x[] / ke[],
+        // which shift down one place per iteration (after kItems shifts they are back in order).
+#pragma unroll 1
         for (int k = 0; k < kItems; ++k) {
+            const float xk = x[0];
+            const uint32_t e = ke[0];
+#pragma unroll
+            for (int q = 0; q < kItems - 1; ++q) {
+                x[q] = x[q + 1];
+                ke[q] = ke[q + 1];
+            }
+            x[kItems - 1] = xk;
+            ke[kItems - 1] = e;
             const uint32_t ownc = cnt_of(k), owna = all_of(k);
-            const Fwd it = {x[k], 0.f, ownc, owna | (((headm >> k) & 1u) << 31)};
+            const Fwd it = {xk, 0.f, ownc, owna | (((headm >> k) & 1u) << 31)};
             run = fcomb(run, it);
             const float logv = __fadd_rn(run.s, run.c);
             const uint32_t b = run.cnt - ownc;   // valid K before | valid Q before << 16
@@ -536,7 +551,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const bool isq = (qm >> k) & 1u;
             const uint32_t own_b = isq ? (b >> 16) : (b & 0xFFFFu);
             const uint32_t jxv = isq ? (ex >> 16) : (ex & 0xFFFFu);
-            const uint32_t e = ke[k];
             const bool valid = (validm >> k) & 1u;
             posv[e] = own_b | jxv << 16;
             lv[e] = valid ? logv : 0.f;
