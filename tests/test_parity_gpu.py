@@ -34,6 +34,9 @@ CASES = {
     # more than the dense path's exponent range, so they keep the exact walk
     "wide_span": scaled(WORKLOADS["uniform_c128"], P=1, T=256, S=4, hd=8, W=4, R=4, gate_mu=-3.0,
                         name="wide_span"),
+    # ~32 write entries per slot and chunk in rows of two column slices (the second partial) with a
+    # ragged last step: long groups (summed ahead of the DW) next to short ones, every slice
+    "wide_hot": scaled(WORKLOADS["wide_ragged"], P=2, T=300, S=16, hd=200, name="wide_hot"),
 }
 
 
