@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
 NCU_TRAFFIC = {
-    "large:dw:17feffa56b22": 1178160640 + 981001984,        # profiles/dram_traffic_large.md
-    "large:phase1:17feffa56b22": 56588032 + 719801600,
+    "large:dw:fb8543c198da": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
+    "large:phase1:fb8543c198da": 55624960 + 718927616,
 }
 
 
