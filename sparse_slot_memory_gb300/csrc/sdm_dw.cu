@@ -19,9 +19,11 @@
 // Rows move as 8-byte (bf16) / 16-byte (f32) lane vectors: 256 / 512 contiguous bytes per warp
 // access. The item's records of up to 32 steps are taken as one sequence in step order, in
 // windows of 32 that arrive in shared memory by cp.async two windows ahead; per sub-batch of up
-// to 4 records every token-row and base-row load is issued before the dependent FMAs. A
+// to 8 records every token-row and base-row load is issued before the dependent FMAs. A
 // sub-batch never holds two records of one slot (those are of different steps): it is cut
-// before the second, whose base row is then loaded after the first one's store.
+// before the second, whose base row is then loaded after the first one's store. A long group
+// (a hot slot's many write entries in one chunk) is one reference record here: its sum comes
+// from long_kernel, which ran before over the group's own records in the same order.
 #include <cuda_bf16.h>
 
 #include <type_traits>
