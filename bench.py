@@ -38,18 +38,22 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
 NCU_TRAFFIC = {
-    "large:dw:fb8543c198da": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
-    "large:phase1:fb8543c198da": 55624960 + 718927616,
+    "large:dw:eecec77319ab": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
+    "large:phase1:eecec77319ab": 55624960 + 718927616,
 }
 
 
 def src_hash() -> str:
+    """Hash of the CUDA sources' code: comment-only lines and blank lines do not count."""
     h = hashlib.sha1()
     d = os.path.join(ROOT, "sparse_slot_memory_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode())
-            h.update(fh.read())
+            for line in fh:
+                t = line.strip()
+                if t and not t.startswith("//"):
+                    h.update(t.encode())
     return h.hexdigest()[:12]
 
 
