@@ -192,3 +192,57 @@ def dw_stream(bank, inputs, p_local, *, S, C, P, steps, valid_last, val_dtype, d
     if track:
         return alt, amb, touched, mag
     return None
+
+
+def pa_chunk(grad, bank, snap_rows, k_idx_c, k_val_c, log_k_c, cpe_c, beta_c, dva_c, *, S, V):
+    """Phase A, the backward of DW, for one chunk (pa_dc_cuda.py, module docstring: "PA per write
+    group"). Float64, plain loops over the chunk's slot groups.
+
+    Per valid write group (slot s with valid write entries; members in sorted order, i.e. token then
+    lane), with gdw = grad[s] before this step and snap = the group's row of the dense snapshot
+    (snap_rows[g], g = the group's ordinal in slot order):
+      sc_m = -beta[tok_m] * k_m * exp(log_k_m)            (the records' scale)
+      grad[s] = gdw * cpe_last + sum_m sc_m * dva[tok_m]  (cpe_last: the last member's cpe)
+      bank[s] = snap                                      (the pre-write row restored)
+      grad_g[e] = cpe_e * <gdw, snap>,  d_k_eff[e] = -beta[tok_e] * <dva[tok_e], snap>
+    Inputs: grad / bank [S, hd] float64 (updated in place), snap_rows [G, hd], k_idx_c / k_val_c /
+    log_k_c / cpe_c [C, W], beta_c [C], dva_c [C, hd]; tokens t >= V and ids outside [0, S) have
+    no group. Returns (d_k_eff [C, W], grad_g [C, W], mag [S, hd], dmag_eff [C, W], dmag_g [C, W]):
+    mag = |gdw * cpe_last| + sum_m |sc_m * dva| of each written grad row (zero elsewhere), dmag_* = the
+    dots' sums of |products| (tolerance bookkeeping).
+    """
+    C, W = k_idx_c.shape
+    hd = grad.shape[1]
+    ids = np.asarray(k_idx_c, np.int64)
+    d_k_eff = np.zeros((C, W))
+    grad_g = np.zeros((C, W))
+    dmag_eff = np.zeros((C, W))
+    dmag_g = np.zeros((C, W))
+    mag = np.zeros_like(grad)
+    slots = snapshot_slots(ids, S=S, V=V)
+    groups = {int(s): [] for s in slots}
+    for t in range(V):                    # entry order (token, then lane) is the sorted order within a slot
+        for j in range(W):
+            if int(ids[t, j]) in groups:
+                groups[int(ids[t, j])].append((t, j))
+    for g, s in enumerate(slots):
+        members = groups[int(s)]
+        gdw = grad[s].copy()
+        snap = np.asarray(snap_rows[g], np.float64)
+        cpe = float(cpe_c[members[-1]])     # cpe_last
+        acc = np.zeros(hd)
+        aabs = np.zeros(hd)
+        for (t, j) in members:
+            sc = -float(beta_c[t]) * float(k_val_c[t, j]) * np.exp(float(log_k_c[t, j]))
+            acc += sc * dva_c[t]
+            aabs += np.abs(sc * dva_c[t])
+        gdot = float(np.dot(gdw, snap))
+        for (t, j) in members:
+            grad_g[t, j] = float(cpe_c[t, j]) * gdot
+            dmag_g[t, j] = abs(float(cpe_c[t, j])) * float(np.sum(np.abs(gdw * snap)))
+            d_k_eff[t, j] = -float(beta_c[t]) * float(np.dot(dva_c[t], snap))
+            dmag_eff[t, j] = abs(float(beta_c[t])) * float(np.sum(np.abs(dva_c[t] * snap)))
+        grad[s] = gdw * cpe + acc
+        mag[s] = np.abs(gdw * cpe) + aabs
+        bank[s] = snap
+    return d_k_eff, grad_g, mag, dmag_eff, dmag_g

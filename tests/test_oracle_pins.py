@@ -459,3 +459,89 @@ def test_snapshot_rows_are_the_pre_step_bank():
         oracle.dw_stream(b, x, 0, step_end=t, **kw)
         sn = snaps[t]
         assert sn["c"] == t and np.array_equal(sn["rows"], b[sn["slots"]])
+
+
+def _pa_hand_case():
+    # 3 tokens, 2 write lanes, 8 slots; token 1's lane 1 is an invalid id (-1).
+    # valid groups by slot: 1 <- (0,0),(1,0),(2,1); 2 <- (0,1); 5 <- (2,0): ordinals 0, 1, 2
+    k = np.array([[1, 2], [1, -1], [5, 1]], np.int32)
+    kv = np.full((3, 2), 0.5)
+    lk = np.zeros((3, 2))            # exp(log_k) = 1
+    cpe = np.full((3, 2), 0.9)
+    beta = np.array([1.0, 2.0, 3.0])
+    dva = np.arange(12, dtype=float).reshape(3, 4)       # rows [0..3], [4..7], [8..11]
+    snap = np.arange(12, dtype=float).reshape(3, 4)      # group rows [0..3], [4..7], [8..11]
+    return k, kv, lk, cpe, beta, dva, snap
+
+
+def test_pa_hand_example():
+    """Phase A on a hand-worked chunk (pa_dc_cuda.py module docstring, "PA per write group"):
+    slot 1: sc = -beta*k*e^0 = -0.5, -1.0, -1.5 for tokens 0, 1, 2, so
+      grad[1] = 1*0.9 - 0.5*[0,1,2,3] - 1.0*[4,5,6,7] - 1.5*[8,9,10,11] = [-15.1, -18.1, -21.1, -24.1];
+    d_k_eff = -beta * <dva[tok], snap of its group>:
+      (0,0): -1*<[0,1,2,3],[0,1,2,3]> = -14; (1,0): -2*<[4..7],[0..3]> = -76; (2,1): -3*<[8..11],[0..3]> = -186;
+      (0,1) slot 2: -1*<[0..3],[4..7]> = -38; (2,0) slot 5: -3*<[8..11],[8..11]> = -1098;
+    grad_g = cpe * <gdw, snap> with gdw = ones: slot 1: 0.9*6 = 5.4, slot 2: 0.9*22 = 19.8, slot 5: 0.9*38 = 34.2."""
+    k, kv, lk, cpe, beta, dva, snap = _pa_hand_case()
+    grad = np.ones((8, 4))
+    bank = np.full((8, 4), 7.0)
+    d_eff, g_g, mag, _, _ = oracle.pa_chunk(grad, bank, snap, k, kv, lk, cpe, beta, dva, S=8, V=3)
+    assert np.allclose(d_eff, [[-14, -38], [-76, 0], [-1098, -186]])
+    assert np.allclose(g_g, [[5.4, 19.8], [5.4, 0], [34.2, 5.4]])
+    assert np.allclose(grad[1], [-15.1, -18.1, -21.1, -24.1])
+    # slot 2: 0.9 - 0.5*[0,1,2,3]; slot 5: 0.9 - 1.5*[8,9,10,11]
+    assert np.allclose(grad[2], [0.9, 0.4, -0.1, -0.6]) and np.allclose(grad[5], [-11.1, -12.6, -14.1, -15.6])
+    # restore: the groups' rows are the snapshot rows, every other row is untouched
+    assert np.array_equal(bank[[1, 2, 5]], snap) and np.all(bank[[0, 3, 4, 6, 7]] == 7.0)
+    assert np.all(grad[[0, 3, 4, 6, 7]] == 1.0) and np.all(mag[[0, 3, 4, 6, 7]] == 0.0)
+
+
+def test_pa_single_entry_closed_form():
+    """One write entry per group: grad = gdw * cpe - beta * k * exp(log_k) * dva, with cpe = exp(g) of
+    the one writer: e.g. g = log(0.5), k = 0.25, beta = 2: grad = 0.5 gdw - 0.25 dva."""
+    k = np.array([[3]], np.int32)
+    gdw = np.array([[2.0, -4.0]])
+    grad = np.zeros((4, 2)); grad[3] = gdw
+    bank = np.zeros((4, 2))
+    dva = np.array([[8.0, 1.0]])
+    d_eff, g_g, *_ = oracle.pa_chunk(grad, bank, np.array([[1.0, 1.0]]), k, np.array([[0.25]]),
+                                     np.array([[np.log(0.5)]]), np.array([[0.5]]), np.array([2.0]), dva, S=4, V=1)
+    assert np.allclose(grad[3], 0.5 * gdw[0] - 0.25 * dva[0])   # [1 - 2, -2 - 0.25]
+    assert np.allclose(grad[3], [-1.0, -2.25])
+    assert np.isclose(d_eff[0, 0], -2.0 * 9.0) and np.isclose(g_g[0, 0], 0.5 * (-2.0))
+
+
+def test_pa_linear_in_grad_and_dva():
+    """Phase A is linear in (grad, dva) for fixed records and snapshot (a dropped term, a wrong
+    sign or a swapped operand breaks one of these)."""
+    rng = np.random.default_rng(3)
+    S, C, W, hd = 16, 6, 3, 5
+    k = rng.integers(0, 5, size=(C, W)).astype(np.int32)
+    kv, lk = rng.standard_normal((C, W)), -rng.random((C, W))
+    cpe = np.broadcast_to(rng.random((1, 1)) + 0.2, (C, W)).copy()
+    beta, snap = rng.random(C), rng.standard_normal((S, hd))
+    g1, g2 = rng.standard_normal((S, hd)), rng.standard_normal((S, hd))
+    d1, d2 = rng.standard_normal((C, hd)), rng.standard_normal((C, hd))
+
+    def run(gr, dv):
+        gr = gr.copy()
+        out = oracle.pa_chunk(gr, np.zeros((S, hd)), snap, k, kv, lk, cpe, beta, dv, S=S, V=C)
+        return gr, out[0], out[1]
+
+    a, b = 1.5, -0.75
+    rs = run(a * g1 + b * g2, a * d1 + b * d2)
+    r1, r2 = run(g1, d1), run(g2, d2)
+    for x, y1, y2 in zip(rs, r1, r2):
+        assert np.allclose(x, a * y1 + b * y2)
+
+
+def test_pa_decay_uses_last_members_cpe():
+    """The group's grad row decays by cpe_last, the last member's cpe (pa_dc_cuda.py module docstring,
+    "PA per write group"), while grad_g of each entry uses its own cpe_e: two members of slot 0 with
+    cpe 0.5 then 0.25, gdw = [1, 2], dva = 0: grad[0] = [0.25, 0.5]; snap = [3, 4]: grad_g = 0.5 * 11 and
+    0.25 * 11."""
+    k = np.array([[0], [0]], np.int32)
+    grad = np.zeros((2, 2)); grad[0] = [1.0, 2.0]
+    _, g_g, *_ = oracle.pa_chunk(grad, np.zeros((2, 2)), np.array([[3.0, 4.0]]), k, np.ones((2, 1)),
+                                 np.zeros((2, 1)), np.array([[0.5], [0.25]]), np.ones(2), np.zeros((2, 2)), S=2, V=2)
+    assert np.array_equal(grad[0], [0.25, 0.5]) and np.array_equal(g_g[:, 0], [5.5, 2.75])
