@@ -38,16 +38,18 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
 NCU_TRAFFIC = {
-    "large:dw:eecec77319ab": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
-    "large:phase1:eecec77319ab": 55624960 + 718927616,
+    "large:dw:c28e9f58496b": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
+    "large:phase1:6922acd872e5": 55624960 + 718927616,
 }
 
 
-def src_hash() -> str:
-    """Hash of the CUDA sources' code: comment-only lines and blank lines do not count."""
+def src_hash(dom: str) -> str:
+    """Hash of the code of the sources that build kernel domain ``dom`` (its own .cu file, the
+    shared internal header and the launch code of sdm_api.cu): comment-only and blank lines do not
+    count, and a source added for another kernel does not change it."""
     h = hashlib.sha1()
     d = os.path.join(ROOT, "sparse_slot_memory_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in ("sdm_api.cu", f"sdm_{dom}.cu", "sdm_internal.cuh"):
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode())
             for line in fh:
@@ -309,7 +311,7 @@ def run_ours(args):
     dom = "dw" if dw_ms >= p1_ms else "phase1"
     dom_ms = dw_ms if dom == "dw" else p1_ms
     achieved = ab[dom] / (dom_ms / 1e3) / 1e9
-    key = f"{args.workload}:{dom}:{src_hash()}"
+    key = f"{args.workload}:{dom}:{src_hash(dom)}"
     traffic = NCU_TRAFFIC.get(key)
     result = None
     if rank == 0:
