@@ -343,6 +343,209 @@ def run_ours(args):
     return result
 
 
+def pa_algorithmic_bytes(w, groups, grad_bytes):
+    """Bytes of one Phase-A pass over every step (the backward of DW): per valid group the grad row
+    read and written, the snapshot row read and the bank row written, and the first member's slot
+    id; per write entry its sorted-row word and the two f32 outputs, plus k, log_k and cpe; per
+    token its d_dva row (f32) and beta."""
+    vt = 2 if w.val_dtype == "bf16" else 4
+    bt = 2 if w.bank_dtype == "bf16" else 4
+    tok = w.N * w.C
+    ent = tok * w.W
+    return groups * (w.hd * (2 * grad_bytes + 2 * bt) + 4) + ent * (4 + 8 + vt + 4 + vt) + tok * (w.hd * 4 + 4)
+
+
+def pa_cpu_baseline(w, x, b, budget_s=12.0, max_chunks=None):
+    """The oracle's Phase A as it stands (float64, single thread) on a bounded sample: the chunks
+    of stream 0, last step first, on the rows that stream touches, until ~budget_s seconds passed.
+    ``x`` / ``b`` hold stream 0 alone (make_inputs / make_backward_inputs with streams=[0])."""
+    import oracle
+
+    P, C = x["P"], w.C
+    p = 0
+    ids = x["k_idx"][p::P].ravel()
+    slots = np.unique(ids[ids >= 0])
+    rng = np.random.default_rng(5)
+    grad = rng.standard_normal((len(slots), w.hd))
+    bank = np.zeros((len(slots), w.hd))
+    kvf = oracle.as_f64(x["k_val"], w.val_dtype)
+    t0 = time.perf_counter()
+    chunks = 0
+    for ti in range(w.steps - 1, -1, -1):
+        c = ti * P + p
+        V = w.valid_last if ti == w.steps - 1 else C
+        kk = np.searchsorted(slots, x["k_idx"][c]).astype(np.int32)
+        kk[x["k_idx"][c] < 0] = -1
+        ng = len(oracle.snapshot_slots(kk, S=len(slots), V=V))
+        lk = -rng.random((C, w.W))
+        cpe = np.exp(lk)
+        oracle.pa_chunk(grad, bank, rng.standard_normal((ng, w.hd)), kk, kvf[c], lk, cpe, b["beta"][c], b["dva"][c],
+                        S=len(slots), V=V)
+        chunks += 1
+        if time.perf_counter() - t0 > budget_s or (max_chunks and chunks >= max_chunks):
+            break
+    dt = time.perf_counter() - t0
+    toks = chunks * C
+    return {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks ({toks} tokens) of stream 0, last step first: Phase A, float64, "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_pa(args):
+    """The backward's Phase A over every step of the workload: one bench step = sdm_pa over steps
+    [0, steps) (one launch per step, last step first). Its inputs come from one untimed saving
+    forward (sorted rows, log_k, cpe, the dense compact snapshot) and the seeded generators (beta,
+    d_dva); grad rows are float32 (the --pa-grad bf16 option: the bank's format)."""
+    import torch
+
+    import sparse_slot_memory_gb300 as sdm
+    from synth import make_backward_inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sdm.build()
+    w = WORKLOADS[args.workload]
+    if args.streams:
+        w = scaled(w, P=args.streams)
+    if args.slots:
+        w = scaled(w, S=args.slots)
+    x = make_inputs(w)
+    b = make_backward_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.cuda()
+
+    d = {"k_idx": dev(x["k_idx"], "i"), "q_idx": dev(x["q_idx"], "i"), "k_val": dev(x["k_val"], w.val_dtype),
+         "q_val": dev(x["q_val"], w.val_dtype), "g": dev(x["g"], "f32"), "dv": dev(x["dv"], w.dv_dtype),
+         "beta": dev(b["beta"], "f32"), "dva": dev(b["dva"], "f32")}
+    del b
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2000 + w.seed + rank)
+    bdt = torch.bfloat16 if w.bank_dtype == "bf16" else torch.float32
+    bank = (torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen) * w.bank_scale).to(bdt)
+    ws = sdm.alloc_workspace(shape)
+    out = sdm.alloc_outputs(shape, fields=("log_k", "cpe", "sorted_k", "ngroups", "repeats"))
+    snap = sdm.alloc_snapshot(shape)
+    sdm.forward_chunks_saving(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], d["dv"], bank, snap,
+                              out, ws)
+    torch.cuda.synchronize()
+    assert sdm.device_status(ws) == 0
+    groups = int(out["ngroups"].sum().item())
+    del ws
+    gdt = torch.bfloat16 if args.pa_grad == "bf16" else torch.float32
+    grad = torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen).to(gdt)
+    d_k_eff = torch.empty((w.N, w.C, w.W), device="cuda")
+    grad_g = torch.empty((w.N, w.C, w.W), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sdm.pa(shape, out["sorted_k"], d["k_idx"], d["k_val"], out["log_k"], out["cpe"], d["beta"], d["dva"], grad,
+               bank, snap, d_k_eff, grad_g, 0, w.steps, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    assert int(status.item()) == 0
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = valid_tokens(w, w.P)
+    value = tokens * world / (ms / 1e3)
+
+    # End to end through the public call with host buffers: per pass, every per-token input of the
+    # pass H2D from pinned host memory (sorted rows, ids, k, log_k, cpe, beta, d_dva, the snapshot),
+    # the pass, both outputs D2H; grad and bank rows are resident state.
+    e2e = None
+    if not args.no_e2e:
+        ins = {"sorted_k": out["sorted_k"], "k_idx": d["k_idx"], "k_val": d["k_val"], "log_k": out["log_k"],
+               "cpe": out["cpe"], "beta": d["beta"], "dva": d["dva"], "snap": snap}
+        pin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in ins.items()}
+        outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in
+                  (("d_k_eff", d_k_eff), ("grad_g", grad_g))}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+        def e2e_step():
+            for k, v in pin.items():
+                ins[k].copy_(v, non_blocking=True)
+            sdm.pa(shape, ins["sorted_k"], ins["k_idx"], ins["k_val"], ins["log_k"], ins["cpe"], ins["beta"],
+                   ins["dva"], grad, bank, ins["snap"], d_k_eff, grad_g, 0, w.steps, status)
+            outs_h["d_k_eff"].copy_(d_k_eff, non_blocking=True)
+            outs_h["grad_g"].copy_(grad_g, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n2 = max(3, min(args.steps, 8))
+        a0 = time.perf_counter()
+        for _ in range(n2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = (time.perf_counter() - a0) * 1e3 / n2
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "per pass: every per-token input H2D from pinned host memory, the pass, both outputs D2H; "
+                       "one stream; grad and bank rows resident; host wall clock"}
+
+    peak, peak_kind = peaks()
+    ab = pa_algorithmic_bytes(w, groups, 2 if args.pa_grad == "bf16" else 4)
+    kern_ms = ms / w.steps                      # one launch per workload step
+    achieved = ab / w.steps / (kern_ms / 1e3) / 1e9
+    key = f"{args.workload}:pa{'_bf16grad' if args.pa_grad == 'bf16' else ''}:{src_hash('pa')}"
+    result = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else pa_cpu_baseline(w, make_inputs(w, streams=[0]),
+                                                                make_backward_inputs(w, streams=[0]),
+                                                                budget_s=args.cpu_seconds)
+        result = {
+            "metric": "SDM backward Phase A (the backward of DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generators; Phase-1 outputs and snapshot from one saving forward)",
+            "config": {"workload": w.name + "+phaseA" + ("+bf16grad" if args.pa_grad == "bf16" else ""),
+                       **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "grad": args.pa_grad, "tokens_per_step_per_gpu": tokens,
+                       "parallelism": f"replicas x{world} (independent streams)",
+                       "l2": "inputs larger than L2 (16 GiB f32 grad rows, 8 GiB bank)"},
+            "kernels_ms": {"pa_per_launch": kern_ms}, "algorithmic_bytes": ab, "groups": groups,
+            "roofline": {"bound": "hbm", "kernel": "pa", "achieved": achieved, "peak": peak,
+                         "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": NCU_TRAFFIC.get(key)},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": w.steps * args.steps,
+            "clocks": clk.summary(), "impl": "ours",
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
 def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
     """The oracle as it stands (float64, single thread) on a bounded sample: whole steps of one
     stream (Phase 1 with the pair triangles, then DW), until ~budget_s seconds have passed."""
@@ -417,9 +620,13 @@ def main():
     ap.add_argument("--streams", type=int, default=0, help="override the workload's stream count (profiling runs)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slots per stream (profiling runs)")
     ap.add_argument("--saving", action="store_true", help="time the saving forward (DW writes the dense snapshot)")
+    ap.add_argument("--pa", action="store_true", help="time the backward's Phase A over every step instead")
+    ap.add_argument("--pa-grad", default="f32", choices=["f32", "bf16"], help="grad row format of --pa")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.pa:
+        run_pa(args)
     else:
         run_ours(args)
 

@@ -227,6 +227,43 @@ sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const int32_t* k_i
                                       int32_t* status_out, sdm_stream_t stream);
 
 /*
+ * Phase A of the backward (pa_dc_cuda.py, module docstring: "PA per write group"; records kernel):
+ * the backward of DW for the steps [step_begin, step_end), LAST step first (one launch per step;
+ * step ti reads the grad rows step ti + 1 wrote). Per valid write group of chunk c = ti * P + p
+ * (slot s, members m in sorted order, as sorted_k lists them):
+ *   sc_m = -beta[c, tok_m] * (f32(k_m) * expf(log_k_m))
+ *   acc = 0; acc = fmaf(sc_m, dva[c, tok_m], acc) over the members in order
+ *   grad[p*S + s] = RN(fmaf(gdw, cpe_last, acc))    gdw = the row before this step, cpe_last = cpe of
+ *                                                    the group's last member (f32 grad: the fmaf itself)
+ *   bank[p*S + s] = the group's snapshot row        (raw bytes: the row before the forward's write)
+ *   grad_g[e] = cpe_e * <gdw, snap>,  d_k_eff[e] = -beta[c, tok_e] * <dva[c, tok_e], snap>
+ * Dots are f32: per lane an fmaf chain over 4 columns of a 128-column slice, an xor butterfly over
+ * the 32 lanes, slices added in order, so results do not depend on the launch geometry.
+ * Arguments (device pointers, 16-byte aligned, caller-owned; shapes use `shape`'s N = steps * P):
+ *   grad_dtype: sdm_dtype of grad (SDM_F32, or SDM_BF16 for grad rows in the bank's format).
+ *   sorted_k [N, C*W] int32: as sdm_phase1 writes it (entries whose slot is outside [0, S) are
+ *            invalid there). log_k f32 / cpe val_dtype [N, C, W]: sdm_phase1's outputs.
+ *   k_idx int32 / k_val val_dtype [N, C, W]: the forward's inputs. beta f32 [N, C].
+ *   dva f32 [N, C, hd]: the gradient of the forward's token rows (dv) for these steps.
+ *   grad [P*S, hd] grad_dtype, bank [P*S, hd] bank_dtype: updated in place.
+ *   snap: the dense compact snapshot rows of the steps in range, [step_end - step_begin, P, C*W, hd]
+ *         in the bank dtype: row ((ti - step_begin) * P + p) * C*W + g for the group of dense ordinal g
+ *         (sdm_dw_saving's layout; a caller holding all N chunks passes its row step_begin * P * C*W).
+ *   d_k_eff, grad_g [N, C, W] f32: written for every entry of the range's chunks (0 for invalid
+ *         entries).
+ *   status (nullable): device word OR-ed with SDM_DEV_BAD_SLOT when a group's slot (k_idx of its
+ *         first member) lies outside [0, S); the group is then skipped.
+ * Errors: SDM_ERR_SHAPE / SDM_ERR_DTYPE / SDM_ERR_ALIGN for the shape (as sdm_phase1), grad_dtype
+ * not 0 or 1 -> SDM_ERR_DTYPE, a NULL array -> SDM_ERR_ARG, a misaligned array -> SDM_ERR_ALIGN, a
+ * bad step range -> SDM_ERR_ARG, a failed launch -> SDM_ERR_CUDA. No launch happens on an error
+ * found before the first launch.
+ */
+sdm_status sdm_pa(const sdm_shape* shape, int32_t grad_dtype, const int32_t* sorted_k, const int32_t* k_idx,
+                  const void* k_val, const float* log_k, const void* cpe, const float* beta, const float* dva,
+                  void* grad, void* bank, const void* snap, float* d_k_eff, float* grad_g, int64_t step_begin,
+                  int64_t step_end, uint32_t* status, sdm_stream_t stream);
+
+/*
  * Synchronizes `stream`, reads the workspace's device status word into *code_out (0 = fine,
  * else SDM_DEV_* bits) and, if `clear`, zeroes it. Returns SDM_ERR_DEVICE when the word is
  * nonzero, SDM_ERR_CUDA when the copy fails.

@@ -195,6 +195,22 @@ def forward_chunks_noalloc(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, 
     _check(st, "sdm_forward_chunks_noalloc")
 
 
+def pa(shape: ShapeSpec, sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, bank, snap, d_k_eff, grad_g,
+       step_begin=0, step_end=None, status=None, stream=None):
+    """sdm_pa: Phase A of the backward for steps [step_begin, step_end), last step first.
+    ``grad`` is float32 or bfloat16 (its dtype is passed as grad_dtype); ``snap`` holds the range's
+    snapshot rows ([steps in range, P, C*W, hd]); ``status`` (optional) is a CUDA int32 tensor of one
+    element to which SDM_DEV_* bits are OR-ed."""
+    step_end = shape.steps if step_end is None else step_end
+    gdt = {torch.float32: _abi.SDM_F32, torch.bfloat16: _abi.SDM_BF16}.get(grad.dtype)
+    if gdt is None:
+        raise TypeError("grad must be float32 or bfloat16")
+    st = _abi.load().sdm_pa(ctypes.byref(shape.c()), gdt, _ptr(sorted_k), _ptr(k_idx), _ptr(k_val), _ptr(log_k),
+                            _ptr(cpe), _ptr(beta), _ptr(dva), _ptr(grad), _ptr(bank), _ptr(snap), _ptr(d_k_eff),
+                            _ptr(grad_g), step_begin, step_end, _ptr(status), _stream(stream))
+    _check(st, "sdm_pa")
+
+
 def device_status(ws, clear: bool = True, stream=None) -> int:
     code = _abi.c_i32(0)
     st = _abi.load().sdm_device_status(_ptr(ws), ctypes.byref(code), int(clear), _stream(stream))

@@ -1,0 +1,397 @@
+// sdm_pa.cu -- Phase A of the chunked sparse-delta-memory backward: the backward of DW, one step
+// at a time, and its C entry point sdm_pa (include/sdm.h).
+//
+// Arithmetic (sparse-delta-memory 2.0.0, pa_dc_cuda.py module docstring, "PA per write group", and
+// its records kernel): per valid write group of a chunk (slot s, members m in Phase-1 sorted order),
+// with gdw = grad[s] before the step and snap = the group's row of the dense compact snapshot,
+//   sc_m = -beta[tok_m] * (f32(k_m) * expf(log_k_m))
+//   acc = 0; acc = fmaf(sc_m, d_dva[tok_m], acc) over the members in order
+//   grad[s] = RN(fmaf(gdw, cpe_last, acc))          (f32: the fmaf result itself)
+//   bank[s] = snap                                    (raw copy of the pre-write row)
+//   grad_g[e] = cpe_e * <gdw, snap>,  d_k_eff[e] = -beta[tok_e] * <d_dva[tok_e], snap>.
+// Every dot is summed the same way whatever the tiling: a lane sums its 4 columns of a 128-column
+// slice in column order (an fmaf chain), the 32 lane partials meet in an xor butterfly (levels 16,
+// 8, 4, 2, 1; both partners add the same pair, so every lane holds the same bits), and the slices'
+// sums add in slice order from 0.
+//
+// GB300 design: one launch per step; a CTA of 8 warps takes one chunk and a tile of 256 sorted
+// positions, a warp the groups whose FIRST lies in its 32 positions (a group may run past the tile:
+// the warp follows it to its LAST). The dense ordinal of a group (its snapshot row) is the count of
+// valid FIRST flags before it in the sorted row: each CTA counts the positions before its tile once.
+// Rows move as a lane's 4 columns (16 bytes f32 / 8 bytes bf16, 512 / 256 contiguous bytes per warp
+// access); the token rows of 8 members are in flight before their FMAs. A group of more than 32
+// members (a hot slot) takes its slices one after the other and keeps each member's dot sum in the
+// d_k_eff output between slices (the member's own lane stores and re-reads it), so its arithmetic
+// is that of a short group.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "sdm_internal.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kPaThreads = 256;
+constexpr int kPaWarps = kPaThreads / 32;
+constexpr int kPaTile = kPaThreads;        // sorted positions per CTA: 32 per warp
+constexpr int kPaBatch = 8;                // member token rows in flight
+constexpr uint32_t kPaSentinel = kFirst | kLast | kInvalidBit;
+
+struct PAArgs {
+    const int32_t* sorted_k;   // [N, nk]
+    const int32_t* k_idx;      // [N, C, W]
+    const void* k_val;         // [N, C, W] value type
+    const float* log_k;        // [N, C, W]
+    const void* cpe;           // [N, C, W] value type
+    const float* beta;         // [N, C]
+    const float* dva;          // [N, C, hd]
+    void* grad;                // [P * S, hd] grad type
+    void* bank;                // [P * S, hd] bank type
+    const void* snap;          // this step's snapshot rows: [P, nk, hd] bank type
+    float* d_k_eff;            // [N, C, W]
+    float* grad_g;             // [N, C, W]
+    uint32_t* status;          // nullable
+    int P, C, W, nk, hd, nsl, tiles;
+    int64_t S, c0;             // c0: the step's first chunk
+};
+
+__device__ __forceinline__ float widen(float x) { return x; }
+__device__ __forceinline__ float widen(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// a lane's 4 columns of a row as floats
+__device__ __forceinline__ void ld4(const float* p, float (&o)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+// the grad row is read once and rewritten in the same launch: the coherent L2 path
+__device__ __forceinline__ void ld4cg(const float* p, float (&o)[4]) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void ld4cg(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
+    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ void st4(float* p, const float (&o)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+// raw copy of a lane's 4 columns (the snapshot row is the bank row's bytes)
+__device__ __forceinline__ void copy4(float* d, const float* s) {
+    *reinterpret_cast<float4*>(d) = __ldg(reinterpret_cast<const float4*>(s));
+}
+__device__ __forceinline__ void copy4(__nv_bfloat16* d, const __nv_bfloat16* s) {
+    *reinterpret_cast<uint2*>(d) = __ldg(reinterpret_cast<const uint2*>(s));
+}
+
+__device__ __forceinline__ float dot4(const float (&x)[4], const float (&y)[4]) {
+    return fmaf(x[3], y[3], fmaf(x[2], y[2], fmaf(x[1], y[1], x[0] * y[0])));
+}
+__device__ __forceinline__ float allsum(float x) {
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) x += __shfl_xor_sync(kFull, x, k);
+    return x;
+}
+__device__ __forceinline__ bool valid_first(uint32_t v) { return (v & kFirst) != 0 && (v & kInvalidBit) == 0; }
+
+// One window of up to 32 members of a group, lane i holding member i.
+struct Member {
+    int n;          // members in this window
+    bool last;      // the window holds the group's LAST
+    bool ok;        // lane < n and the entry names a token and lane of the chunk
+    int tok;        // token (0 when !ok)
+    int64_t o;      // entry index of the chunk's [C, W] arrays (global)
+    float sc, cp, beta;
+};
+
+template <typename ValT>
+__device__ __forceinline__ Member member_window(const PAArgs& a, const int32_t* srow, int q, int64_t c, int lane) {
+    Member m;
+    const int pos = q + lane;
+    const uint32_t v = pos < a.nk ? static_cast<uint32_t>(__ldg(srow + pos)) : kPaSentinel;
+    const uint32_t lastm = __ballot_sync(kFull, (v & kLast) != 0);
+    m.last = lastm != 0;
+    m.n = m.last ? __ffs(lastm) : 32;
+    const int t = static_cast<int>((v >> kTokenShift) & 0xFFu);
+    const int j = static_cast<int>(v & 0xFFu);
+    m.ok = lane < m.n && (v & kInvalidBit) == 0 && t < a.C && j < a.W;
+    m.tok = m.ok ? t : 0;
+    m.o = c * a.nk + (m.ok ? t * a.W + j : 0);
+    m.sc = 0.f;
+    m.cp = 1.f;
+    m.beta = 0.f;
+    if (m.ok) {
+        const float kv = widen(static_cast<const ValT*>(a.k_val)[m.o]);
+        const float lk = __ldg(a.log_k + m.o);
+        m.cp = widen(static_cast<const ValT*>(a.cpe)[m.o]);
+        m.beta = __ldg(a.beta + c * a.C + t);
+        m.sc = -m.beta * (kv * expf(lk));
+    }
+    return m;
+}
+
+// acc += the window's terms on this lane's 4 columns; returns this lane's member's <dva, snap> sum
+// over the slice (lanes >= m.n get 0).
+__device__ __forceinline__ float window_terms(const Member& m, const float* dva_col, int hd, bool on,
+                                              const float (&sn)[4], float (&acc)[4], int lane) {
+    float mine = 0.f;
+    const uint32_t okm = __ballot_sync(kFull, m.ok);   // members that name an entry of the chunk
+    for (int k0 = 0; k0 < m.n; k0 += kPaBatch) {
+        float d[kPaBatch][4];
+#pragma unroll
+        for (int u = 0; u < kPaBatch; ++u) {
+            const int tk = __shfl_sync(kFull, m.tok, (k0 + u) & 31);
+            if (((okm >> ((k0 + u) & 31)) & 1u) && k0 + u < m.n && on) {
+                ld4(dva_col + static_cast<int64_t>(tk) * hd, d[u]);
+            } else {
+                d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPaBatch; ++u) {
+            const float s = __shfl_sync(kFull, m.sc, (k0 + u) & 31);
+            if (k0 + u < m.n && ((okm >> ((k0 + u) & 31)) & 1u)) {   // warp-uniform
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = fmaf(s, d[u][i], acc[i]);
+                const float r = allsum(dot4(d[u], sn));
+                if (lane == k0 + u) mine = r;
+            }
+        }
+    }
+    return mine;
+}
+
+template <typename GradT, typename BankT, typename ValT>
+__global__ void __launch_bounds__(kPaThreads) pa_kernel(const PAArgs a) {
+    __shared__ int before_s[kPaWarps];   // valid FIRSTs before the tile, per warp's share of the count
+    __shared__ int in_s[kPaWarps];       // valid FIRSTs in each warp's 32 positions
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cl = static_cast<int>(blockIdx.x / a.tiles);   // stream of the chunk
+    const int tile = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.tiles);
+    const int64_t c = a.c0 + cl;
+    const int nk = a.nk, hd = a.hd;
+    const int32_t* const srow = a.sorted_k + c * nk;
+    const int r0 = tile * kPaTile;
+
+    int before = 0;
+    for (int i = threadIdx.x; i < r0; i += kPaThreads) before += valid_first(static_cast<uint32_t>(__ldg(srow + i)));
+    before = __reduce_add_sync(kFull, before);
+    const int q0 = r0 + warp * 32;
+    const int pos = q0 + lane;
+    const uint32_t v = pos < nk ? static_cast<uint32_t>(__ldg(srow + pos)) : kPaSentinel;
+    const uint32_t fmask = __ballot_sync(kFull, valid_first(v));
+    if (lane == 0) {
+        before_s[warp] = before;
+        in_s[warp] = __popc(fmask);
+    }
+    __syncthreads();
+    int ord = 0;
+#pragma unroll
+    for (int w = 0; w < kPaWarps; ++w) ord += before_s[w] + (w < warp ? in_s[w] : 0);
+
+    // invalid entries of these positions: zero outputs
+    if (pos < nk && (v & kInvalidBit) != 0) {
+        const int t = static_cast<int>((v >> kTokenShift) & 0xFFu), j = static_cast<int>(v & 0xFFu);
+        if (t < a.C && j < a.W) {
+            a.d_k_eff[c * nk + t * a.W + j] = 0.f;
+            a.grad_g[c * nk + t * a.W + j] = 0.f;
+        }
+    }
+
+    GradT* const grad = static_cast<GradT*>(a.grad);
+    BankT* const bank = static_cast<BankT*>(a.bank);
+    const BankT* const snap = static_cast<const BankT*>(a.snap);
+    const float* const dva_chunk = a.dva + c * a.C * static_cast<int64_t>(hd);
+    uint32_t bad = 0;
+    for (uint32_t fm = fmask; fm != 0; fm &= fm - 1u, ++ord) {
+        const int f = q0 + __ffs(fm) - 1;
+        const Member m0 = member_window<ValT>(a, srow, f, c, lane);
+        const int32_t s = __shfl_sync(kFull, m0.ok ? __ldg(a.k_idx + m0.o) : -1, 0);
+        if (s < 0 || static_cast<int64_t>(s) >= a.S) {   // not a row of the bank: the group is dropped
+            bad |= 1u;
+            continue;
+        }
+        const int64_t row = (static_cast<int64_t>(cl) * a.S + s) * hd;
+        const int64_t srow_g = (static_cast<int64_t>(cl) * nk + ord) * hd;
+        float gsum = 0.f;
+        if (m0.last) {
+            // ---- a group of at most 32 members: its scalars stay in the lanes ----------------
+            const float cpl = __shfl_sync(kFull, m0.cp, m0.n - 1);
+            float dk = 0.f;
+            for (int sl = 0; sl < a.nsl; ++sl) {
+                const int col = sl * 128 + lane * 4;
+                const bool on = col < hd;
+                float g4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (on) {
+                    ld4cg(grad + row + col, g4);
+                    ld4(snap + srow_g + col, s4);
+                    copy4(bank + row + col, snap + srow_g + col);
+                }
+                gsum += allsum(dot4(g4, s4));
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                dk += window_terms(m0, dva_chunk + col, hd, on, s4, acc, lane);
+                if (on) {
+                    float o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = fmaf(g4[i], cpl, acc[i]);
+                    st4(grad + row + col, o);
+                }
+            }
+            if (m0.ok) {
+                a.d_k_eff[m0.o] = -m0.beta * dk;
+                a.grad_g[m0.o] = m0.cp * gsum;
+            }
+        } else {
+            // ---- a long group: slices outside, windows inside; dot sums kept in d_k_eff --------
+            for (int sl = 0; sl < a.nsl; ++sl) {
+                const int col = sl * 128 + lane * 4;
+                const bool on = col < hd;
+                float g4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (on) {
+                    ld4cg(grad + row + col, g4);
+                    ld4(snap + srow_g + col, s4);
+                    copy4(bank + row + col, snap + srow_g + col);
+                }
+                gsum += allsum(dot4(g4, s4));
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float cpl = 1.f;
+                for (int q = f;; q += 32) {
+                    const Member m = member_window<ValT>(a, srow, q, c, lane);
+                    const float r = window_terms(m, dva_chunk + col, hd, on, s4, acc, lane);
+                    if (m.ok) a.d_k_eff[m.o] = (sl == 0 ? 0.f : a.d_k_eff[m.o]) + r;
+                    if (m.last) {
+                        cpl = __shfl_sync(kFull, m.cp, m.n - 1);
+                        break;
+                    }
+                }
+                if (on) {
+                    float o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = fmaf(g4[i], cpl, acc[i]);
+                    st4(grad + row + col, o);
+                }
+            }
+            for (int q = f;; q += 32) {
+                const Member m = member_window<ValT>(a, srow, q, c, lane);
+                if (m.ok) {
+                    a.d_k_eff[m.o] = -m.beta * a.d_k_eff[m.o];
+                    a.grad_g[m.o] = m.cp * gsum;
+                }
+                if (m.last) break;
+            }
+        }
+    }
+    if (bad && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
+}
+
+template <typename GradT, typename BankT, typename ValT>
+cudaError_t launch_t(const PAArgs& a, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>(a.P) * static_cast<unsigned>(a.tiles);
+    pa_kernel<GradT, BankT, ValT><<<blocks, kPaThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename GradT, typename BankT>
+cudaError_t launch_v(const PAArgs& a, int val_bf16, cudaStream_t stream) {
+    return val_bf16 ? launch_t<GradT, BankT, __nv_bfloat16>(a, stream) : launch_t<GradT, BankT, float>(a, stream);
+}
+
+cudaError_t launch_pa(const PAArgs& a, int grad_bf16, int bank_bf16, int val_bf16, cudaStream_t stream) {
+    if (grad_bf16)
+        return bank_bf16 ? launch_v<__nv_bfloat16, __nv_bfloat16>(a, val_bf16, stream)
+                         : launch_v<__nv_bfloat16, float>(a, val_bf16, stream);
+    return bank_bf16 ? launch_v<float, __nv_bfloat16>(a, val_bf16, stream) : launch_v<float, float>(a, val_bf16, stream);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// the shape rules of the forward's entry points (the same shape describes both directions)
+sdm_status check_shape(const sdm_shape* s) {
+    if (s == nullptr) return SDM_ERR_ARG;
+    if (s->val_dtype < 0 || s->val_dtype > 1 || s->dv_dtype < 0 || s->dv_dtype > 1 || s->bank_dtype < 0 ||
+        s->bank_dtype > 1)
+        return SDM_ERR_DTYPE;
+    if (s->P < 1 || s->C < 1 || s->C > kMaxC || s->W < 1 || s->W > kMaxLanes || s->R < 1 || s->R > kMaxLanes ||
+        s->steps < 1 || s->S < 1 || s->S > 0x7FFFFFFFll || s->hd < 1 || s->valid_last < 1 || s->valid_last > s->C ||
+        (s->gate_per_entry != 0 && s->gate_per_entry != 1))
+        return SDM_ERR_SHAPE;
+    if (s->hd % 4 != 0) return SDM_ERR_ALIGN;
+    const int64_t n = static_cast<int64_t>(s->C) * (s->W + s->R);
+    if (n > kMaxRow) return SDM_ERR_SHAPE;
+    if (s->steps > (int64_t(1) << 40) / s->P) return SDM_ERR_SHAPE;
+    const int64_t N = s->steps * s->P;
+    if (s->S > (int64_t(1) << 62) / s->P / s->hd) return SDM_ERR_SHAPE;
+    if (N > (int64_t(1) << 62) / (static_cast<int64_t>(s->C) * s->C + s->C * int64_t(s->hd) + n)) return SDM_ERR_SHAPE;
+    return SDM_OK;
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" sdm_status sdm_pa(const sdm_shape* shape, int32_t grad_dtype, const int32_t* sorted_k, const int32_t* k_idx,
+                             const void* k_val, const float* log_k, const void* cpe, const float* beta,
+                             const float* dva, void* grad, void* bank, const void* snap, float* d_k_eff,
+                             float* grad_g, int64_t step_begin, int64_t step_end, uint32_t* status,
+                             sdm_stream_t stream) {
+    sdm_status st = check_shape(shape);
+    if (st != SDM_OK) return st;
+    if (grad_dtype != SDM_F32 && grad_dtype != SDM_BF16) return SDM_ERR_DTYPE;
+    if (step_begin < 0 || step_end > shape->steps || step_begin > step_end) return SDM_ERR_ARG;
+    const void* ptrs[] = {sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, bank, snap, d_k_eff, grad_g};
+    for (const void* p : ptrs)
+        if (p == nullptr) return SDM_ERR_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return SDM_ERR_ALIGN;
+    if (step_begin == step_end) return SDM_OK;
+    PAArgs a;
+    memset(&a, 0, sizeof(a));
+    a.sorted_k = sorted_k;
+    a.k_idx = k_idx;
+    a.k_val = k_val;
+    a.log_k = log_k;
+    a.cpe = cpe;
+    a.beta = beta;
+    a.dva = dva;
+    a.grad = grad;
+    a.bank = bank;
+    a.d_k_eff = d_k_eff;
+    a.grad_g = grad_g;
+    a.status = status;
+    a.P = shape->P;
+    a.C = shape->C;
+    a.W = shape->W;
+    a.nk = shape->C * shape->W;
+    a.hd = shape->hd;
+    a.nsl = (shape->hd + 127) / 128;
+    a.tiles = (a.nk + kPaTile - 1) / kPaTile;
+    a.S = shape->S;
+    const size_t bank_elem = shape->bank_dtype == SDM_BF16 ? 2 : 4;
+    const int64_t step_rows = static_cast<int64_t>(a.P) * a.nk;   // snapshot rows of one step
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // the backward runs the steps last to first: step ti reads the grad rows step ti + 1 wrote
+    for (int64_t ti = step_end - 1; ti >= step_begin; --ti) {
+        a.c0 = ti * a.P;
+        a.snap = static_cast<const unsigned char*>(snap) + (ti - step_begin) * step_rows * a.hd * bank_elem;
+        if (launch_pa(a, grad_dtype == SDM_BF16, shape->bank_dtype == SDM_BF16, shape->val_dtype == SDM_BF16, cs) !=
+            cudaSuccess)
+            return SDM_ERR_CUDA;
+    }
+    return SDM_OK;
+}

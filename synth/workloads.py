@@ -173,3 +173,39 @@ def make_bank_stream(w: Workload, p: int) -> np.ndarray:
     rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 7]))
     x = (rng.standard_normal((w.S, w.hd), dtype=np.float32) * np.float32(w.bank_scale)).astype(np.float32)
     return f32_to_bf16_bits(x) if w.bank_dtype == "bf16" else x
+
+
+# ---- inputs of the backward's Phase A (the backward of DW) ------------------------------------
+# The Phase-A contract (pa_dc_cuda.py, module docstring) takes, besides the forward's inputs and
+# Phase-1 outputs: beta [N, C] (a write strength per token, here sigmoid(N(0, 1))), d_dva [N, C, hd]
+# float32 (the gradient of the token rows, normal with dv_scale), the grad rows [P * S, hd] (normal,
+# scale 1) and the dense compact snapshot rows (any rows of the bank dtype: normal with bank_scale).
+
+def make_backward_inputs(w: Workload, streams=None) -> dict:
+    """beta [N, C] float32 and dva [N, C, hd] float32, chunk-major like make_inputs."""
+    streams = list(range(w.P)) if streams is None else list(streams)
+    Ps, st, C, hd = len(streams), w.steps, w.C, w.hd
+    beta = np.empty((st, Ps, C), np.float32)
+    dva = np.empty((st, Ps, C, hd), np.float32)
+    for i, p in enumerate(streams):
+        r_b, r_d = [np.random.default_rng(s) for s in np.random.SeedSequence([w.seed, p, 11]).spawn(2)]
+        z = r_b.standard_normal((st, C))
+        beta[:, i] = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+        dva[:, i] = (r_d.standard_normal((st, C, hd), dtype=np.float32) * np.float32(w.dv_scale)).astype(np.float32)
+    N = st * Ps
+    return {"beta": beta.reshape(N, C), "dva": dva.reshape(N, C, hd)}
+
+
+def make_grad_stream(w: Workload, p: int, rows=None) -> np.ndarray:
+    """Grad rows of stream p before the backward's first Phase-A step: [S, hd] float32 normal (or
+    only the rows ``rows`` of it, drawn the same)."""
+    rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 13]))
+    x = rng.standard_normal((w.S, w.hd), dtype=np.float32)
+    return x if rows is None else x[rows]
+
+
+def make_snapshot_chunk(w: Workload, c: int) -> np.ndarray:
+    """Dense compact snapshot rows of chunk c: [C * W, hd] in the bank dtype (uint16 bits for bf16)."""
+    rng = np.random.default_rng(np.random.SeedSequence([w.seed, c, 17]))
+    x = (rng.standard_normal((w.C * w.W, w.hd), dtype=np.float32) * np.float32(w.bank_scale)).astype(np.float32)
+    return f32_to_bf16_bits(x) if w.bank_dtype == "bf16" else x
