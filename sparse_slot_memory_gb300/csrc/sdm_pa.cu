@@ -36,7 +36,9 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr int kPaThreads = 256;
 constexpr int kPaWarps = kPaThreads / 32;
 constexpr int kPaTile = kPaThreads;        // sorted positions per CTA: 32 per warp
-constexpr int kPaBatch = 8;                // member token rows in flight
+constexpr int kPaBatch = 4;                // a long group's member token rows in flight together
+constexpr int kPaRing = 8;                 // in-window positions whose rows are in flight (per warp)
+constexpr int kPaCountUnroll = 16;         // sorted words per thread in flight while counting FIRSTs
 constexpr uint32_t kPaSentinel = kFirst | kLast | kInvalidBit;
 
 struct PAArgs {
@@ -97,6 +99,14 @@ __device__ __forceinline__ void copy4(float* d, const float* s) {
 }
 __device__ __forceinline__ void copy4(__nv_bfloat16* d, const __nv_bfloat16* s) {
     *reinterpret_cast<uint2*>(d) = __ldg(reinterpret_cast<const uint2*>(s));
+}
+
+// raw copy of a lane's 4 columns from shared memory (the snapshot row's bytes)
+__device__ __forceinline__ void copy_raw4(float* d, const float* s) {
+    *reinterpret_cast<float4*>(d) = *reinterpret_cast<const float4*>(s);
+}
+__device__ __forceinline__ void copy_raw4(__nv_bfloat16* d, const __nv_bfloat16* s) {
+    *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(s);
 }
 
 __device__ __forceinline__ float dot4(const float (&x)[4], const float (&y)[4]) {
@@ -176,11 +186,114 @@ __device__ __forceinline__ float window_terms(const Member& m, const float* dva_
     return mine;
 }
 
+// A group that starts at sorted position f and ends past its warp's 32 positions (a hot slot):
+// windows of 32 members follow it to its LAST; slices outside, windows inside, each member's dot
+// sum kept in d_k_eff between slices. Same arithmetic and order as the in-window groups.
 template <typename GradT, typename BankT, typename ValT>
-__global__ void __launch_bounds__(kPaThreads) pa_kernel(const PAArgs a) {
+__device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, int64_t c, int cl, int f, int ord,
+                                        int lane, uint32_t* bad) {
+    GradT* const grad = static_cast<GradT*>(a.grad);
+    BankT* const bank = static_cast<BankT*>(a.bank);
+    const BankT* const snap = static_cast<const BankT*>(a.snap);
+    const int hd = a.hd;
+    const float* const dva_chunk = a.dva + c * a.C * static_cast<int64_t>(hd);
+    const Member m0 = member_window<ValT>(a, srow, f, c, lane);
+    const int32_t s = __shfl_sync(kFull, m0.ok ? __ldg(a.k_idx + m0.o) : -1, 0);
+    if (s < 0 || static_cast<int64_t>(s) >= a.S) {   // not a row of the bank: the group is dropped
+        *bad = 1u;
+        for (int q = f;; q += 32) {
+            const Member m = member_window<ValT>(a, srow, q, c, lane);
+            if (m.ok) a.d_k_eff[m.o] = a.grad_g[m.o] = 0.f;
+            if (m.last) break;
+        }
+        return;
+    }
+    const int64_t row = (static_cast<int64_t>(cl) * a.S + s) * hd;
+    const int64_t srow_g = (static_cast<int64_t>(cl) * a.nk + ord) * hd;
+    float gsum = 0.f;
+    for (int sl = 0; sl < a.nsl; ++sl) {
+        const int col = sl * 128 + lane * 4;
+        const bool on = col < hd;
+        float g4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (on) {
+            ld4cg(grad + row + col, g4);
+            ld4(snap + srow_g + col, s4);
+            copy4(bank + row + col, snap + srow_g + col);
+        }
+        gsum += allsum(dot4(g4, s4));
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float cpl = 1.f;
+        for (int q = f;; q += 32) {
+            const Member m = member_window<ValT>(a, srow, q, c, lane);
+            const float r = window_terms(m, dva_chunk + col, hd, on, s4, acc, lane);
+            if (m.ok) a.d_k_eff[m.o] = (sl == 0 ? 0.f : a.d_k_eff[m.o]) + r;
+            if (m.last) {
+                cpl = __shfl_sync(kFull, m.cp, m.n - 1);
+                break;
+            }
+        }
+        if (on) {
+            float o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = fmaf(g4[i], cpl, acc[i]);
+            st4(grad + row + col, o);
+        }
+    }
+    for (int q = f;; q += 32) {
+        const Member m = member_window<ValT>(a, srow, q, c, lane);
+        if (m.ok) {
+            a.d_k_eff[m.o] = -m.beta * a.d_k_eff[m.o];
+            a.grad_g[m.o] = m.cp * gsum;
+        }
+        if (m.last) break;
+    }
+}
+
+// Per-lane asynchronous copies into shared memory (each lane later reads back only what it copied).
+__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src, int bytes) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    if (bytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <typename T>
+__device__ __forceinline__ void get4(const T* p, float (&o)[4]);
+template <>
+__device__ __forceinline__ void get4(const float* p, float (&o)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void get4(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+// Shared memory of one warp: a ring of kPaRing positions, per position and lane the lane's 4 columns
+// of the token row (f32), of the grad row and of the snapshot row.
+template <typename GradT, typename BankT>
+struct PaRing {
+    float4 dva[kPaRing][32];
+    GradT grad[kPaRing][32][4];
+    BankT snap[kPaRing][32][4];
+};
+
+template <typename GradT, typename BankT>
+constexpr size_t pa_smem_bytes() { return sizeof(PaRing<GradT, BankT>) * kPaWarps; }
+
+template <typename GradT, typename BankT, typename ValT>
+__global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
     __shared__ int before_s[kPaWarps];   // valid FIRSTs before the tile, per warp's share of the count
     __shared__ int in_s[kPaWarps];       // valid FIRSTs in each warp's 32 positions
+    extern __shared__ __align__(16) unsigned char pa_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    PaRing<GradT, BankT>& ring = reinterpret_cast<PaRing<GradT, BankT>*>(pa_smem)[warp];
     const int cl = static_cast<int>(blockIdx.x / a.tiles);   // stream of the chunk
     const int tile = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.tiles);
     const int64_t c = a.c0 + cl;
@@ -188,121 +301,167 @@ __global__ void __launch_bounds__(kPaThreads) pa_kernel(const PAArgs a) {
     const int32_t* const srow = a.sorted_k + c * nk;
     const int r0 = tile * kPaTile;
 
-    int before = 0;
-    for (int i = threadIdx.x; i < r0; i += kPaThreads) before += valid_first(static_cast<uint32_t>(__ldg(srow + i)));
-    before = __reduce_add_sync(kFull, before);
+    // ---- this lane's sorted position and its entry's scalars (all lanes at once) ----------------
     const int q0 = r0 + warp * 32;
     const int pos = q0 + lane;
     const uint32_t v = pos < nk ? static_cast<uint32_t>(__ldg(srow + pos)) : kPaSentinel;
+    const int t = static_cast<int>((v >> kTokenShift) & 0xFFu), j = static_cast<int>(v & 0xFFu);
+    const bool named = t < a.C && j < a.W;              // names an entry of the chunk
+    const bool ok = (v & kInvalidBit) == 0 && named;
+    const int64_t o = c * nk + (named ? t * a.W + j : 0);
+    int32_t slot = -1;
+    float sc = 0.f, cp = 1.f, be = 0.f;
+    if (ok) {
+        slot = __ldg(a.k_idx + o);
+        const float kv = widen(static_cast<const ValT*>(a.k_val)[o]);
+        const float lk = __ldg(a.log_k + o);
+        cp = widen(static_cast<const ValT*>(a.cpe)[o]);
+        be = __ldg(a.beta + c * a.C + t);
+        sc = -be * (kv * expf(lk));
+    }
     const uint32_t fmask = __ballot_sync(kFull, valid_first(v));
+    const uint32_t lmask = __ballot_sync(kFull, ok && (v & kLast) != 0);
+    const uint32_t okmask = __ballot_sync(kFull, ok);
+
+    // ---- dense ordinal of the window's first group: valid FIRSTs before it ----------------------
+    // (the loads of a thread's words are issued together: a 4096-entry row is one round trip)
+    int before = 0;
+    for (int i0 = threadIdx.x; i0 < r0; i0 += kPaThreads * kPaCountUnroll) {
+        uint32_t wv[kPaCountUnroll];
+#pragma unroll
+        for (int u = 0; u < kPaCountUnroll; ++u) {
+            const int i = i0 + u * kPaThreads;
+            wv[u] = i < r0 ? static_cast<uint32_t>(__ldg(srow + i)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kPaCountUnroll; ++u) before += valid_first(wv[u]);
+    }
+    before = __reduce_add_sync(kFull, before);
     if (lane == 0) {
         before_s[warp] = before;
         in_s[warp] = __popc(fmask);
     }
     __syncthreads();
-    int ord = 0;
+    int ord0 = 0;
 #pragma unroll
-    for (int w = 0; w < kPaWarps; ++w) ord += before_s[w] + (w < warp ? in_s[w] : 0);
+    for (int w = 0; w < kPaWarps; ++w) ord0 += before_s[w] + (w < warp ? in_s[w] : 0);
 
     // invalid entries of these positions: zero outputs
-    if (pos < nk && (v & kInvalidBit) != 0) {
-        const int t = static_cast<int>((v >> kTokenShift) & 0xFFu), j = static_cast<int>(v & 0xFFu);
-        if (t < a.C && j < a.W) {
-            a.d_k_eff[c * nk + t * a.W + j] = 0.f;
-            a.grad_g[c * nk + t * a.W + j] = 0.f;
-        }
-    }
+    if ((v & kInvalidBit) != 0 && pos < nk && named) a.d_k_eff[o] = a.grad_g[o] = 0.f;
+    if (fmask == 0) return;   // no group starts here (a previous warp's group, or invalid entries)
+
+    // ---- the groups that start and end in this window: positions [f0, cend] ----------------------
+    // The last group to start here may run past the window ("open"); it is walked afterwards.
+    const int f0 = __ffs(fmask) - 1;
+    const int flast = 31 - __clz(fmask);
+    const bool open = (lmask >> flast) == 0u;
+    const int cend = open ? flast - 1 : 31 - __clz(lmask);
+    // this lane's group: the nearest FIRST at or before it (its lane index), -1 if none
+    const uint32_t upto = fmask & (lane == 31 ? kFull : ((2u << lane) - 1u));
+    const int myf = upto ? 31 - __clz(upto) : -1;
+    const bool mine = ok && myf >= 0 && lane <= cend;    // this lane's entry is in a closed group here
+    const int32_t gslot = __shfl_sync(kFull, slot, myf < 0 ? 0 : myf);
+    const bool mybad = gslot < 0 || static_cast<int64_t>(gslot) >= a.S;
 
     GradT* const grad = static_cast<GradT*>(a.grad);
     BankT* const bank = static_cast<BankT*>(a.bank);
     const BankT* const snap = static_cast<const BankT*>(a.snap);
     const float* const dva_chunk = a.dva + c * a.C * static_cast<int64_t>(hd);
     uint32_t bad = 0;
-    for (uint32_t fm = fmask; fm != 0; fm &= fm - 1u, ++ord) {
-        const int f = q0 + __ffs(fm) - 1;
-        const Member m0 = member_window<ValT>(a, srow, f, c, lane);
-        const int32_t s = __shfl_sync(kFull, m0.ok ? __ldg(a.k_idx + m0.o) : -1, 0);
-        if (s < 0 || static_cast<int64_t>(s) >= a.S) {   // not a row of the bank: the group is dropped
-            bad |= 1u;
-            continue;
-        }
-        const int64_t row = (static_cast<int64_t>(cl) * a.S + s) * hd;
-        const int64_t srow_g = (static_cast<int64_t>(cl) * nk + ord) * hd;
-        float gsum = 0.f;
-        if (m0.last) {
-            // ---- a group of at most 32 members: its scalars stay in the lanes ----------------
-            const float cpl = __shfl_sync(kFull, m0.cp, m0.n - 1);
-            float dk = 0.f;
-            for (int sl = 0; sl < a.nsl; ++sl) {
-                const int col = sl * 128 + lane * 4;
-                const bool on = col < hd;
-                float g4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
-                if (on) {
-                    ld4cg(grad + row + col, g4);
-                    ld4(snap + srow_g + col, s4);
-                    copy4(bank + row + col, snap + srow_g + col);
-                }
-                gsum += allsum(dot4(g4, s4));
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                dk += window_terms(m0, dva_chunk + col, hd, on, s4, acc, lane);
-                if (on) {
-                    float o[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = fmaf(g4[i], cpl, acc[i]);
-                    st4(grad + row + col, o);
-                }
-            }
-            if (m0.ok) {
-                a.d_k_eff[m0.o] = -m0.beta * dk;
-                a.grad_g[m0.o] = m0.cp * gsum;
-            }
-        } else {
-            // ---- a long group: slices outside, windows inside; dot sums kept in d_k_eff --------
-            for (int sl = 0; sl < a.nsl; ++sl) {
-                const int col = sl * 128 + lane * 4;
-                const bool on = col < hd;
-                float g4[4] = {0.f, 0.f, 0.f, 0.f}, s4[4] = {0.f, 0.f, 0.f, 0.f};
-                if (on) {
-                    ld4cg(grad + row + col, g4);
-                    ld4(snap + srow_g + col, s4);
-                    copy4(bank + row + col, snap + srow_g + col);
-                }
-                gsum += allsum(dot4(g4, s4));
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                float cpl = 1.f;
-                for (int q = f;; q += 32) {
-                    const Member m = member_window<ValT>(a, srow, q, c, lane);
-                    const float r = window_terms(m, dva_chunk + col, hd, on, s4, acc, lane);
-                    if (m.ok) a.d_k_eff[m.o] = (sl == 0 ? 0.f : a.d_k_eff[m.o]) + r;
-                    if (m.last) {
-                        cpl = __shfl_sync(kFull, m.cp, m.n - 1);
-                        break;
+    float dk = 0.f, gs = 0.f;   // this lane's entry: its <dva, snap> and <gdw, snap> sums over the slices
+    if (cend >= f0) {
+        for (int sl = 0; sl < a.nsl; ++sl) {
+            const int col = sl * 128 + lane * 4;
+            const bool on = col < hd;
+            // position k's rows go to ring slot (k - f0) % kPaRing: its token row, and for a group's
+            // FIRST the group's grad and snapshot rows; one commit group per position
+            auto issue = [&](int k) {
+                if (k <= cend) {   // warp-uniform
+                    const int ks = (k - f0) % kPaRing;
+                    const int tk = __shfl_sync(kFull, t, k);
+                    const int32_t sk = __shfl_sync(kFull, slot, k);
+                    if (((okmask >> k) & 1u) && on)
+                        cp_async(&ring.dva[ks][lane], dva_chunk + static_cast<int64_t>(tk) * hd + col, 16);
+                    if (((fmask >> k) & 1u) && on && sk >= 0 && static_cast<int64_t>(sk) < a.S) {
+                        const int g = ord0 + __popc(fmask & ((1u << k) - 1u));
+                        cp_async(&ring.grad[ks][lane][0], grad + (static_cast<int64_t>(cl) * a.S + sk) * hd + col,
+                                 static_cast<int>(4 * sizeof(GradT)));
+                        cp_async(&ring.snap[ks][lane][0], snap + (static_cast<int64_t>(cl) * nk + g) * hd + col,
+                                 static_cast<int>(4 * sizeof(BankT)));
                     }
                 }
-                if (on) {
-                    float o[4];
+                cp_commit();
+            };
+#pragma unroll 1
+            for (int k = f0; k < f0 + kPaRing - 1; ++k) issue(k);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, cg[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
+            int64_t crow = 0;
+            bool cbad = true;
+#pragma unroll 1
+            for (int k = f0; k <= cend; ++k) {
+                issue(k + kPaRing - 1);
+                cp_wait<kPaRing - 1>();   // position k's copies have landed
+                const int ks = (k - f0) % kPaRing;
+                if ((fmask >> k) & 1u) {    // a group starts: its rows become current
+                    const int32_t sk = __shfl_sync(kFull, slot, k);
+                    cbad = sk < 0 || static_cast<int64_t>(sk) >= a.S;
+                    crow = (static_cast<int64_t>(cl) * a.S + (cbad ? 0 : sk)) * hd + col;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = fmaf(g4[i], cpl, acc[i]);
-                    st4(grad + row + col, o);
+                    for (int i = 0; i < 4; ++i) {
+                        cg[i] = 0.f;
+                        cs[i] = 0.f;
+                        acc[i] = 0.f;
+                    }
+                    if (!cbad) {
+                        if (on) {
+                            get4(&ring.grad[ks][lane][0], cg);
+                            get4(&ring.snap[ks][lane][0], cs);
+                            copy_raw4(bank + crow, &ring.snap[ks][lane][0]);
+                        }
+                        const float gsum = allsum(dot4(cg, cs));
+                        if (myf == k) gs += gsum;
+                    } else {
+                        bad = 1u;
+                    }
+                }
+                const float skk = __shfl_sync(kFull, sc, k);
+                if (!cbad && ((okmask >> k) & 1u)) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (on) get4(reinterpret_cast<const float*>(&ring.dva[ks][lane]), d);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(skk, d[i], acc[i]);
+                    const float r = allsum(dot4(d, cs));
+                    if (lane == k) dk += r;
+                }
+                if ((lmask >> k) & 1u) {    // the group ends: its grad row
+                    const float cpl = __shfl_sync(kFull, cp, k);
+                    if (!cbad && on) {
+                        float ov[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) ov[i] = fmaf(cg[i], cpl, acc[i]);
+                        st4(grad + crow, ov);
+                    }
                 }
             }
-            for (int q = f;; q += 32) {
-                const Member m = member_window<ValT>(a, srow, q, c, lane);
-                if (m.ok) {
-                    a.d_k_eff[m.o] = -m.beta * a.d_k_eff[m.o];
-                    a.grad_g[m.o] = m.cp * gsum;
-                }
-                if (m.last) break;
-            }
+            cp_wait<0>();
+        }
+        if (mine) {
+            a.d_k_eff[o] = mybad ? 0.f : -be * dk;
+            a.grad_g[o] = mybad ? 0.f : cp * gs;
         }
     }
+    if (open) open_group<GradT, BankT, ValT>(a, srow, c, cl, q0 + flast, ord0 + __popc(fmask) - 1, lane, &bad);
     if (bad && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
 
 template <typename GradT, typename BankT, typename ValT>
 cudaError_t launch_t(const PAArgs& a, cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>(a.P) * static_cast<unsigned>(a.tiles);
-    pa_kernel<GradT, BankT, ValT><<<blocks, kPaThreads, 0, stream>>>(a);
+    constexpr size_t smem = pa_smem_bytes<GradT, BankT>();
+    cudaError_t e = cudaFuncSetAttribute(pa_kernel<GradT, BankT, ValT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    pa_kernel<GradT, BankT, ValT><<<blocks, kPaThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
