@@ -10,19 +10,22 @@
 //   bank[s] = snap                                    (raw copy of the pre-write row)
 //   grad_g[e] = cpe_e * <gdw, snap>,  d_k_eff[e] = -beta[tok_e] * <d_dva[tok_e], snap>.
 // Every dot is summed the same way whatever the tiling: a lane sums its 4 columns of a 128-column
-// slice in column order (an fmaf chain), the 32 lane partials meet in an xor butterfly (levels 16,
-// 8, 4, 2, 1; both partners add the same pair, so every lane holds the same bits), and the slices'
-// sums add in slice order from 0.
+// slice in column order (an fmaf chain), the 32 lane partials meet in one fixed tree (pairs of lanes
+// l, l ^ h for h = 1, 2, 4, 8, 16; both partners of a pair add the same two values, so the sum does
+// not depend on which lane computes it), and the slices' sums add in slice order from 0.
 //
 // GB300 design: one launch per step; a CTA of 8 warps takes one chunk and a tile of 256 sorted
-// positions, a warp the groups whose FIRST lies in its 32 positions (a group may run past the tile:
-// the warp follows it to its LAST). The dense ordinal of a group (its snapshot row) is the count of
-// valid FIRST flags before it in the sorted row: each CTA counts the positions before its tile once.
-// Rows move as a lane's 4 columns (16 bytes f32 / 8 bytes bf16, 512 / 256 contiguous bytes per warp
-// access); the token rows of 8 members are in flight before their FMAs. A group of more than 32
-// members (a hot slot) takes its slices one after the other and keeps each member's dot sum in the
-// d_k_eff output between slices (the member's own lane stores and re-reads it), so its arithmetic
-// is that of a short group.
+// positions, a warp its 32 positions. All 32 lanes load their entries' scalars (slot, k, log_k, cpe,
+// beta) at once. The dense ordinal of a group (its snapshot row) is the count of valid FIRST flags
+// before it in the sorted row: each CTA counts the positions before its tile once. The rows of the
+// groups that start and end in the warp's positions (nearly all of them) stream through a per-warp
+// shared-memory ring: every lane cp.async-copies its own 4 columns of a position's token row and, at
+// a group's FIRST, of the group's grad and snapshot rows, 8 positions ahead, and reads back only what
+// it copied. Per aligned block of 8 positions the 16 dot partials (8 entry dots, 8 group dots) are
+// reduced across the lanes together, transposed (16 shuffles for 16 sums), each landing in the lane
+// of its position. A group that starts in the warp's positions and runs past them (a hot slot) is
+// walked afterwards in windows of 32 members; it keeps each member's dot sum in d_k_eff between
+// slices (the member's own lane stores and re-reads it), with the same arithmetic.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -112,9 +115,39 @@ __device__ __forceinline__ void copy_raw4(__nv_bfloat16* d, const __nv_bfloat16*
 __device__ __forceinline__ float dot4(const float (&x)[4], const float (&y)[4]) {
     return fmaf(x[3], y[3], fmaf(x[2], y[2], fmaf(x[1], y[1], x[0] * y[0])));
 }
+// The sum of x over the 32 lanes, in every lane: an xor butterfly of levels 1, 2, 4, 8, 16 (both
+// partners add the same pair, so every lane holds the same bits).
 __device__ __forceinline__ float allsum(float x) {
 #pragma unroll
-    for (int k = 16; k >= 1; k >>= 1) x += __shfl_xor_sync(kFull, x, k);
+    for (int k = 1; k <= 16; k <<= 1) x += __shfl_xor_sync(kFull, x, k);
+    return x;
+}
+
+// 16 values per lane, each summed over the 32 lanes by the same tree as allsum (levels 1, 2, 4, 8,
+// 16; a level-h node adds the values of lanes l and l ^ h), transposed: at level h a lane keeps the
+// values whose index bit matches its lane bit and adds its partner's copy, so each level halves the
+// values. Lane l returns the sum of value (l & 15): 16 shuffles for 16 sums instead of 80.
+__device__ __forceinline__ float tsum16(const float (&v)[16], int lane) {
+    float a[8], b[4], c[2];
+    const bool h1 = lane & 1, h2 = lane & 2, h4 = lane & 4, h8 = lane & 8;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {   // a[m]: index 2m + (lane & 1)
+        const float keep = h1 ? v[2 * m + 1] : v[2 * m], send = h1 ? v[2 * m] : v[2 * m + 1];
+        a[m] = keep + __shfl_xor_sync(kFull, send, 1);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {   // b[m]: index 4m + (lane & 3)
+        const float keep = h2 ? a[2 * m + 1] : a[2 * m], send = h2 ? a[2 * m] : a[2 * m + 1];
+        b[m] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {   // c[m]: index 8m + (lane & 7)
+        const float keep = h4 ? b[2 * m + 1] : b[2 * m], send = h4 ? b[2 * m] : b[2 * m + 1];
+        c[m] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+    const float keep = h8 ? c[1] : c[0], send = h8 ? c[0] : c[1];
+    float x = keep + __shfl_xor_sync(kFull, send, 8);   // index lane & 15
+    x += __shfl_xor_sync(kFull, x, 16);
     return x;
 }
 __device__ __forceinline__ bool valid_first(uint32_t v) { return (v & kFirst) != 0 && (v & kInvalidBit) == 0; }
@@ -397,52 +430,80 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, cg[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
             int64_t crow = 0;
             bool cbad = true;
+            float gfirst = 0.f;   // a FIRST lane: its group's <gdw, snap> over this slice
+            // positions in aligned blocks of 8: the block's dot partials are reduced across the lanes
+            // together (transposed), position k's sum landing in lane k
 #pragma unroll 1
-            for (int k = f0; k <= cend; ++k) {
-                issue(k + kPaRing - 1);
-                cp_wait<kPaRing - 1>();   // position k's copies have landed
-                const int ks = (k - f0) % kPaRing;
-                if ((fmask >> k) & 1u) {    // a group starts: its rows become current
-                    const int32_t sk = __shfl_sync(kFull, slot, k);
-                    cbad = sk < 0 || static_cast<int64_t>(sk) >= a.S;
-                    crow = (static_cast<int64_t>(cl) * a.S + (cbad ? 0 : sk)) * hd + col;
+            for (int blk = f0 >> 3; blk <= (cend >> 3); ++blk) {
+                float dp[8], gp[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        cg[i] = 0.f;
-                        cs[i] = 0.f;
-                        acc[i] = 0.f;
-                    }
-                    if (!cbad) {
-                        if (on) {
-                            get4(&ring.grad[ks][lane][0], cg);
-                            get4(&ring.snap[ks][lane][0], cs);
-                            copy_raw4(bank + crow, &ring.snap[ks][lane][0]);
+                for (int i = 0; i < 8; ++i) {
+                    dp[i] = 0.f;
+                    gp[i] = 0.f;
+                    const int k = blk * 8 + i;
+                    if (k < f0 || k > cend) continue;   // warp-uniform
+                    issue(k + kPaRing - 1);
+                    cp_wait<kPaRing - 1>();   // position k's copies have landed
+                    const int ks = (k - f0) % kPaRing;
+                    if ((fmask >> k) & 1u) {    // a group starts: its rows become current
+                        const int32_t sk = __shfl_sync(kFull, slot, k);
+                        cbad = sk < 0 || static_cast<int64_t>(sk) >= a.S;
+                        crow = (static_cast<int64_t>(cl) * a.S + (cbad ? 0 : sk)) * hd + col;
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            cg[x] = 0.f;
+                            cs[x] = 0.f;
+                            acc[x] = 0.f;
                         }
-                        const float gsum = allsum(dot4(cg, cs));
-                        if (myf == k) gs += gsum;
-                    } else {
-                        bad = 1u;
+                        if (!cbad) {
+                            if (on) {
+                                get4(&ring.grad[ks][lane][0], cg);
+                                get4(&ring.snap[ks][lane][0], cs);
+                                copy_raw4(bank + crow, &ring.snap[ks][lane][0]);
+                            }
+                            gp[i] = dot4(cg, cs);
+                        } else {
+                            bad = 1u;
+                        }
+                    }
+                    const float skk = __shfl_sync(kFull, sc, k);
+                    if (!cbad && ((okmask >> k) & 1u)) {
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
+                        if (on) get4(reinterpret_cast<const float*>(&ring.dva[ks][lane]), d);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) acc[x] = fmaf(skk, d[x], acc[x]);
+                        dp[i] = dot4(d, cs);
+                    }
+                    if ((lmask >> k) & 1u) {    // the group ends: its grad row
+                        const float cpl = __shfl_sync(kFull, cp, k);
+                        if (!cbad && on) {
+                            float ov[4];
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) ov[x] = fmaf(cg[x], cpl, acc[x]);
+                            st4(grad + crow, ov);
+                        }
                     }
                 }
-                const float skk = __shfl_sync(kFull, sc, k);
-                if (!cbad && ((okmask >> k) & 1u)) {
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (on) get4(reinterpret_cast<const float*>(&ring.dva[ks][lane]), d);
+                // index (lane & 15) of the 16 values ends in lane `lane`: the block's entry dots sit at
+                // i + 8 * (blk & 1) so that position 8 * blk + i is lane-aligned, the group dots at the other half
+                const bool odd = (blk & 1) != 0;
+                float vals[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(skk, d[i], acc[i]);
-                    const float r = allsum(dot4(d, cs));
-                    if (lane == k) dk += r;
+                for (int i = 0; i < 8; ++i) {
+                    vals[i] = odd ? gp[i] : dp[i];
+                    vals[i + 8] = odd ? dp[i] : gp[i];
                 }
-                if ((lmask >> k) & 1u) {    // the group ends: its grad row
-                    const float cpl = __shfl_sync(kFull, cp, k);
-                    if (!cbad && on) {
-                        float ov[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) ov[i] = fmaf(cg[i], cpl, acc[i]);
-                        st4(grad + crow, ov);
-                    }
+                const float red = tsum16(vals, lane);
+                const float gred = __shfl_xor_sync(kFull, red, 8);
+                const bool inblk = (lane >> 3) == blk && lane >= f0 && lane <= cend;
+                if (inblk) {
+                    dk += red;
+                    if ((fmask >> lane) & 1u) gfirst = gred;
                 }
             }
+            // every member adds its group's <gdw, snap> (from the group's FIRST lane)
+            const float g_of_mine = __shfl_sync(kFull, gfirst, myf < 0 ? 0 : myf);
+            if (myf >= 0) gs += g_of_mine;
             cp_wait<0>();
         }
         if (mine) {
