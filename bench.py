@@ -40,6 +40,10 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "large:dw:c28e9f58496b": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
     "large:phase1:6922acd872e5": 55624960 + 718927616,
+    # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
+    # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
+    "large:pa:38b81c18d626": round((106329344 + 43213568) * 4186081 / 4161534),
+    "large:pa_bf16grad:38b81c18d626": round((73005824 + 15511552) * 4186081 / 4161534),
 }
 
 

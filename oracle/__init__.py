@@ -1,13 +1,16 @@
-"""Float64 CPU oracle of the sparse-delta-memory forward hot path (Phase 1 + DW).
+"""Float64 CPU oracle of the sparse-delta-memory forward hot path (Phase 1 + DW), the saving
+forward's snapshot order and the backward's Phase A.
 
 TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's
 CPU-baseline leg may import this package. It shares no code with the CUDA path and never
-imports it. The arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight loops); this
-module builds it with the host C compiler on first use and marshals numpy arrays.
+imports it. The forward's arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight
+loops); this module builds it with the host C compiler on first use and marshals numpy arrays.
+``snapshot_slots`` and ``pa_chunk`` (Phase A) are plain numpy / Python loops here.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
 definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
-Python's ``sorted``, rex/cpe closed forms, flag invariants).
+Python's ``sorted``, rex/cpe closed forms, flag invariants; for Phase A a hand-worked chunk, the
+single-entry closed form, linearity and the cpe_last rule).
 """
 
 from __future__ import annotations
