@@ -1,16 +1,17 @@
 """Float64 CPU oracle of the sparse-delta-memory forward hot path (Phase 1 + DW), the saving
-forward's snapshot order and the backward's Phase A.
+forward's snapshot order and the backward's Phase A and GDS.
 
 TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's
 CPU-baseline leg may import this package. It shares no code with the CUDA path and never
 imports it. The forward's arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight
 loops); this module builds it with the host C compiler on first use and marshals numpy arrays.
-``snapshot_slots`` and ``pa_chunk`` (Phase A) are plain numpy / Python loops here.
+``snapshot_slots``, ``pa_chunk`` (Phase A) and ``gds_chunk`` (GDS) are plain numpy / Python loops here.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
 definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
 Python's ``sorted``, rex/cpe closed forms, flag invariants; for Phase A a hand-worked chunk, the
-single-entry closed form, linearity and the cpe_last rule).
+single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked chunk and the
+adjoint identity between the scatter and the weighted read).
 """
 
 from __future__ import annotations
@@ -249,3 +250,41 @@ def pa_chunk(grad, bank, snap_rows, k_idx_c, k_val_c, log_k_c, cpe_c, beta_c, dv
         mag[s] = np.abs(gdw * cpe) + aabs
         bank[s] = snap
     return d_k_eff, grad_g, mag, dmag_eff, dmag_g
+
+
+def gds_chunk(grad, bank, q_idx_c, q_val_c, log_q_c, gr_c, *, S, V):
+    """GDS, the read side of the backward, for one chunk (mover_da2_cuda.py, module docstring and the
+    "GDS, split by data need" comment; the read records of its qrec kernel). Float64, plain loops.
+
+    (1) dots in token order: d_q_w[t, r] = <gr[t], bank[q_idx[t, r]]> for every valid token t < V
+        (0 for padding tokens and for ids outside [0, S));
+    (2) the grad scatter: per read group (slot s with valid read entries; members in sorted order, i.e.
+        token then lane) acc = sum_m sc_m * gr[tok_m], sc = q * exp(log_q) (the read record's scale),
+        and grad[s] = grad[s] + acc, once per group.
+    Inputs: grad / bank [S, hd] float64 (grad updated in place), q_idx_c / q_val_c / log_q_c [C, R],
+    gr_c [C, hd]. Returns (d_q_w [C, R], mag [S, hd], dmag [C, R]): mag = |grad before| + sum |sc * gr|
+    of each updated row (zero elsewhere), dmag = sum |products| of each dot (tolerance bookkeeping).
+    """
+    C, R = q_idx_c.shape
+    ids = np.asarray(q_idx_c, np.int64)
+    d_q_w = np.zeros((C, R))
+    dmag = np.zeros((C, R))
+    groups = {}
+    for t in range(V):
+        for r in range(R):
+            s = int(ids[t, r])
+            if 0 <= s < S:
+                d_q_w[t, r] = float(np.dot(gr_c[t], bank[s]))
+                dmag[t, r] = float(np.sum(np.abs(gr_c[t] * bank[s])))
+                groups.setdefault(s, []).append((t, r))
+    mag = np.zeros_like(grad)
+    for s in sorted(groups):
+        acc = np.zeros(grad.shape[1])
+        aabs = np.zeros(grad.shape[1])
+        for (t, r) in groups[s]:
+            sc = float(q_val_c[t, r]) * np.exp(float(log_q_c[t, r]))
+            acc += sc * gr_c[t]
+            aabs += np.abs(sc * gr_c[t])
+        mag[s] = np.abs(grad[s]) + aabs
+        grad[s] = grad[s] + acc
+    return d_q_w, mag, dmag

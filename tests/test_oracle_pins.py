@@ -545,3 +545,46 @@ def test_pa_decay_uses_last_members_cpe():
     _, g_g, *_ = oracle.pa_chunk(grad, np.zeros((2, 2)), np.array([[3.0, 4.0]]), k, np.ones((2, 1)),
                                  np.zeros((2, 1)), np.array([[0.5], [0.25]]), np.ones(2), np.zeros((2, 2)), S=2, V=2)
     assert np.array_equal(grad[0], [0.25, 0.5]) and np.array_equal(g_g[:, 0], [5.5, 2.75])
+
+
+def test_gds_hand_example():
+    """GDS on a hand-worked chunk (mover_da2_cuda.py, "GDS, split by data need"): 3 tokens, 2 read lanes,
+    V = 2 (token 2 is padding). Entries: (0,0) slot 1, (0,1) slot 3, (1,0) slot 1, (1,1) id 9 (outside S = 4).
+    gr = [[1, 2], [3, -1], [7, 7]], bank rows 1 = [2, 0], 3 = [1, 1]; q = 0.5 everywhere, log_q = 0 except
+    (1,0) with log_q = log 2 (sc = 1):
+      d_q_w = [[<[1,2],[2,0]> = 2, <[1,2],[1,1]> = 3], [<[3,-1],[2,0]> = 6, 0], [0, 0]];
+      slot 1: acc = 0.5 [1, 2] + 1 [3, -1] = [3.5, 0]; slot 3: acc = 0.5 [1, 2] = [0.5, 1]."""
+    q_idx = np.array([[1, 3], [1, 9], [2, 2]], np.int32)
+    q_val = np.full((3, 2), 0.5)
+    log_q = np.zeros((3, 2)); log_q[1, 0] = np.log(2.0)
+    gr = np.array([[1.0, 2.0], [3.0, -1.0], [7.0, 7.0]])
+    bank = np.zeros((4, 2)); bank[1] = [2, 0]; bank[3] = [1, 1]; bank[2] = [5, 5]
+    grad = np.full((4, 2), 10.0)
+    d, mag, _ = oracle.gds_chunk(grad, bank, q_idx, q_val, log_q, gr, S=4, V=2)
+    assert np.allclose(d, [[2, 3], [6, 0], [0, 0]])
+    assert np.allclose(grad, [[10, 10], [13.5, 10], [10, 10], [10.5, 11]])
+    assert np.all(mag[[0, 2]] == 0) and np.allclose(mag[1], [10 + 0.5 + 3, 10 + 1 + 1])
+
+
+def test_gds_scatter_is_the_adjoint_of_the_weighted_read():
+    """The scatter is the transpose of the read: for any rows B, sum_s <grad_after[s] - grad_before[s], B[s]>
+    equals sum over valid entries of sc * <gr[t], B[slot]>, and with B = bank that is sum sc * d_q_w. A
+    wrong slot, token, lane or scale on either side breaks it."""
+    rng = np.random.default_rng(11)
+    S, C, R, hd, V = 12, 9, 3, 6, 7
+    q_idx = rng.integers(-1, S + 1, size=(C, R)).astype(np.int32)   # some ids outside [0, S)
+    q_val, log_q = rng.standard_normal((C, R)), -rng.random((C, R))
+    gr, bank = rng.standard_normal((C, hd)), rng.standard_normal((S, hd))
+    g0 = rng.standard_normal((S, hd))
+    grad = g0.copy()
+    d, *_ = oracle.gds_chunk(grad, bank, q_idx, q_val, log_q, gr, S=S, V=V)
+    sc = q_val * np.exp(log_q)
+    valid = (q_idx >= 0) & (q_idx < S) & (np.arange(C)[:, None] < V)
+    assert np.isclose(np.sum((grad - g0) * bank), np.sum(sc[valid] * d[valid]))
+    B = rng.standard_normal((S, hd))
+    rhs = sum(sc[t, r] * np.dot(gr[t], B[q_idx[t, r]]) for t in range(C) for r in range(R) if valid[t, r])
+    assert np.isclose(np.sum((grad - g0) * B), rhs)
+    assert np.all(d[~valid] == 0.0)
+    # rows no valid entry reads are untouched
+    unread = np.setdiff1d(np.arange(S), q_idx[valid])
+    assert np.array_equal(grad[unread], g0[unread])
