@@ -550,6 +550,203 @@ def run_pa(args):
     return result
 
 
+def count_read_groups(x):
+    """Slots with at least one valid read entry, per chunk (exactly, from the data)."""
+    q = x["q_idx"].reshape(x["q_idx"].shape[0], -1).astype(np.int64)
+    total = 0
+    for c0 in range(0, q.shape[0], 256):
+        blk = np.sort(q[c0:c0 + 256], axis=1)
+        distinct = np.concatenate([np.ones((blk.shape[0], 1), bool), blk[:, 1:] != blk[:, :-1]], axis=1)
+        total += int((distinct & (blk >= 0)).sum())
+    return total
+
+
+def gds_algorithmic_bytes(w, qgroups, grad_bytes):
+    """Bytes of one GDS pass over every step (the read side of the backward): per read group its bank
+    row read (the dots) and its grad row read and written (the scatter); per read entry its sorted-row
+    word, slot id, q, log_q and d_q_w; per token its reading-gradient row (f32)."""
+    vt = 2 if w.val_dtype == "bf16" else 4
+    bt = 2 if w.bank_dtype == "bf16" else 4
+    tok = w.N * w.C
+    return qgroups * w.hd * (bt + 2 * grad_bytes) + tok * w.R * (4 + 4 + vt + 4 + 4) + tok * w.hd * 4
+
+
+def gds_cpu_baseline(w, x, gr, budget_s=12.0, max_chunks=None):
+    """The oracle's GDS as it stands (float64, single thread) on a bounded sample: the chunks of stream 0,
+    last step first, on the rows that stream reads. ``x`` / ``gr`` hold stream 0 alone."""
+    import oracle
+
+    P, C = x["P"], w.C
+    ids = x["q_idx"][0::P].ravel()
+    slots = np.unique(ids[ids >= 0])
+    rng = np.random.default_rng(6)
+    grad = rng.standard_normal((len(slots), w.hd))
+    bank = rng.standard_normal((len(slots), w.hd))
+    qvf = oracle.as_f64(x["q_val"], w.val_dtype)
+    t0 = time.perf_counter()
+    chunks = 0
+    for ti in range(w.steps - 1, -1, -1):
+        c = ti * P
+        V = w.valid_last if ti == w.steps - 1 else C
+        qq = np.searchsorted(slots, x["q_idx"][c]).astype(np.int32)
+        qq[x["q_idx"][c] < 0] = -1
+        oracle.gds_chunk(grad, bank, qq, qvf[c], -rng.random((C, w.R)), gr[c], S=len(slots), V=V)
+        chunks += 1
+        if time.perf_counter() - t0 > budget_s or (max_chunks and chunks >= max_chunks):
+            break
+    dt = time.perf_counter() - t0
+    toks = chunks * C
+    return {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks ({toks} tokens) of stream 0, last step first: GDS, float64, "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_gds(args):
+    """GDS over every step of the workload: one bench step = sdm_gds over steps [0, steps) (two launches
+    per step, last step first). sorted_q and log_q come from one untimed Phase 1 on the GPU, the reading
+    gradients from the seeded generator; grad rows are float32 (--pa-grad bf16: the bank's format)."""
+    import torch
+
+    import sparse_slot_memory_gb300 as sdm
+    from synth import make_read_grads
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sdm.build()
+    w = WORKLOADS[args.workload]
+    if args.streams:
+        w = scaled(w, P=args.streams)
+    if args.slots:
+        w = scaled(w, S=args.slots)
+    x = make_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.cuda()
+
+    d = {"k_idx": dev(x["k_idx"], "i"), "q_idx": dev(x["q_idx"], "i"), "k_val": dev(x["k_val"], w.val_dtype),
+         "q_val": dev(x["q_val"], w.val_dtype), "g": dev(x["g"], "f32"), "gr": dev(make_read_grads(w), "f32")}
+    ws = sdm.alloc_workspace(shape)
+    out = sdm.alloc_outputs(shape, fields=("log_q", "sorted_q", "repeats"))
+    sdm.phase1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], out, ws)
+    torch.cuda.synchronize()
+    assert sdm.device_status(ws) == 0
+    del ws
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3000 + w.seed + rank)
+    bdt = torch.bfloat16 if w.bank_dtype == "bf16" else torch.float32
+    bank = (torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen) * w.bank_scale).to(bdt)
+    gdt = torch.bfloat16 if args.pa_grad == "bf16" else torch.float32
+    grad = torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen).to(gdt)
+    d_q_w = torch.empty((w.N, w.C, w.R), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sdm.gds(shape, out["sorted_q"], d["q_idx"], d["q_val"], out["log_q"], d["gr"], bank, grad, d_q_w, 0, w.steps,
+                status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    assert int(status.item()) == 0
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = valid_tokens(w, w.P)
+    value = tokens * world / (ms / 1e3)
+
+    # End to end with host buffers: per pass, every per-token input H2D from pinned host memory (sorted
+    # read rows, ids, q, log_q, the reading gradients), the pass, d_q_w D2H; grad and bank rows resident.
+    e2e = None
+    if not args.no_e2e:
+        ins = {"sorted_q": out["sorted_q"], "q_idx": d["q_idx"], "q_val": d["q_val"], "log_q": out["log_q"],
+               "gr": d["gr"]}
+        pin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in ins.items()}
+        out_h = torch.empty(d_q_w.shape, dtype=d_q_w.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k, v in pin.items():
+                ins[k].copy_(v, non_blocking=True)
+            sdm.gds(shape, ins["sorted_q"], ins["q_idx"], ins["q_val"], ins["log_q"], ins["gr"], bank, grad, d_q_w, 0,
+                    w.steps, status)
+            out_h.copy_(d_q_w, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n2 = max(3, min(args.steps, 8))
+        a0 = time.perf_counter()
+        for _ in range(n2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = (time.perf_counter() - a0) * 1e3 / n2
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "per pass: every per-token input H2D from pinned host memory, the pass, d_q_w D2H; one "
+                       "stream; grad and bank rows resident; host wall clock"}
+
+    peak, peak_kind = peaks()
+    qgroups = count_read_groups(x)
+    ab = gds_algorithmic_bytes(w, qgroups, 2 if args.pa_grad == "bf16" else 4)
+    step_ms = ms / w.steps                      # one workload step: the dots and the scatter launch
+    achieved = ab / w.steps / (step_ms / 1e3) / 1e9
+    key = f"{args.workload}:gds{'_bf16grad' if args.pa_grad == 'bf16' else ''}:{src_hash('gds')}"
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            x0 = make_inputs(w, streams=[0])
+            cpu = gds_cpu_baseline(w, x0, make_read_grads(w, streams=[0]).astype(np.float64), budget_s=args.cpu_seconds)
+        result = {
+            "metric": "SDM backward GDS (read-side dots + grad scatter) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generators; sorted read rows and log_q from one Phase 1)",
+            "config": {"workload": w.name + "+gds" + ("+bf16grad" if args.pa_grad == "bf16" else ""),
+                       **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "grad": args.pa_grad, "tokens_per_step_per_gpu": tokens,
+                       "parallelism": f"replicas x{world} (independent streams)",
+                       "l2": "inputs larger than L2 (16 GiB f32 grad rows, 8 GiB bank)"},
+            "kernels_ms": {"gds_per_workload_step": step_ms}, "algorithmic_bytes": ab, "read_groups": qgroups,
+            "roofline": {"bound": "hbm", "kernel": "gds (dots + scatter launches of one step)", "achieved": achieved,
+                         "peak": peak, "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(key)},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * w.steps * args.steps,
+            "clocks": clk.summary(), "impl": "ours",
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
 def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
     """The oracle as it stands (float64, single thread) on a bounded sample: whole steps of one
     stream (Phase 1 with the pair triangles, then DW), until ~budget_s seconds have passed."""
@@ -625,12 +822,15 @@ def main():
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slots per stream (profiling runs)")
     ap.add_argument("--saving", action="store_true", help="time the saving forward (DW writes the dense snapshot)")
     ap.add_argument("--pa", action="store_true", help="time the backward's Phase A over every step instead")
-    ap.add_argument("--pa-grad", default="f32", choices=["f32", "bf16"], help="grad row format of --pa")
+    ap.add_argument("--gds", action="store_true", help="time the backward's GDS (read side) over every step instead")
+    ap.add_argument("--pa-grad", default="f32", choices=["f32", "bf16"], help="grad row format of --pa / --gds")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.pa:
         run_pa(args)
+    elif args.gds:
+        run_gds(args)
     else:
         run_ours(args)
 

@@ -264,6 +264,31 @@ sdm_status sdm_pa(const sdm_shape* shape, int32_t grad_dtype, const int32_t* sor
                   int64_t step_end, uint32_t* status, sdm_stream_t stream);
 
 /*
+ * GDS, the read side of the backward (mover_da2_cuda.py: module docstring, the "GDS, split by data
+ * need" comment, its read-records kernel), for the steps [step_begin, step_end), LAST step first
+ * (two launches per step: the dots, then the scatter). Per chunk c = ti * P + p:
+ *   d_q_w[c, t, r] = <gr[c, t], bank[p*S + q_idx[c, t, r]]> for the valid tokens t (t < valid_last
+ *                   in the last step's chunks, else t < C); 0 for padding tokens;
+ *   per read group (slot s with valid read entries; members m in sorted order as sorted_q lists them)
+ *   acc = 0; acc = fmaf(sc_m, gr[c, tok_m], acc), sc = f32(q_m) * expf(log_q_m);
+ *   grad[p*S + s] = RN(grad[p*S + s] + acc)          (one rounding per element; f32 grad: the sum)
+ * Dots are f32 like sdm_pa's (per-lane fmaf chain over 4 columns, a fixed lane tree, slices in
+ * order), so results do not depend on the launch geometry; every grad row has one writer per launch.
+ * Arguments (device pointers, 16-byte aligned, caller-owned; N = steps * P):
+ *   grad_dtype: sdm_dtype of grad (SDM_F32, or SDM_BF16 for grad rows in the bank's format).
+ *   sorted_q [N, C*R] int32: as sdm_phase1 writes it. log_q f32 [N, C, R]: sdm_phase1's output.
+ *   q_idx int32 / q_val val_dtype [N, C, R]: the forward's inputs. gr f32 [N, C, hd]: the gradient of
+ *   the read results. bank [P*S, hd] bank_dtype: read only. grad [P*S, hd] grad_dtype: updated in
+ *   place (must not alias bank). d_q_w [N, C, R] f32: written for every read entry of the range.
+ *   status (nullable): device word OR-ed with SDM_DEV_BAD_SLOT when a valid token's read id lies
+ *   outside [0, S) (its dot is 0 and it adds nothing).
+ * Errors: as sdm_pa.
+ */
+sdm_status sdm_gds(const sdm_shape* shape, int32_t grad_dtype, const int32_t* sorted_q, const int32_t* q_idx,
+                   const void* q_val, const float* log_q, const float* gr, const void* bank, void* grad, float* d_q_w,
+                   int64_t step_begin, int64_t step_end, uint32_t* status, sdm_stream_t stream);
+
+/*
  * Synchronizes `stream`, reads the workspace's device status word into *code_out (0 = fine,
  * else SDM_DEV_* bits) and, if `clear`, zeroes it. Returns SDM_ERR_DEVICE when the word is
  * nonzero, SDM_ERR_CUDA when the copy fails.

@@ -19,6 +19,7 @@ from .api import (  # noqa: F401
     forward_chunks,
     forward_chunks_saving,
     forward_chunks_noalloc,
+    gds,
     pa,
     phase1,
     phase1_saving,

@@ -211,6 +211,21 @@ def pa(shape: ShapeSpec, sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, ba
     _check(st, "sdm_pa")
 
 
+def gds(shape: ShapeSpec, sorted_q, q_idx, q_val, log_q, gr, bank, grad, d_q_w, step_begin=0, step_end=None,
+        status=None, stream=None):
+    """sdm_gds: the read side of the backward for steps [step_begin, step_end), last step first.
+    ``grad`` is float32 or bfloat16 (its dtype is passed as grad_dtype); ``status`` (optional) is a CUDA
+    int32 tensor of one element to which SDM_DEV_* bits are OR-ed."""
+    step_end = shape.steps if step_end is None else step_end
+    gdt = {torch.float32: _abi.SDM_F32, torch.bfloat16: _abi.SDM_BF16}.get(grad.dtype)
+    if gdt is None:
+        raise TypeError("grad must be float32 or bfloat16")
+    st = _abi.load().sdm_gds(ctypes.byref(shape.c()), gdt, _ptr(sorted_q), _ptr(q_idx), _ptr(q_val), _ptr(log_q),
+                             _ptr(gr), _ptr(bank), _ptr(grad), _ptr(d_q_w), step_begin, step_end, _ptr(status),
+                             _stream(stream))
+    _check(st, "sdm_gds")
+
+
 def device_status(ws, clear: bool = True, stream=None) -> int:
     code = _abi.c_i32(0)
     st = _abi.load().sdm_device_status(_ptr(ws), ctypes.byref(code), int(clear), _stream(stream))

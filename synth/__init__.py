@@ -1,5 +1,5 @@
 """Seeded synthetic inputs for the sparse-delta-memory forward (Phase 1 + decay-and-write) and
-the backward's Phase A.
+the backward's Phase A and GDS.
 
 This package is shared by the tests, the benchmark and the oracle's callers. It only draws
 random numbers and lays them out; it holds none of the method's arithmetic.
@@ -15,5 +15,6 @@ from .workloads import (  # noqa: F401
     make_grad_stream,
     make_snapshot_chunk,
     make_inputs,
+    make_read_grads,
     scaled,
 )

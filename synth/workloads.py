@@ -209,3 +209,15 @@ def make_snapshot_chunk(w: Workload, c: int) -> np.ndarray:
     rng = np.random.default_rng(np.random.SeedSequence([w.seed, c, 17]))
     x = (rng.standard_normal((w.C * w.W, w.hd), dtype=np.float32) * np.float32(w.bank_scale)).astype(np.float32)
     return f32_to_bf16_bits(x) if w.bank_dtype == "bf16" else x
+
+
+def make_read_grads(w: Workload, streams=None) -> np.ndarray:
+    """gr [N, C, hd] float32: the gradient of every token's read result (GDS, the read side of the
+    backward), normal with scale 1, chunk-major like make_inputs."""
+    streams = list(range(w.P)) if streams is None else list(streams)
+    Ps, st, C, hd = len(streams), w.steps, w.C, w.hd
+    gr = np.empty((st, Ps, C, hd), np.float32)
+    for i, p in enumerate(streams):
+        rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 19]))
+        gr[:, i] = rng.standard_normal((st, C, hd), dtype=np.float32)
+    return gr.reshape(st * Ps, C, hd)
