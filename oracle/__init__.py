@@ -1,17 +1,19 @@
 """Float64 CPU oracle of the sparse-delta-memory forward hot path (Phase 1 + DW), the saving
-forward's snapshot order and the backward's Phase A and GDS.
+forward's snapshot order and the backward's Phase A, GWR and GDS.
 
 TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's
 CPU-baseline leg may import this package. It shares no code with the CUDA path and never
 imports it. The forward's arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight
 loops); this module builds it with the host C compiler on first use and marshals numpy arrays.
-``snapshot_slots``, ``pa_chunk`` (Phase A) and ``gds_chunk`` (GDS) are plain numpy / Python loops here.
+``snapshot_slots``, ``pa_chunk`` (Phase A), ``gwr_chunk`` (GWR) and ``gds_chunk`` (GDS) are plain numpy /
+Python loops here.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
 definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
 Python's ``sorted``, rex/cpe closed forms, flag invariants; for Phase A a hand-worked chunk, the
 single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked chunk and the
-adjoint identity between the scatter and the weighted read).
+adjoint identity between the scatter and the weighted read; for GWR a hand-worked chunk and a
+dense gather matrix applied by a library matmul).
 """
 
 from __future__ import annotations
@@ -288,3 +290,30 @@ def gds_chunk(grad, bank, q_idx_c, q_val_c, log_q_c, gr_c, *, S, V):
         mag[s] = np.abs(grad[s]) + aabs
         grad[s] = grad[s] + acc
     return d_q_w, mag, dmag
+
+
+def gwr_chunk(grad, k_idx_c, write_w_c, dv_c, *, S, V):
+    """GWR, the write side's token gather of the backward, for one chunk (pa_dc_cuda.py, module
+    docstring: "GWR"). Float64, plain loops over tokens and their write lanes in order.
+
+    For every valid token t < V: d_delta_v[t] = sum over lanes n of write_w[t, n] * grad[k_idx[t, n]]
+    and d_k_pd[t, n] = <dv[t], grad[k_idx[t, n]]> (ids outside [0, S) add nothing and get 0); padding
+    tokens get zeros. Inputs: grad [S, hd] (read only), k_idx_c / write_w_c [C, W], dv_c [C, hd].
+    Returns (d_delta_v [C, hd], d_k_pd [C, W], mag [C, hd], dmag [C, W]): mag = sum |w * grad row| per
+    token, dmag = sum |products| per dot (tolerance bookkeeping).
+    """
+    C, W = k_idx_c.shape
+    hd = grad.shape[1]
+    d_delta_v = np.zeros((C, hd))
+    mag = np.zeros((C, hd))
+    d_k_pd = np.zeros((C, W))
+    dmag = np.zeros((C, W))
+    for t in range(V):
+        for n in range(W):
+            s = int(k_idx_c[t, n])
+            if 0 <= s < S:
+                d_delta_v[t] += float(write_w_c[t, n]) * grad[s]
+                mag[t] += np.abs(float(write_w_c[t, n]) * grad[s])
+                d_k_pd[t, n] = float(np.dot(dv_c[t], grad[s]))
+                dmag[t, n] = float(np.sum(np.abs(dv_c[t] * grad[s])))
+    return d_delta_v, d_k_pd, mag, dmag

@@ -588,3 +588,37 @@ def test_gds_scatter_is_the_adjoint_of_the_weighted_read():
     # rows no valid entry reads are untouched
     unread = np.setdiff1d(np.arange(S), q_idx[valid])
     assert np.array_equal(grad[unread], g0[unread])
+
+
+def test_gwr_hand_example():
+    """GWR on a hand-worked chunk (pa_dc_cuda.py module docstring, "GWR"): 3 tokens, 2 write lanes, V = 2.
+    grad rows 0 = [1, 0], 2 = [0, 2], 3 = [1, 1]; k_idx = [[0, 2], [3, 7 (outside S = 4)], [2, 2]];
+    w = [[2, 3], [-1, 5], [9, 9]]; dv = [[1, 1], [2, -1], [4, 4]]:
+      d_delta_v[0] = 2 [1, 0] + 3 [0, 2] = [2, 6]; d_delta_v[1] = -1 [1, 1] = [-1, -1]; token 2: 0;
+      d_k_pd = [[<[1,1],[1,0]> = 1, <[1,1],[0,2]> = 2], [<[2,-1],[1,1]> = 1, 0], [0, 0]]."""
+    grad = np.zeros((4, 2)); grad[0] = [1, 0]; grad[2] = [0, 2]; grad[3] = [1, 1]; grad[1] = [7, 7]
+    k_idx = np.array([[0, 2], [3, 7], [2, 2]], np.int32)
+    w = np.array([[2.0, 3.0], [-1.0, 5.0], [9.0, 9.0]])
+    dv = np.array([[1.0, 1.0], [2.0, -1.0], [4.0, 4.0]])
+    dd, pd, *_ = oracle.gwr_chunk(grad, k_idx, w, dv, S=4, V=2)
+    assert np.allclose(dd, [[2, 6], [-1, -1], [0, 0]])
+    assert np.allclose(pd, [[1, 2], [1, 0], [0, 0]])
+
+
+def test_gwr_matches_a_dense_gather_matrix():
+    """d_delta_v = M @ grad with M[t, s] = sum of w[t, n] over the valid lanes n with k_idx[t, n] = s (a
+    library matmul), and sum_t <d_delta_v[t], dv[t]> = sum of w * d_k_pd (the two outputs agree)."""
+    rng = np.random.default_rng(12)
+    S, C, W, hd, V = 10, 8, 4, 5, 6
+    k_idx = rng.integers(-1, S + 2, size=(C, W)).astype(np.int32)
+    w, dv, grad = rng.standard_normal((C, W)), rng.standard_normal((C, hd)), rng.standard_normal((S, hd))
+    dd, pd, *_ = oracle.gwr_chunk(grad, k_idx, w, dv, S=S, V=V)
+    M = np.zeros((C, S))
+    for t in range(V):
+        for n in range(W):
+            if 0 <= k_idx[t, n] < S:
+                M[t, k_idx[t, n]] += w[t, n]
+    assert np.allclose(dd, M @ grad)
+    assert np.isclose(np.sum(dd * dv), np.sum(w * pd))
+    valid = (k_idx >= 0) & (k_idx < S) & (np.arange(C)[:, None] < V)
+    assert np.all(pd[~valid] == 0.0)
