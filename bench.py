@@ -747,6 +747,174 @@ def run_gds(args):
     return result
 
 
+def gwr_algorithmic_bytes(w, grad_bytes):
+    """Bytes of one GWR pass over every step: per write entry its grad row read, slot id, weight and
+    d_k_pd; per token its dv row read and its d_delta_v row (f32) written."""
+    dvt = 2 if w.dv_dtype == "bf16" else 4
+    tok = w.N * w.C
+    return tok * w.W * (w.hd * grad_bytes + 4 + 4 + 4) + tok * w.hd * (dvt + 4)
+
+
+def gwr_cpu_baseline(w, x, ww, budget_s=12.0, max_chunks=None):
+    """The oracle's GWR as it stands (float64, single thread) on a bounded sample: the chunks of stream
+    0 on the rows that stream writes. ``x`` / ``ww`` hold stream 0 alone."""
+    import oracle
+
+    C = w.C
+    ids = x["k_idx"].ravel()
+    slots = np.unique(ids[ids >= 0])
+    grad = np.random.default_rng(7).standard_normal((len(slots), w.hd))
+    dvf = oracle.as_f64(x["dv"], w.dv_dtype)
+    t0 = time.perf_counter()
+    chunks = 0
+    for ti in range(w.steps - 1, -1, -1):
+        V = w.valid_last if ti == w.steps - 1 else C
+        kk = np.searchsorted(slots, x["k_idx"][ti]).astype(np.int32)
+        kk[x["k_idx"][ti] < 0] = -1
+        oracle.gwr_chunk(grad, kk, ww[ti].astype(np.float64), dvf[ti * C:(ti + 1) * C], S=len(slots), V=V)
+        chunks += 1
+        if time.perf_counter() - t0 > budget_s or (max_chunks and chunks >= max_chunks):
+            break
+    dt = time.perf_counter() - t0
+    toks = chunks * C
+    return {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks ({toks} tokens) of stream 0: GWR, float64, {dt:.1f} s single-threaded"}
+
+
+def run_gwr(args):
+    """GWR over every step of the workload: one bench step = sdm_gwr over steps [0, steps) (one launch per
+    step). Ids and token rows are the workload's, write weights from the seeded generator, grad rows
+    float32 (--pa-grad bf16: the bank's format)."""
+    import torch
+
+    import sparse_slot_memory_gb300 as sdm
+    from synth import make_write_weights
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sdm.build()
+    w = WORKLOADS[args.workload]
+    if args.streams:
+        w = scaled(w, P=args.streams)
+    if args.slots:
+        w = scaled(w, S=args.slots)
+    x = make_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.cuda()
+
+    d = {"k_idx": dev(x["k_idx"], "i"), "write_w": dev(make_write_weights(w), "f32"), "dv": dev(x["dv"], w.dv_dtype)}
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4000 + w.seed + rank)
+    gdt = torch.bfloat16 if args.pa_grad == "bf16" else torch.float32
+    grad = torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen).to(gdt)
+    d_dd = torch.empty((w.N, w.C, w.hd), device="cuda")
+    d_pd = torch.empty((w.N, w.C, w.W), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sdm.gwr(shape, d["k_idx"], d["write_w"], d["dv"], grad, d_dd, d_pd, 0, w.steps, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = valid_tokens(w, w.P)
+    value = tokens * world / (ms / 1e3)
+
+    # End to end with host buffers: per pass the ids, weights and token rows H2D from pinned memory, the
+    # pass, both outputs D2H; grad rows resident.
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in d.items()}
+        outs = {"d_delta_v": d_dd, "d_k_pd": d_pd}
+        outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+        def e2e_step():
+            for k, v in pin.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            for k, v in outs.items():
+                outs_h[k].copy_(v, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n2 = max(3, min(args.steps, 8))
+        a0 = time.perf_counter()
+        for _ in range(n2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = (time.perf_counter() - a0) * 1e3 / n2
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "per pass: ids, weights and token rows H2D from pinned host memory, the pass, both outputs "
+                       "D2H; one stream; grad rows resident; host wall clock"}
+
+    peak, peak_kind = peaks()
+    ab = gwr_algorithmic_bytes(w, 2 if args.pa_grad == "bf16" else 4)
+    kern_ms = ms / w.steps
+    achieved = ab / w.steps / (kern_ms / 1e3) / 1e9
+    key = f"{args.workload}:gwr{'_bf16grad' if args.pa_grad == 'bf16' else ''}:{src_hash('gwr')}"
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            cpu = gwr_cpu_baseline(w, make_inputs(w, streams=[0]), make_write_weights(w, streams=[0]),
+                                   budget_s=args.cpu_seconds)
+        result = {
+            "metric": "SDM backward GWR (write-side token gather) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generators)",
+            "config": {"workload": w.name + "+gwr" + ("+bf16grad" if args.pa_grad == "bf16" else ""),
+                       **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "grad": args.pa_grad, "tokens_per_step_per_gpu": tokens,
+                       "parallelism": f"replicas x{world} (independent streams)",
+                       "l2": "inputs larger than L2 (16 GiB f32 grad rows)"},
+            "kernels_ms": {"gwr_per_launch": kern_ms}, "algorithmic_bytes": ab,
+            "roofline": {"bound": "hbm", "kernel": "gwr", "achieved": achieved, "peak": peak,
+                         "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": NCU_TRAFFIC.get(key)},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": w.steps * args.steps,
+            "clocks": clk.summary(), "impl": "ours",
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
 def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
     """The oracle as it stands (float64, single thread) on a bounded sample: whole steps of one
     stream (Phase 1 with the pair triangles, then DW), until ~budget_s seconds have passed."""
@@ -823,6 +991,7 @@ def main():
     ap.add_argument("--saving", action="store_true", help="time the saving forward (DW writes the dense snapshot)")
     ap.add_argument("--pa", action="store_true", help="time the backward's Phase A over every step instead")
     ap.add_argument("--gds", action="store_true", help="time the backward's GDS (read side) over every step instead")
+    ap.add_argument("--gwr", action="store_true", help="time the backward's GWR (write-side gather) over every step")
     ap.add_argument("--pa-grad", default="f32", choices=["f32", "bf16"], help="grad row format of --pa / --gds")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -831,6 +1000,8 @@ def main():
         run_pa(args)
     elif args.gds:
         run_gds(args)
+    elif args.gwr:
+        run_gwr(args)
     else:
         run_ours(args)
 

@@ -264,6 +264,26 @@ sdm_status sdm_pa(const sdm_shape* shape, int32_t grad_dtype, const int32_t* sor
                   int64_t step_end, uint32_t* status, sdm_stream_t stream);
 
 /*
+ * GWR, the token gather of the write side of the backward (pa_dc_cuda.py: module docstring, "GWR",
+ * and its GWR kernel), for the steps [step_begin, step_end), LAST step first (one launch per step).
+ * Per chunk c = ti * P + p and valid token t (t < valid_last in the last step's chunks, else t < C):
+ *   d_delta_v[c, t] = acc, acc = 0; acc = fmaf(write_w[c, t, n], grad[p*S + k_idx[c, t, n]], acc)
+ *                     over the write lanes n = 0 .. W-1 in order;
+ *   d_k_pd[c, t, n] = <dv[c*C + t], grad[p*S + k_idx[c, t, n]]>  (f32 dots as sdm_pa's);
+ * padding tokens get zero rows and zero dots.
+ * Arguments (device pointers, 16-byte aligned, caller-owned; N = steps * P):
+ *   grad_dtype: sdm_dtype of grad. k_idx int32 [N, C, W]: the forward's write ids. write_w f32
+ *   [N, C, W]: the write weights. dv [N*C, hd] dv_dtype: the forward's token rows. grad [P*S, hd]
+ *   grad_dtype: read only. d_delta_v f32 [N, C, hd], d_k_pd f32 [N, C, W]: written for the range.
+ *   status (nullable): device word OR-ed with SDM_DEV_BAD_SLOT when a valid token's write id lies
+ *   outside [0, S) (that lane adds nothing and its dot is 0).
+ * Errors: as sdm_pa.
+ */
+sdm_status sdm_gwr(const sdm_shape* shape, int32_t grad_dtype, const int32_t* k_idx, const float* write_w,
+                   const void* dv, const void* grad, float* d_delta_v, float* d_k_pd, int64_t step_begin,
+                   int64_t step_end, uint32_t* status, sdm_stream_t stream);
+
+/*
  * GDS, the read side of the backward (mover_da2_cuda.py: module docstring, the "GDS, split by data
  * need" comment, its read-records kernel), for the steps [step_begin, step_end), LAST step first
  * (two launches per step: the dots, then the scatter). Per chunk c = ti * P + p:

@@ -20,6 +20,7 @@ from .api import (  # noqa: F401
     forward_chunks_saving,
     forward_chunks_noalloc,
     gds,
+    gwr,
     pa,
     phase1,
     phase1_saving,

@@ -211,6 +211,19 @@ def pa(shape: ShapeSpec, sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, ba
     _check(st, "sdm_pa")
 
 
+def gwr(shape: ShapeSpec, k_idx, write_w, dv, grad, d_delta_v, d_k_pd, step_begin=0, step_end=None, status=None,
+        stream=None):
+    """sdm_gwr: the write side's token gather of the backward for steps [step_begin, step_end), last
+    step first. ``grad`` is float32 or bfloat16 (passed as grad_dtype)."""
+    step_end = shape.steps if step_end is None else step_end
+    gdt = {torch.float32: _abi.SDM_F32, torch.bfloat16: _abi.SDM_BF16}.get(grad.dtype)
+    if gdt is None:
+        raise TypeError("grad must be float32 or bfloat16")
+    st = _abi.load().sdm_gwr(ctypes.byref(shape.c()), gdt, _ptr(k_idx), _ptr(write_w), _ptr(dv), _ptr(grad),
+                             _ptr(d_delta_v), _ptr(d_k_pd), step_begin, step_end, _ptr(status), _stream(stream))
+    _check(st, "sdm_gwr")
+
+
 def gds(shape: ShapeSpec, sorted_q, q_idx, q_val, log_q, gr, bank, grad, d_q_w, step_begin=0, step_end=None,
         status=None, stream=None):
     """sdm_gds: the read side of the backward for steps [step_begin, step_end), last step first.

@@ -1,0 +1,184 @@
+// sdm_gwr.cu -- GWR, the token gather of the write side of the chunked sparse-delta-memory
+// backward, and its C entry point sdm_gwr (include/sdm.h).
+//
+// Arithmetic (sparse-delta-memory 2.0.0, pa_dc_cuda.py: module docstring, "GWR", and its GWR kernel),
+// per chunk c = ti * P + p and valid token t (padding tokens get zeros):
+//   d_delta_v[c, t] = acc, acc = 0; acc = fmaf(write_w[c, t, n], grad[p*S + k_idx[c, t, n]], acc)
+//                     over the write lanes n = 0 .. W-1 in order;
+//   d_k_pd[c, t, n] = <dv[c*C + t], grad[p*S + k_idx[c, t, n]]>,
+// the dot summed like every dot of the backward here (per lane an fmaf chain over its 4 columns of a
+// 128-column slice, the 32 lane partials in one fixed lane tree, slices added in order from 0).
+//
+// GB300 design: one launch per step, one warp per token. The grad rows of 16 write lanes are in flight
+// at once (a lane's 4 columns of each, kept in the storage type); the same registers feed the
+// gather's fmaf chain and the 16 dots, which are reduced across the lanes together (transposed), lane
+// n storing d_k_pd of lane n. Rows wider than 128 columns take their slices one after the other; a
+// token's dot sums are then carried in d_k_pd between slices by the lane that stores them.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "sdm_internal.cuh"
+#include "sdm_rows.cuh"
+
+namespace sdm {
+namespace {
+
+using namespace rows;
+
+constexpr int kGwrThreads = 256;
+constexpr int kGwrWarps = kGwrThreads / 32;
+
+struct GWRArgs {
+    const int32_t* k_idx;      // [N, C, W]
+    const float* write_w;      // [N, C, W]
+    const void* dv;            // [N * C, hd] dv type
+    const void* grad;          // [P * S, hd] grad type (read only)
+    float* d_delta_v;          // [N, C, hd]
+    float* d_k_pd;             // [N, C, W]
+    uint32_t* status;          // nullable
+    int P, C, W, hd, nsl, groups;
+    int valid;                 // valid tokens of this step's chunks
+    int64_t S, c0;
+};
+
+template <typename GradT, typename DvT>
+__global__ void __launch_bounds__(kGwrThreads) gwr_kernel(const GWRArgs a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cl = static_cast<int>(blockIdx.x / a.groups);
+    const int tg = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.groups);
+    const int t = tg * kGwrWarps + warp;
+    if (t >= a.C) return;   // warp-uniform
+    const int64_t c = a.c0 + cl;
+    const int hd = a.hd, W = a.W;
+    const bool tvalid = t < a.valid;
+    const int64_t tok = c * a.C + t;
+    const GradT* const grad = static_cast<const GradT*>(a.grad) + static_cast<int64_t>(cl) * a.S * hd;
+    const DvT* const dvrow = static_cast<const DvT*>(a.dv) + tok * hd;
+    const int32_t* const ki = a.k_idx + tok * W;
+    const float* const wi = a.write_w + tok * W;
+    float* const pd = a.d_k_pd + tok * W;
+    float* const out = a.d_delta_v + tok * hd;
+    uint32_t bad = 0;
+    for (int sl = 0; sl < a.nsl; ++sl) {
+        const int col = sl * 128 + lane * 4;
+        const bool on = col < hd;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (on && tvalid) ld4(dvrow + col, x);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int e0 = 0; e0 < W; e0 += 16) {
+            // lane e < 16: the slot and weight of write lane e0 + e (slot -1: no row)
+            int32_t myslot = -1;
+            float myw = 0.f;
+            if (tvalid && lane < 16 && e0 + lane < W) {
+                myslot = __ldg(ki + e0 + lane);
+                myw = __ldg(wi + e0 + lane);
+                if (myslot < 0 || static_cast<int64_t>(myslot) >= a.S) {
+                    myslot = -1;
+                    bad = 1u;
+                }
+            }
+            Raw4<GradT> g[16];   // the 16 lanes' grad rows, all in flight
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int32_t s = __shfl_sync(kFull, myslot, e);
+                g[e].zero();
+                if (on && s >= 0) g[e].ld(grad + static_cast<int64_t>(s) * hd + col);
+            }
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float we = __shfl_sync(kFull, myw, e);
+                const int32_t s = __shfl_sync(kFull, myslot, e);
+                float gf[4];
+                g[e].get(gf);
+                if (e0 + e < W && s >= 0) {   // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(we, gf[i], acc[i]);
+                }
+                v[e] = dot4(x, gf);
+            }
+            const float r = tsum16(v, lane);   // lane l: write lane e0 + (l & 15)
+            if (lane < 16 && e0 + lane < W) pd[e0 + lane] = (sl == 0 ? 0.f : pd[e0 + lane]) + r;
+        }
+        if (on) st4(out + col, acc);
+    }
+    if (__any_sync(kFull, bad != 0) && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
+}
+
+template <typename GradT>
+cudaError_t launch_g(const GWRArgs& a, int dv_bf16, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>(a.P) * a.groups;
+    if (dv_bf16)
+        gwr_kernel<GradT, __nv_bfloat16><<<blocks, kGwrThreads, 0, stream>>>(a);
+    else
+        gwr_kernel<GradT, float><<<blocks, kGwrThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// the shape rules of the forward's entry points (the same shape describes both directions)
+sdm_status check_shape(const sdm_shape* s) {
+    if (s == nullptr) return SDM_ERR_ARG;
+    if (s->val_dtype < 0 || s->val_dtype > 1 || s->dv_dtype < 0 || s->dv_dtype > 1 || s->bank_dtype < 0 ||
+        s->bank_dtype > 1)
+        return SDM_ERR_DTYPE;
+    if (s->P < 1 || s->C < 1 || s->C > kMaxC || s->W < 1 || s->W > kMaxLanes || s->R < 1 || s->R > kMaxLanes ||
+        s->steps < 1 || s->S < 1 || s->S > 0x7FFFFFFFll || s->hd < 1 || s->valid_last < 1 || s->valid_last > s->C ||
+        (s->gate_per_entry != 0 && s->gate_per_entry != 1))
+        return SDM_ERR_SHAPE;
+    if (s->hd % 4 != 0) return SDM_ERR_ALIGN;
+    const int64_t n = static_cast<int64_t>(s->C) * (s->W + s->R);
+    if (n > kMaxRow) return SDM_ERR_SHAPE;
+    if (s->steps > (int64_t(1) << 40) / s->P) return SDM_ERR_SHAPE;
+    const int64_t N = s->steps * s->P;
+    if (s->S > (int64_t(1) << 62) / s->P / s->hd) return SDM_ERR_SHAPE;
+    if (N > (int64_t(1) << 62) / (static_cast<int64_t>(s->C) * s->C + s->C * int64_t(s->hd) + n)) return SDM_ERR_SHAPE;
+    return SDM_OK;
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" sdm_status sdm_gwr(const sdm_shape* shape, int32_t grad_dtype, const int32_t* k_idx, const float* write_w,
+                              const void* dv, const void* grad, float* d_delta_v, float* d_k_pd, int64_t step_begin,
+                              int64_t step_end, uint32_t* status, sdm_stream_t stream) {
+    sdm_status st = check_shape(shape);
+    if (st != SDM_OK) return st;
+    if (grad_dtype != SDM_F32 && grad_dtype != SDM_BF16) return SDM_ERR_DTYPE;
+    if (step_begin < 0 || step_end > shape->steps || step_begin > step_end) return SDM_ERR_ARG;
+    const void* ptrs[] = {k_idx, write_w, dv, grad, d_delta_v, d_k_pd};
+    for (const void* p : ptrs)
+        if (p == nullptr) return SDM_ERR_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return SDM_ERR_ALIGN;
+    if (step_begin == step_end) return SDM_OK;
+    GWRArgs a;
+    memset(&a, 0, sizeof(a));
+    a.k_idx = k_idx;
+    a.write_w = write_w;
+    a.dv = dv;
+    a.grad = grad;
+    a.d_delta_v = d_delta_v;
+    a.d_k_pd = d_k_pd;
+    a.status = status;
+    a.P = shape->P;
+    a.C = shape->C;
+    a.W = shape->W;
+    a.hd = shape->hd;
+    a.nsl = (shape->hd + 127) / 128;
+    a.groups = (shape->C + kGwrWarps - 1) / kGwrWarps;
+    a.S = shape->S;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    for (int64_t ti = step_end - 1; ti >= step_begin; --ti) {   // last step first, like the backward
+        a.c0 = ti * a.P;
+        a.valid = ti == shape->steps - 1 ? shape->valid_last : shape->C;
+        const cudaError_t e = grad_dtype == SDM_BF16 ? launch_g<__nv_bfloat16>(a, shape->dv_dtype == SDM_BF16, cs)
+                                                     : launch_g<float>(a, shape->dv_dtype == SDM_BF16, cs);
+        if (e != cudaSuccess) return SDM_ERR_CUDA;
+    }
+    return SDM_OK;
+}

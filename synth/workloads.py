@@ -221,3 +221,15 @@ def make_read_grads(w: Workload, streams=None) -> np.ndarray:
         rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 19]))
         gr[:, i] = rng.standard_normal((st, C, hd), dtype=np.float32)
     return gr.reshape(st * Ps, C, hd)
+
+
+def make_write_weights(w: Workload, streams=None) -> np.ndarray:
+    """write_w [N, C, W] float32: the weights of the backward's token gather (GWR), normal with the
+    workload's value scale, chunk-major like make_inputs."""
+    streams = list(range(w.P)) if streams is None else list(streams)
+    Ps, st, C, W = len(streams), w.steps, w.C, w.W
+    out = np.empty((st, Ps, C, W), np.float32)
+    for i, p in enumerate(streams):
+        rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 23]))
+        out[:, i] = (rng.standard_normal((st, C, W), dtype=np.float32) * np.float32(w.val_scale)).astype(np.float32)
+    return out.reshape(st * Ps, C, W)
