@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -44,16 +45,24 @@ NCU_TRAFFIC = {
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
     "large:pa:38b81c18d626": round((106329344 + 43213568) * 4186081 / 4161534),
     "large:pa_bf16grad:38b81c18d626": round((73005824 + 15511552) * 4186081 / 4161534),
+    # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
+    # scaled by the read-groups ratio 4185964 / 4161643
+    "large:gds:3ed5ceddcb46": round((38025216 + 256 + 72641536 + 19404288) * 4185964 / 4161643),
+    # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
+    "large:gwr:941236122f79": 69741312 + 11264,
 }
 
 
 def src_hash(dom: str) -> str:
-    """Hash of the code of the sources that build kernel domain ``dom`` (its own .cu file, the
-    shared internal header and the launch code of sdm_api.cu): comment-only and blank lines do not
-    count, and a source added for another kernel does not change it."""
+    """Hash of the code of the sources that build kernel domain ``dom``: its own .cu file, the local
+    headers it includes and the launch code of sdm_api.cu. Comment-only and blank lines do not count,
+    and a source added for another kernel does not change it."""
     h = hashlib.sha1()
     d = os.path.join(ROOT, "sparse_slot_memory_gb300", "csrc")
-    for f in ("sdm_api.cu", f"sdm_{dom}.cu", "sdm_internal.cuh"):
+    own = f"sdm_{dom}.cu"
+    with open(os.path.join(d, own), encoding="utf-8") as fh:
+        heads = sorted(set(re.findall(r'#include "([^"/]+\.cuh)"', fh.read())))
+    for f in ["sdm_api.cu", own] + heads:
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             h.update(f.encode())
             for line in fh:
