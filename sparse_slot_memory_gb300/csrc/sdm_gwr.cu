@@ -16,6 +16,7 @@
 // token's dot sums are then carried in d_k_pd between slices by the lane that stores them.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "sdm_internal.cuh"
@@ -78,21 +79,26 @@ __global__ void __launch_bounds__(kGwrThreads) gwr_kernel(const GWRArgs a) {
                     bad = 1u;
                 }
             }
-            Raw4<GradT> g[16];   // the 16 lanes' grad rows, all in flight
+            // the 16 lanes' grad rows, all in flight: every load is unconditional (a lane without a
+            // row reads row 0 / column 0 of the stream and drops the value), so none waits on a branch
+            const uint32_t hasrow = __ballot_sync(kFull, myslot >= 0);
+            const int ccol = on ? col : 0;
+            Raw4<GradT> g[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int32_t s = __shfl_sync(kFull, myslot, e);
-                g[e].zero();
-                if (on && s >= 0) g[e].ld(grad + static_cast<int64_t>(s) * hd + col);
+                g[e].ld(grad + static_cast<int64_t>(s < 0 ? 0 : s) * hd + ccol);
             }
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const float we = __shfl_sync(kFull, myw, e);
-                const int32_t s = __shfl_sync(kFull, myslot, e);
                 float gf[4];
                 g[e].get(gf);
-                if (e0 + e < W && s >= 0) {   // warp-uniform
+                const bool use = ((hasrow >> e) & 1u) && on;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) gf[i] = use ? gf[i] : 0.f;
+                if ((hasrow >> e) & 1u) {   // warp-uniform
 #pragma unroll
                     for (int i = 0; i < 4; ++i) acc[i] = fmaf(we, gf[i], acc[i]);
                 }
@@ -106,14 +112,106 @@ __global__ void __launch_bounds__(kGwrThreads) gwr_kernel(const GWRArgs a) {
     if (__any_sync(kFull, bad != 0) && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
 
+// Rows of at most 128 columns and at most 16 write lanes (one slice, one block of lanes): the same
+// arithmetic as gwr_kernel, with a grid of resident warps only, each looping over tokens; the next
+// token's ids, weights and dv row load while the current token's grad rows are in flight.
+template <typename GradT, typename DvT>
+__global__ void __launch_bounds__(kGwrThreads) gwr_loop_kernel(const GWRArgs a, int total_warps) {
+    const int lane = threadIdx.x & 31;
+    const int ntok = a.P * a.C;
+    int it = blockIdx.x * kGwrWarps + (threadIdx.x >> 5);
+    if (it >= ntok) return;   // warp-uniform
+    const int hd = a.hd, W = a.W;
+    const int col = lane * 4;
+    const bool on = col < hd;
+    const int ccol = on ? col : 0;
+    uint32_t bad = 0;
+    // a token's ids, weights (lanes < W) and dv row
+    auto fetch = [&](int i, int32_t& slot, float& wt, float (&x)[4]) {
+        const int cl = i / a.C, t = i - cl * a.C;
+        const int64_t tok = (a.c0 + cl) * a.C + t;
+        slot = -1;
+        wt = 0.f;
+        x[0] = x[1] = x[2] = x[3] = 0.f;
+        if (t < a.valid) {
+            if (lane < W) {
+                slot = __ldg(a.k_idx + tok * W + lane);
+                wt = __ldg(a.write_w + tok * W + lane);
+                if (slot < 0 || static_cast<int64_t>(slot) >= a.S) {
+                    slot = -1;
+                    bad = 1u;
+                }
+            }
+            if (on) ld4(static_cast<const DvT*>(a.dv) + tok * hd + col, x);
+        }
+    };
+    int32_t myslot;
+    float myw, x[4];
+    fetch(it, myslot, myw, x);
+    for (;;) {
+        const int cl = it / a.C, t = it - cl * a.C;
+        const int64_t tok = (a.c0 + cl) * a.C + t;
+        const GradT* const grad = static_cast<const GradT*>(a.grad) + static_cast<int64_t>(cl) * a.S * hd;
+        const uint32_t hasrow = __ballot_sync(kFull, myslot >= 0);
+        Raw4<GradT> g[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int32_t s = __shfl_sync(kFull, myslot, e);
+            g[e].ld(grad + static_cast<int64_t>(s < 0 ? 0 : s) * hd + ccol);
+        }
+        const int nit = it + total_warps;
+        int32_t nslot = -1;
+        float nw = 0.f, nx[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nit < ntok) fetch(nit, nslot, nw, nx);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float we = __shfl_sync(kFull, myw, e);
+            float gf[4];
+            g[e].get(gf);
+            const bool use = ((hasrow >> e) & 1u) && on;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gf[i] = use ? gf[i] : 0.f;
+            if ((hasrow >> e) & 1u) {   // warp-uniform
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = fmaf(we, gf[i], acc[i]);
+            }
+            v[e] = dot4(x, gf);
+        }
+        const float r = tsum16(v, lane);
+        if (lane < W) a.d_k_pd[tok * W + lane] = 0.f + r;
+        if (on) st4(a.d_delta_v + tok * hd + col, acc);
+        if (nit >= ntok) break;
+        it = nit;
+        myslot = nslot;
+        myw = nw;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = nx[i];
+    }
+    if (__any_sync(kFull, bad != 0) && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
+}
+
+template <typename GradT, typename DvT>
+cudaError_t launch_gd(const GWRArgs& a, cudaStream_t stream) {
+    if (a.nsl == 1 && a.W <= 16) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gwr_loop_kernel<GradT, DvT>, kGwrThreads, 0);
+        if (e != cudaSuccess) return e;
+        const int ntok = a.P * a.C;
+        const int blocks = std::max(1, std::min((ntok + kGwrWarps - 1) / kGwrWarps, sms * std::max(per_sm, 1)));
+        gwr_loop_kernel<GradT, DvT><<<blocks, kGwrThreads, 0, stream>>>(a, blocks * kGwrWarps);
+    } else {
+        gwr_kernel<GradT, DvT><<<static_cast<unsigned>(a.P) * a.groups, kGwrThreads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 template <typename GradT>
 cudaError_t launch_g(const GWRArgs& a, int dv_bf16, cudaStream_t stream) {
-    const unsigned blocks = static_cast<unsigned>(a.P) * a.groups;
-    if (dv_bf16)
-        gwr_kernel<GradT, __nv_bfloat16><<<blocks, kGwrThreads, 0, stream>>>(a);
-    else
-        gwr_kernel<GradT, float><<<blocks, kGwrThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return dv_bf16 ? launch_gd<GradT, __nv_bfloat16>(a, stream) : launch_gd<GradT, float>(a, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
