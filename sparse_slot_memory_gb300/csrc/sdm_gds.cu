@@ -22,6 +22,7 @@
 // Every grad row is written by one warp once per launch (a single writer: no atomics).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "sdm_internal.cuh"
@@ -88,23 +89,98 @@ __global__ void __launch_bounds__(kGdsThreads) gds_dots_kernel(const GDSArgs a) 
             const bool on = col < hd;
             float x[4] = {0.f, 0.f, 0.f, 0.f};
             if (on && tvalid) ld4(grow + col, x);
-            Raw4<BankT> m[16];   // the 16 entries' bank rows, all in flight
+            // the 16 entries' bank rows, all in flight: every load is unconditional (a lane without a
+            // row reads row 0 / column 0 of the stream and drops the value), so none waits on a branch
+            const uint32_t hasrow = __ballot_sync(kFull, myslot >= 0);
+            const int ccol = on ? col : 0;
+            Raw4<BankT> m[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int32_t s = __shfl_sync(kFull, myslot, e);
-                m[e].zero();
-                if (on && s >= 0) m[e].ld(bank + static_cast<int64_t>(s) * hd + col);
+                m[e].ld(bank + static_cast<int64_t>(s < 0 ? 0 : s) * hd + ccol);
             }
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 float mf[4];
                 m[e].get(mf);
+                const bool use = ((hasrow >> e) & 1u) && on;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mf[i] = use ? mf[i] : 0.f;
                 v[e] = dot4(x, mf);
             }
             total += tsum16(v, lane);
         }
         if (lane < 16 && e0 + lane < R) drow[e0 + lane] = tvalid ? total : 0.f;
+    }
+    if (__any_sync(kFull, bad != 0) && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
+}
+
+// Rows of at most 128 columns and at most 16 read lanes (one slice, one block of entries): the same
+// arithmetic as gds_dots_kernel, with a grid of resident warps only, each looping over tokens; the
+// next token's ids and reading gradient load while the current token's bank rows are in flight.
+template <typename BankT>
+__global__ void __launch_bounds__(kGdsThreads) gds_dots_loop_kernel(const GDSArgs a, int total_warps) {
+    const int lane = threadIdx.x & 31;
+    const int ntok = a.P * a.C;
+    int it = blockIdx.x * kGdsWarps + (threadIdx.x >> 5);
+    if (it >= ntok) return;   // warp-uniform
+    const int hd = a.hd, R = a.R;
+    const int col = lane * 4;
+    const bool on = col < hd;
+    const int ccol = on ? col : 0;
+    uint32_t bad = 0;
+    auto fetch = [&](int i, int32_t& slot, float (&x)[4]) {
+        const int cl = i / a.C, t = i - cl * a.C;
+        const int64_t tok = (a.c0 + cl) * a.C + t;
+        slot = -1;
+        x[0] = x[1] = x[2] = x[3] = 0.f;
+        if (t < a.valid) {
+            if (lane < R) {
+                slot = __ldg(a.q_idx + tok * R + lane);
+                if (slot < 0 || static_cast<int64_t>(slot) >= a.S) {
+                    slot = -1;
+                    bad = 1u;
+                }
+            }
+            if (on) ld4(a.gr + tok * hd + col, x);
+        }
+    };
+    int32_t myslot;
+    float x[4];
+    fetch(it, myslot, x);
+    for (;;) {
+        const int cl = it / a.C, t = it - cl * a.C;
+        const int64_t tok = (a.c0 + cl) * a.C + t;
+        const BankT* const bank = static_cast<const BankT*>(a.bank) + static_cast<int64_t>(cl) * a.S * hd;
+        const uint32_t hasrow = __ballot_sync(kFull, myslot >= 0);
+        Raw4<BankT> m[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int32_t s = __shfl_sync(kFull, myslot, e);
+            m[e].ld(bank + static_cast<int64_t>(s < 0 ? 0 : s) * hd + ccol);
+        }
+        const int nit = it + total_warps;
+        int32_t nslot = -1;
+        float nx[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nit < ntok) fetch(nit, nslot, nx);
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float mf[4];
+            m[e].get(mf);
+            const bool use = ((hasrow >> e) & 1u) && on;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mf[i] = use ? mf[i] : 0.f;
+            v[e] = dot4(x, mf);
+        }
+        const float total = 0.f + tsum16(v, lane);
+        if (lane < R) a.d_q_w[tok * R + lane] = t < a.valid ? total : 0.f;
+        if (nit >= ntok) break;
+        it = nit;
+        myslot = nslot;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = nx[i];
     }
     if (__any_sync(kFull, bad != 0) && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
@@ -314,13 +390,26 @@ cudaError_t launch_scatter(const GDSArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <typename BankT>
+cudaError_t launch_dots(const GDSArgs& a, cudaStream_t stream) {
+    if (a.nsl == 1 && a.R <= 16) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gds_dots_loop_kernel<BankT>, kGdsThreads, 0);
+        if (e != cudaSuccess) return e;
+        const int ntok = a.P * a.C;
+        const int blocks = std::max(1, std::min((ntok + kGdsWarps - 1) / kGdsWarps, sms * std::max(per_sm, 1)));
+        gds_dots_loop_kernel<BankT><<<blocks, kGdsThreads, 0, stream>>>(a, blocks * kGdsWarps);
+    } else {
+        gds_dots_kernel<BankT><<<static_cast<unsigned>(a.P) * a.dgroups, kGdsThreads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gds(const GDSArgs& a, int grad_bf16, int bank_bf16, int val_bf16, cudaStream_t stream) {
-    const unsigned dblocks = static_cast<unsigned>(a.P) * a.dgroups;
-    if (bank_bf16)
-        gds_dots_kernel<__nv_bfloat16><<<dblocks, kGdsThreads, 0, stream>>>(a);
-    else
-        gds_dots_kernel<float><<<dblocks, kGdsThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = bank_bf16 ? launch_dots<__nv_bfloat16>(a, stream) : launch_dots<float>(a, stream);
     if (e != cudaSuccess) return e;
     if (grad_bf16)
         return val_bf16 ? launch_scatter<__nv_bfloat16, __nv_bfloat16>(a, stream)
