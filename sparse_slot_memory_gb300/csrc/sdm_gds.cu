@@ -313,24 +313,25 @@ __global__ void __launch_bounds__(kGdsThreads, 2) gds_scatter_kernel(const GDSAr
     const int flast = 31 - __clz(fmask);
     const bool open = (lmask >> flast) == 0u;
     const int cend = open ? flast - 1 : 31 - __clz(lmask);
-    GradT* const grad = static_cast<GradT*>(a.grad);
+    GradT* const grad_s = static_cast<GradT*>(a.grad) + static_cast<int64_t>(cl) * a.S * hd;   // the stream's rows
     const float* const gr_chunk = a.gr + c * a.C * static_cast<int64_t>(hd);
     uint32_t bad = 0;
     if (cend >= f0) {
         for (int sl = 0; sl < a.nsl; ++sl) {
             const int col = sl * 128 + lane * 4;
             const bool on = col < hd;
+            const int ccol = on ? col : 0;   // a lane past the row copies nothing (zero fill) from column 0
             // position k's rows go to ring slot (k - f0) % kGdsRing: its token's reading gradient and,
             // for a group's FIRST, the group's grad row; one commit group per position
             auto issue = [&](int k) {
                 if (k <= cend) {   // warp-uniform
-                    const int ks = (k - f0) % kGdsRing;
+                    const int ks = (k - f0) & (kGdsRing - 1);
                     const int tk = __shfl_sync(kFull, t, k);
                     const int32_t sk = __shfl_sync(kFull, slot, k);
-                    if (((okmask >> k) & 1u) && on)
-                        cp4(reinterpret_cast<float*>(&ring.gr[ks][lane]), gr_chunk + static_cast<int64_t>(tk) * hd + col);
-                    if (((fmask >> k) & 1u) && on && sk >= 0 && static_cast<int64_t>(sk) < a.S)
-                        cp4(&ring.grad[ks][lane][0], grad + (static_cast<int64_t>(cl) * a.S + sk) * hd + col);
+                    if ((okmask >> k) & 1u)
+                        cp4z(reinterpret_cast<float*>(&ring.gr[ks][lane]), gr_chunk + tk * hd + ccol, on);
+                    if (((fmask >> k) & 1u) && sk >= 0 && static_cast<int64_t>(sk) < a.S)
+                        cp4z(&ring.grad[ks][lane][0], grad_s + static_cast<int64_t>(sk) * hd + ccol, on);
                 }
                 cp_commit();
             };
@@ -339,25 +340,22 @@ __global__ void __launch_bounds__(kGdsThreads, 2) gds_scatter_kernel(const GDSAr
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, cg[4] = {0.f, 0.f, 0.f, 0.f};
             int64_t crow = 0;
             bool cbad = true;
-#pragma unroll 1
+#pragma unroll 4
             for (int k = f0; k <= cend; ++k) {
                 issue(k + kGdsRing - 1);
-                cp_wait<kGdsRing - 1>();   // position k's copies have landed
-                const int ks = (k - f0) % kGdsRing;
+                cp_wait<kGdsRing - 1>();   // position k's copies have landed (zeros past the row)
+                const int ks = (k - f0) & (kGdsRing - 1);
                 if ((fmask >> k) & 1u) {   // a group starts
                     const int32_t sk = __shfl_sync(kFull, slot, k);
                     cbad = sk < 0 || static_cast<int64_t>(sk) >= a.S;
-                    crow = (static_cast<int64_t>(cl) * a.S + (cbad ? 0 : sk)) * hd + col;
+                    crow = static_cast<int64_t>(cbad ? 0 : sk) * hd + ccol;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[i] = 0.f;
-                        cg[i] = 0.f;
-                    }
+                    for (int i = 0; i < 4; ++i) acc[i] = 0.f;
                     if (cbad) bad = 1u;
-                    else if (on) get4(&ring.grad[ks][lane][0], cg);
+                    else get4(&ring.grad[ks][lane][0], cg);
                 }
                 const float skk = __shfl_sync(kFull, sc, k);
-                if (!cbad && ((okmask >> k) & 1u) && on) {
+                if (!cbad && ((okmask >> k) & 1u)) {
                     float d[4];
                     get4(reinterpret_cast<const float*>(&ring.gr[ks][lane]), d);
 #pragma unroll
@@ -367,7 +365,7 @@ __global__ void __launch_bounds__(kGdsThreads, 2) gds_scatter_kernel(const GDSAr
                     float o[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) o[i] = cg[i] + acc[i];
-                    st4(grad + crow, o);
+                    st4(grad_s + crow, o);
                 }
             }
             cp_wait<0>();

@@ -290,6 +290,15 @@ __device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src, i
     else
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem_src) : "memory");
 }
+// The same with a zero fill: a lane with `on` false reads nothing and writes zeros.
+__device__ __forceinline__ void cp_async_z(void* smem_dst, const void* gmem_src, int bytes, bool on) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    const int n = on ? bytes : 0;
+    if (bytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -396,9 +405,10 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
     const int32_t gslot = __shfl_sync(kFull, slot, myf < 0 ? 0 : myf);
     const bool mybad = gslot < 0 || static_cast<int64_t>(gslot) >= a.S;
 
-    GradT* const grad = static_cast<GradT*>(a.grad);
-    BankT* const bank = static_cast<BankT*>(a.bank);
-    const BankT* const snap = static_cast<const BankT*>(a.snap);
+    // the stream's rows and the chunk's token rows and snapshot rows (element pointers)
+    GradT* const grad_s = static_cast<GradT*>(a.grad) + static_cast<int64_t>(cl) * a.S * hd;
+    BankT* const bank_s = static_cast<BankT*>(a.bank) + static_cast<int64_t>(cl) * a.S * hd;
+    const BankT* const snap_c = static_cast<const BankT*>(a.snap) + static_cast<int64_t>(cl) * nk * hd;
     const float* const dva_chunk = a.dva + c * a.C * static_cast<int64_t>(hd);
     uint32_t bad = 0;
     float dk = 0.f, gs = 0.f;   // this lane's entry: its <dva, snap> and <gdw, snap> sums over the slices
@@ -406,21 +416,22 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
         for (int sl = 0; sl < a.nsl; ++sl) {
             const int col = sl * 128 + lane * 4;
             const bool on = col < hd;
+            const int ccol = on ? col : 0;   // a lane past the row copies nothing (zero fill) from column 0
             // position k's rows go to ring slot (k - f0) % kPaRing: its token row, and for a group's
             // FIRST the group's grad and snapshot rows; one commit group per position
             auto issue = [&](int k) {
                 if (k <= cend) {   // warp-uniform
-                    const int ks = (k - f0) % kPaRing;
+                    const int ks = (k - f0) & (kPaRing - 1);
                     const int tk = __shfl_sync(kFull, t, k);
                     const int32_t sk = __shfl_sync(kFull, slot, k);
-                    if (((okmask >> k) & 1u) && on)
-                        cp_async(&ring.dva[ks][lane], dva_chunk + static_cast<int64_t>(tk) * hd + col, 16);
-                    if (((fmask >> k) & 1u) && on && sk >= 0 && static_cast<int64_t>(sk) < a.S) {
+                    if ((okmask >> k) & 1u)
+                        cp_async_z(&ring.dva[ks][lane], dva_chunk + tk * hd + ccol, 16, on);
+                    if (((fmask >> k) & 1u) && sk >= 0 && static_cast<int64_t>(sk) < a.S) {
                         const int g = ord0 + __popc(fmask & ((1u << k) - 1u));
-                        cp_async(&ring.grad[ks][lane][0], grad + (static_cast<int64_t>(cl) * a.S + sk) * hd + col,
-                                 static_cast<int>(4 * sizeof(GradT)));
-                        cp_async(&ring.snap[ks][lane][0], snap + (static_cast<int64_t>(cl) * nk + g) * hd + col,
-                                 static_cast<int>(4 * sizeof(BankT)));
+                        cp_async_z(&ring.grad[ks][lane][0], grad_s + static_cast<int64_t>(sk) * hd + ccol,
+                                   static_cast<int>(4 * sizeof(GradT)), on);
+                        cp_async_z(&ring.snap[ks][lane][0], snap_c + static_cast<int64_t>(g) * hd + ccol,
+                                   static_cast<int>(4 * sizeof(BankT)), on);
                     }
                 }
                 cp_commit();
@@ -443,24 +454,18 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
                     const int k = blk * 8 + i;
                     if (k < f0 || k > cend) continue;   // warp-uniform
                     issue(k + kPaRing - 1);
-                    cp_wait<kPaRing - 1>();   // position k's copies have landed
-                    const int ks = (k - f0) % kPaRing;
+                    cp_wait<kPaRing - 1>();   // position k's copies have landed (zeros past the row)
+                    const int ks = (k - f0) & (kPaRing - 1);
                     if ((fmask >> k) & 1u) {    // a group starts: its rows become current
                         const int32_t sk = __shfl_sync(kFull, slot, k);
                         cbad = sk < 0 || static_cast<int64_t>(sk) >= a.S;
-                        crow = (static_cast<int64_t>(cl) * a.S + (cbad ? 0 : sk)) * hd + col;
+                        crow = static_cast<int64_t>(cbad ? 0 : sk) * hd + ccol;
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            cg[x] = 0.f;
-                            cs[x] = 0.f;
-                            acc[x] = 0.f;
-                        }
+                        for (int x = 0; x < 4; ++x) acc[x] = 0.f;
                         if (!cbad) {
-                            if (on) {
-                                get4(&ring.grad[ks][lane][0], cg);
-                                get4(&ring.snap[ks][lane][0], cs);
-                                copy_raw4(bank + crow, &ring.snap[ks][lane][0]);
-                            }
+                            get4(&ring.grad[ks][lane][0], cg);
+                            get4(&ring.snap[ks][lane][0], cs);
+                            if (on) copy_raw4(bank_s + crow, &ring.snap[ks][lane][0]);
                             gp[i] = dot4(cg, cs);
                         } else {
                             bad = 1u;
@@ -468,8 +473,8 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
                     }
                     const float skk = __shfl_sync(kFull, sc, k);
                     if (!cbad && ((okmask >> k) & 1u)) {
-                        float d[4] = {0.f, 0.f, 0.f, 0.f};
-                        if (on) get4(reinterpret_cast<const float*>(&ring.dva[ks][lane]), d);
+                        float d[4];
+                        get4(reinterpret_cast<const float*>(&ring.dva[ks][lane]), d);
 #pragma unroll
                         for (int x = 0; x < 4; ++x) acc[x] = fmaf(skk, d[x], acc[x]);
                         dp[i] = dot4(d, cs);
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
                             float ov[4];
 #pragma unroll
                             for (int x = 0; x < 4; ++x) ov[x] = fmaf(cg[x], cpl, acc[x]);
-                            st4(grad + crow, ov);
+                            st4(grad_s + crow, ov);
                         }
                     }
                 }

@@ -88,6 +88,16 @@ __device__ __forceinline__ void cp4(T* smem_dst, const T* gmem_src) {
     else
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem_src) : "memory");
 }
+// The same with a zero fill: a lane with `on` false reads nothing and writes zeros.
+template <typename T>
+__device__ __forceinline__ void cp4z(T* smem_dst, const T* gmem_src, bool on) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    const int n = on ? static_cast<int>(4 * sizeof(T)) : 0;
+    if constexpr (sizeof(T) == 4)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
