@@ -19,6 +19,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "sdm_checks.cuh"
 #include "sdm_internal.cuh"
 #include "sdm_rows.cuh"
 
@@ -214,28 +215,6 @@ cudaError_t launch_g(const GWRArgs& a, int dv_bf16, cudaStream_t stream) {
     return dv_bf16 ? launch_gd<GradT, __nv_bfloat16>(a, stream) : launch_gd<GradT, float>(a, stream);
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// the shape rules of the forward's entry points (the same shape describes both directions)
-sdm_status check_shape(const sdm_shape* s) {
-    if (s == nullptr) return SDM_ERR_ARG;
-    if (s->val_dtype < 0 || s->val_dtype > 1 || s->dv_dtype < 0 || s->dv_dtype > 1 || s->bank_dtype < 0 ||
-        s->bank_dtype > 1)
-        return SDM_ERR_DTYPE;
-    if (s->P < 1 || s->C < 1 || s->C > kMaxC || s->W < 1 || s->W > kMaxLanes || s->R < 1 || s->R > kMaxLanes ||
-        s->steps < 1 || s->S < 1 || s->S > 0x7FFFFFFFll || s->hd < 1 || s->valid_last < 1 || s->valid_last > s->C ||
-        (s->gate_per_entry != 0 && s->gate_per_entry != 1))
-        return SDM_ERR_SHAPE;
-    if (s->hd % 4 != 0) return SDM_ERR_ALIGN;
-    const int64_t n = static_cast<int64_t>(s->C) * (s->W + s->R);
-    if (n > kMaxRow) return SDM_ERR_SHAPE;
-    if (s->steps > (int64_t(1) << 40) / s->P) return SDM_ERR_SHAPE;
-    const int64_t N = s->steps * s->P;
-    if (s->S > (int64_t(1) << 62) / s->P / s->hd) return SDM_ERR_SHAPE;
-    if (N > (int64_t(1) << 62) / (static_cast<int64_t>(s->C) * s->C + s->C * int64_t(s->hd) + n)) return SDM_ERR_SHAPE;
-    return SDM_OK;
-}
-
 }  // namespace
 }  // namespace sdm
 
@@ -244,15 +223,9 @@ using namespace sdm;
 extern "C" sdm_status sdm_gwr(const sdm_shape* shape, int32_t grad_dtype, const int32_t* k_idx, const float* write_w,
                               const void* dv, const void* grad, float* d_delta_v, float* d_k_pd, int64_t step_begin,
                               int64_t step_end, uint32_t* status, sdm_stream_t stream) {
-    sdm_status st = check_shape(shape);
+    const void* const ptrs[] = {k_idx, write_w, dv, grad, d_delta_v, d_k_pd};
+    const sdm_status st = checks::check_backward(shape, grad_dtype, step_begin, step_end, ptrs);
     if (st != SDM_OK) return st;
-    if (grad_dtype != SDM_F32 && grad_dtype != SDM_BF16) return SDM_ERR_DTYPE;
-    if (step_begin < 0 || step_end > shape->steps || step_begin > step_end) return SDM_ERR_ARG;
-    const void* ptrs[] = {k_idx, write_w, dv, grad, d_delta_v, d_k_pd};
-    for (const void* p : ptrs)
-        if (p == nullptr) return SDM_ERR_ARG;
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return SDM_ERR_ALIGN;
     if (step_begin == step_end) return SDM_OK;
     GWRArgs a;
     memset(&a, 0, sizeof(a));

@@ -30,12 +30,15 @@
 
 #include <cstring>
 
+#include "sdm_checks.cuh"
 #include "sdm_internal.cuh"
+#include "sdm_rows.cuh"
 
 namespace sdm {
 namespace {
 
-constexpr uint32_t kFull = 0xFFFFFFFFu;
+using namespace rows;
+
 constexpr int kPaThreads = 256;
 constexpr int kPaWarps = kPaThreads / 32;
 constexpr int kPaTile = kPaThreads;        // sorted positions per CTA: 32 per warp
@@ -62,40 +65,6 @@ struct PAArgs {
     int64_t S, c0;             // c0: the step's first chunk
 };
 
-__device__ __forceinline__ float widen(float x) { return x; }
-__device__ __forceinline__ float widen(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// a lane's 4 columns of a row as floats
-__device__ __forceinline__ void ld4(const float* p, float (&o)[4]) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-}
-__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&o)[4]) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
-}
-// the grad row is read once and rewritten in the same launch: the coherent L2 path
-__device__ __forceinline__ void ld4cg(const float* p, float (&o)[4]) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-}
-__device__ __forceinline__ void ld4cg(const __nv_bfloat16* p, float (&o)[4]) {
-    const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
-    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
-}
-__device__ __forceinline__ void st4(float* p, const float (&o)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
-}
-__device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&lo);
-    u.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p) = u;
-}
 // raw copy of a lane's 4 columns (the snapshot row is the bank row's bytes)
 __device__ __forceinline__ void copy4(float* d, const float* s) {
     *reinterpret_cast<float4*>(d) = __ldg(reinterpret_cast<const float4*>(s));
@@ -112,44 +81,6 @@ __device__ __forceinline__ void copy_raw4(__nv_bfloat16* d, const __nv_bfloat16*
     *reinterpret_cast<uint2*>(d) = *reinterpret_cast<const uint2*>(s);
 }
 
-__device__ __forceinline__ float dot4(const float (&x)[4], const float (&y)[4]) {
-    return fmaf(x[3], y[3], fmaf(x[2], y[2], fmaf(x[1], y[1], x[0] * y[0])));
-}
-// The sum of x over the 32 lanes, in every lane: an xor butterfly of levels 1, 2, 4, 8, 16 (both
-// partners add the same pair, so every lane holds the same bits).
-__device__ __forceinline__ float allsum(float x) {
-#pragma unroll
-    for (int k = 1; k <= 16; k <<= 1) x += __shfl_xor_sync(kFull, x, k);
-    return x;
-}
-
-// 16 values per lane, each summed over the 32 lanes by the same tree as allsum (levels 1, 2, 4, 8,
-// 16; a level-h node adds the values of lanes l and l ^ h), transposed: at level h a lane keeps the
-// values whose index bit matches its lane bit and adds its partner's copy, so each level halves the
-// values. Lane l returns the sum of value (l & 15): 16 shuffles for 16 sums instead of 80.
-__device__ __forceinline__ float tsum16(const float (&v)[16], int lane) {
-    float a[8], b[4], c[2];
-    const bool h1 = lane & 1, h2 = lane & 2, h4 = lane & 4, h8 = lane & 8;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {   // a[m]: index 2m + (lane & 1)
-        const float keep = h1 ? v[2 * m + 1] : v[2 * m], send = h1 ? v[2 * m] : v[2 * m + 1];
-        a[m] = keep + __shfl_xor_sync(kFull, send, 1);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {   // b[m]: index 4m + (lane & 3)
-        const float keep = h2 ? a[2 * m + 1] : a[2 * m], send = h2 ? a[2 * m] : a[2 * m + 1];
-        b[m] = keep + __shfl_xor_sync(kFull, send, 2);
-    }
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {   // c[m]: index 8m + (lane & 7)
-        const float keep = h4 ? b[2 * m + 1] : b[2 * m], send = h4 ? b[2 * m] : b[2 * m + 1];
-        c[m] = keep + __shfl_xor_sync(kFull, send, 4);
-    }
-    const float keep = h8 ? c[1] : c[0], send = h8 ? c[0] : c[1];
-    float x = keep + __shfl_xor_sync(kFull, send, 8);   // index lane & 15
-    x += __shfl_xor_sync(kFull, x, 16);
-    return x;
-}
 __device__ __forceinline__ bool valid_first(uint32_t v) { return (v & kFirst) != 0 && (v & kInvalidBit) == 0; }
 
 // One window of up to 32 members of a group, lane i holding member i.
@@ -282,41 +213,6 @@ __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, in
     }
 }
 
-// Per-lane asynchronous copies into shared memory (each lane later reads back only what it copied).
-__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src, int bytes) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-    if (bytes == 16)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
-    else
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem_src) : "memory");
-}
-// The same with a zero fill: a lane with `on` false reads nothing and writes zeros.
-__device__ __forceinline__ void cp_async_z(void* smem_dst, const void* gmem_src, int bytes, bool on) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-    const int n = on ? bytes : 0;
-    if (bytes == 16)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
-    else
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(d), "l"(gmem_src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-template <typename T>
-__device__ __forceinline__ void get4(const T* p, float (&o)[4]);
-template <>
-__device__ __forceinline__ void get4(const float* p, float (&o)[4]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-}
-template <>
-__device__ __forceinline__ void get4(const __nv_bfloat16* p, float (&o)[4]) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
-}
-
 // Shared memory of one warp: a ring of kPaRing positions, per position and lane the lane's 4 columns
 // of the token row (f32), of the grad row and of the snapshot row.
 template <typename GradT, typename BankT>
@@ -425,13 +321,11 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
                     const int tk = __shfl_sync(kFull, t, k);
                     const int32_t sk = __shfl_sync(kFull, slot, k);
                     if ((okmask >> k) & 1u)
-                        cp_async_z(&ring.dva[ks][lane], dva_chunk + tk * hd + ccol, 16, on);
+                        cp4z(reinterpret_cast<float*>(&ring.dva[ks][lane]), dva_chunk + tk * hd + ccol, on);
                     if (((fmask >> k) & 1u) && sk >= 0 && static_cast<int64_t>(sk) < a.S) {
                         const int g = ord0 + __popc(fmask & ((1u << k) - 1u));
-                        cp_async_z(&ring.grad[ks][lane][0], grad_s + static_cast<int64_t>(sk) * hd + ccol,
-                                   static_cast<int>(4 * sizeof(GradT)), on);
-                        cp_async_z(&ring.snap[ks][lane][0], snap_c + static_cast<int64_t>(g) * hd + ccol,
-                                   static_cast<int>(4 * sizeof(BankT)), on);
+                        cp4z(&ring.grad[ks][lane][0], grad_s + static_cast<int64_t>(sk) * hd + ccol, on);
+                        cp4z(&ring.snap[ks][lane][0], snap_c + static_cast<int64_t>(g) * hd + ccol, on);
                     }
                 }
                 cp_commit();
@@ -543,28 +437,6 @@ cudaError_t launch_pa(const PAArgs& a, int grad_bf16, int bank_bf16, int val_bf1
     return bank_bf16 ? launch_v<float, __nv_bfloat16>(a, val_bf16, stream) : launch_v<float, float>(a, val_bf16, stream);
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// the shape rules of the forward's entry points (the same shape describes both directions)
-sdm_status check_shape(const sdm_shape* s) {
-    if (s == nullptr) return SDM_ERR_ARG;
-    if (s->val_dtype < 0 || s->val_dtype > 1 || s->dv_dtype < 0 || s->dv_dtype > 1 || s->bank_dtype < 0 ||
-        s->bank_dtype > 1)
-        return SDM_ERR_DTYPE;
-    if (s->P < 1 || s->C < 1 || s->C > kMaxC || s->W < 1 || s->W > kMaxLanes || s->R < 1 || s->R > kMaxLanes ||
-        s->steps < 1 || s->S < 1 || s->S > 0x7FFFFFFFll || s->hd < 1 || s->valid_last < 1 || s->valid_last > s->C ||
-        (s->gate_per_entry != 0 && s->gate_per_entry != 1))
-        return SDM_ERR_SHAPE;
-    if (s->hd % 4 != 0) return SDM_ERR_ALIGN;
-    const int64_t n = static_cast<int64_t>(s->C) * (s->W + s->R);
-    if (n > kMaxRow) return SDM_ERR_SHAPE;
-    if (s->steps > (int64_t(1) << 40) / s->P) return SDM_ERR_SHAPE;
-    const int64_t N = s->steps * s->P;
-    if (s->S > (int64_t(1) << 62) / s->P / s->hd) return SDM_ERR_SHAPE;
-    if (N > (int64_t(1) << 62) / (static_cast<int64_t>(s->C) * s->C + s->C * int64_t(s->hd) + n)) return SDM_ERR_SHAPE;
-    return SDM_OK;
-}
-
 }  // namespace
 }  // namespace sdm
 
@@ -575,15 +447,9 @@ extern "C" sdm_status sdm_pa(const sdm_shape* shape, int32_t grad_dtype, const i
                              const float* dva, void* grad, void* bank, const void* snap, float* d_k_eff,
                              float* grad_g, int64_t step_begin, int64_t step_end, uint32_t* status,
                              sdm_stream_t stream) {
-    sdm_status st = check_shape(shape);
+    const void* const ptrs[] = {sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, bank, snap, d_k_eff, grad_g};
+    const sdm_status st = checks::check_backward(shape, grad_dtype, step_begin, step_end, ptrs);
     if (st != SDM_OK) return st;
-    if (grad_dtype != SDM_F32 && grad_dtype != SDM_BF16) return SDM_ERR_DTYPE;
-    if (step_begin < 0 || step_end > shape->steps || step_begin > step_end) return SDM_ERR_ARG;
-    const void* ptrs[] = {sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, bank, snap, d_k_eff, grad_g};
-    for (const void* p : ptrs)
-        if (p == nullptr) return SDM_ERR_ARG;
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return SDM_ERR_ALIGN;
     if (step_begin == step_end) return SDM_OK;
     PAArgs a;
     memset(&a, 0, sizeof(a));
