@@ -1,6 +1,7 @@
 /*
- * sdm.h -- C ABI of the GB300 (sm_103a) forward hot path of the chunked sparse-delta-memory
- * (SDM) recurrence: Phase 1 and the Phase-2 decay-and-write (DW).
+ * sdm.h -- C ABI of the GB300 (sm_103a) hot path of the chunked sparse-delta-memory (SDM)
+ * recurrence: the forward's Phase 1 and Phase-2 decay-and-write (DW), the saving forward's dense
+ * snapshot, and the deterministic backward's step kernels (Phase A, GWR, GDS).
  *
  * Definitions followed (sparse-delta-memory 2.0.0):
  *   phase1_cuda.py, module docstring ........ the Phase-1 outputs and the determinism contract
@@ -12,6 +13,9 @@
  *                                              acc = fma(sc_m, dv[tok_m], acc) in sorted order
  *   mover_fx_cuda.py, module docstring ....... the bank-direct DW contract (base read from the
  *                                              bank row itself; one writer per row and launch)
+ *   pa_dc_cuda.py, module docstring .......... the backward step: Phase A (the backward of DW)
+ *                                              and GWR (the write side's token gather)
+ *   mover_da2_cuda.py, "GDS, split by data need" the backward's read side (dots and scatter)
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer owned by the caller. The library never allocates
@@ -30,8 +34,8 @@
  *     1 <= S <= 2^31 - 1, P * S * hd fits in int64.
  *   - Shape, dtype, alignment and workspace errors are returned BEFORE any launch. Errors the
  *     device finds (a valid slot id outside [0, S)) are OR-ed into a status word inside the
- *     workspace; read it with sdm_device_status. No kernel traps, and no kernel waits on another
- *     thread block.
+ *     workspace (read it with sdm_device_status), or, for the backward entry points, into the
+ *     caller's optional status word. No kernel traps, and no kernel waits on another thread block.
  *   - Determinism: for fixed inputs, shapes and GPU type every output is bitwise reproducible.
  *     The sort is stable, scans combine in a fixed tree, every A/QK cell and every bank row has
  *     one writer that adds its terms in an input-determined order, and no atomics touch a sum.
