@@ -120,32 +120,38 @@ __device__ __forceinline__ Member member_window(const PAArgs& a, const int32_t* 
 }
 
 // acc += the window's terms on this lane's 4 columns; returns this lane's member's <dva, snap> sum
-// over the slice (lanes >= m.n get 0).
+// over the slice (lanes >= m.n get 0). Members go in blocks of 16 whose dot partials are reduced
+// across the lanes together (rows::tsum16, the tree of rows::allsum): member k's sum lands in lane k.
 __device__ __forceinline__ float window_terms(const Member& m, const float* dva_col, int hd, bool on,
                                               const float (&sn)[4], float (&acc)[4], int lane) {
     float mine = 0.f;
     const uint32_t okm = __ballot_sync(kFull, m.ok);   // members that name an entry of the chunk
-    for (int k0 = 0; k0 < m.n; k0 += kPaBatch) {
-        float d[kPaBatch][4];
+    for (int k0 = 0; k0 < m.n; k0 += 16) {   // k0 = 0 or 16
+        float v[16];
 #pragma unroll
-        for (int u = 0; u < kPaBatch; ++u) {
-            const int tk = __shfl_sync(kFull, m.tok, (k0 + u) & 31);
-            if (((okm >> ((k0 + u) & 31)) & 1u) && k0 + u < m.n && on) {
-                ld4(dva_col + static_cast<int64_t>(tk) * hd, d[u]);
-            } else {
+        for (int b = 0; b < 16; b += kPaBatch) {
+            float d[kPaBatch][4];
+#pragma unroll
+            for (int u = 0; u < kPaBatch; ++u) {
+                const int k = k0 + b + u;
+                const int tk = __shfl_sync(kFull, m.tok, k & 31);
                 d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+                if (k < m.n && ((okm >> (k & 31)) & 1u) && on) ld4(dva_col + static_cast<int64_t>(tk) * hd, d[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kPaBatch; ++u) {
+                const int k = k0 + b + u;
+                const float scu = __shfl_sync(kFull, m.sc, k & 31);
+                v[b + u] = 0.f;
+                if (k < m.n && ((okm >> (k & 31)) & 1u)) {   // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[u][i], acc[i]);
+                    v[b + u] = dot4(d[u], sn);
+                }
             }
         }
-#pragma unroll
-        for (int u = 0; u < kPaBatch; ++u) {
-            const float s = __shfl_sync(kFull, m.sc, (k0 + u) & 31);
-            if (k0 + u < m.n && ((okm >> ((k0 + u) & 31)) & 1u)) {   // warp-uniform
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = fmaf(s, d[u][i], acc[i]);
-                const float r = allsum(dot4(d[u], sn));
-                if (lane == k0 + u) mine = r;
-            }
-        }
+        const float red = tsum16(v, lane);
+        if ((lane >> 4) == (k0 >> 4)) mine = red;
     }
     return mine;
 }
@@ -187,14 +193,24 @@ __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, in
         gsum += allsum(dot4(g4, s4));
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         float cpl = 1.f;
+        Member m = member_window<ValT>(a, srow, f, c, lane);
         for (int q = f;; q += 32) {
-            const Member m = member_window<ValT>(a, srow, q, c, lane);
+            Member nm = m;
+            if (!m.last) nm = member_window<ValT>(a, srow, q + 32, c, lane);   // the next window's scalars in flight
             const float r = window_terms(m, dva_chunk + col, hd, on, s4, acc, lane);
-            if (m.ok) a.d_k_eff[m.o] = (sl == 0 ? 0.f : a.d_k_eff[m.o]) + r;
+            if (m.ok) {
+                if (a.nsl == 1) {   // one slice: the sums are final
+                    a.d_k_eff[m.o] = -m.beta * (0.f + r);
+                    a.grad_g[m.o] = m.cp * gsum;
+                } else {
+                    a.d_k_eff[m.o] = (sl == 0 ? 0.f : a.d_k_eff[m.o]) + r;
+                }
+            }
             if (m.last) {
                 cpl = __shfl_sync(kFull, m.cp, m.n - 1);
                 break;
             }
+            m = nm;
         }
         if (on) {
             float o[4];
@@ -203,6 +219,7 @@ __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, in
             st4(grad + row + col, o);
         }
     }
+    if (a.nsl == 1) return;
     for (int q = f;; q += 32) {
         const Member m = member_window<ValT>(a, srow, q, c, lane);
         if (m.ok) {
