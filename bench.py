@@ -43,7 +43,7 @@ NCU_TRAFFIC = {
     "large:phase1:6922acd872e5": 55624960 + 718927616,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:e9db2724dc98": round((106344960 + 43424256) * 4186081 / 4161534),
+    "large:pa:4c47240459f4": round((106345728 + 43396352) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
     "large:gds:30cb5bbb86cc": round((38027264 + 512 + 72652032 + 19650048) * 4185964 / 4161643),

@@ -42,7 +42,6 @@ using namespace rows;
 constexpr int kPaThreads = 256;
 constexpr int kPaWarps = kPaThreads / 32;
 constexpr int kPaTile = kPaThreads;        // sorted positions per CTA: 32 per warp
-constexpr int kPaBatch = 4;                // a long group's member token rows in flight together
 constexpr int kPaRing = 8;                 // in-window positions whose rows are in flight (per warp)
 constexpr int kPaCountUnroll = 16;         // sorted words per thread in flight while counting FIRSTs
 constexpr uint32_t kPaSentinel = kFirst | kLast | kInvalidBit;
@@ -120,34 +119,36 @@ __device__ __forceinline__ Member member_window(const PAArgs& a, const int32_t* 
 }
 
 // acc += the window's terms on this lane's 4 columns; returns this lane's member's <dva, snap> sum
-// over the slice (lanes >= m.n get 0). Members go in blocks of 16 whose dot partials are reduced
+// over the slice (lanes >= m.n get 0). Members go in blocks of 16: the block's 16 token rows are
+// cp.async-copied into the warp's shared-memory ring at once (one round trip per block; each lane
+// copies and reads back its own 4 columns, zeros past the row), then their dot partials are reduced
 // across the lanes together (rows::tsum16, the tree of rows::allsum): member k's sum lands in lane k.
-__device__ __forceinline__ float window_terms(const Member& m, const float* dva_col, int hd, bool on,
-                                              const float (&sn)[4], float (&acc)[4], int lane) {
+__device__ __forceinline__ float window_terms(const Member& m, const float* dva_col, bool dva_on, int hd,
+                                              const float (&sn)[4], float (&acc)[4], int lane, float4* buf) {
     float mine = 0.f;
     const uint32_t okm = __ballot_sync(kFull, m.ok);   // members that name an entry of the chunk
     for (int k0 = 0; k0 < m.n; k0 += 16) {   // k0 = 0 or 16
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int k = k0 + u;
+            const int tk = __shfl_sync(kFull, m.tok, k & 31);
+            if (k < m.n && ((okm >> (k & 31)) & 1u))   // warp-uniform
+                cp4z(reinterpret_cast<float*>(&buf[u * 32 + lane]), dva_col + static_cast<int64_t>(tk) * hd, dva_on);
+        }
+        cp_commit();
+        cp_wait<0>();
         float v[16];
 #pragma unroll
-        for (int b = 0; b < 16; b += kPaBatch) {
-            float d[kPaBatch][4];
+        for (int u = 0; u < 16; ++u) {
+            const int k = k0 + u;
+            const float scu = __shfl_sync(kFull, m.sc, k & 31);
+            v[u] = 0.f;
+            if (k < m.n && ((okm >> (k & 31)) & 1u)) {   // warp-uniform
+                float d[4];
+                get4(reinterpret_cast<const float*>(&buf[u * 32 + lane]), d);
 #pragma unroll
-            for (int u = 0; u < kPaBatch; ++u) {
-                const int k = k0 + b + u;
-                const int tk = __shfl_sync(kFull, m.tok, k & 31);
-                d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
-                if (k < m.n && ((okm >> (k & 31)) & 1u) && on) ld4(dva_col + static_cast<int64_t>(tk) * hd, d[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < kPaBatch; ++u) {
-                const int k = k0 + b + u;
-                const float scu = __shfl_sync(kFull, m.sc, k & 31);
-                v[b + u] = 0.f;
-                if (k < m.n && ((okm >> (k & 31)) & 1u)) {   // warp-uniform
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[u][i], acc[i]);
-                    v[b + u] = dot4(d[u], sn);
-                }
+                for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[i], acc[i]);
+                v[u] = dot4(d, sn);
             }
         }
         const float red = tsum16(v, lane);
@@ -161,7 +162,7 @@ __device__ __forceinline__ float window_terms(const Member& m, const float* dva_
 // sum kept in d_k_eff between slices. Same arithmetic and order as the in-window groups.
 template <typename GradT, typename BankT, typename ValT>
 __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, int64_t c, int cl, int f, int ord,
-                                        int lane, uint32_t* bad) {
+                                        int lane, uint32_t* bad, float4* buf) {
     GradT* const grad = static_cast<GradT*>(a.grad);
     BankT* const bank = static_cast<BankT*>(a.bank);
     const BankT* const snap = static_cast<const BankT*>(a.snap);
@@ -197,7 +198,7 @@ __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, in
         for (int q = f;; q += 32) {
             Member nm = m;
             if (!m.last) nm = member_window<ValT>(a, srow, q + 32, c, lane);   // the next window's scalars in flight
-            const float r = window_terms(m, dva_chunk + col, hd, on, s4, acc, lane);
+            const float r = window_terms(m, dva_chunk + (on ? col : 0), on, hd, s4, acc, lane, buf);
             if (m.ok) {
                 if (a.nsl == 1) {   // one slice: the sums are final
                     a.d_k_eff[m.o] = -m.beta * (0.f + r);
@@ -427,7 +428,11 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
             a.grad_g[o] = mybad ? 0.f : cp * gs;
         }
     }
-    if (open) open_group<GradT, BankT, ValT>(a, srow, c, cl, q0 + flast, ord0 + __popc(fmask) - 1, lane, &bad);
+    // the walk reuses the warp's ring (idle by now: every copy has landed) as 16 token-row slots
+    static_assert(sizeof(PaRing<GradT, BankT>) >= 16 * 32 * sizeof(float4), "the ring holds 16 rows per lane");
+    if (open)
+        open_group<GradT, BankT, ValT>(a, srow, c, cl, q0 + flast, ord0 + __popc(fmask) - 1, lane, &bad,
+                                       reinterpret_cast<float4*>(&ring));
     if (bad && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
 
