@@ -46,7 +46,7 @@ NCU_TRAFFIC = {
     "large:pa:4c47240459f4": round((106345728 + 43396352) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
-    "large:gds:30cb5bbb86cc": round((38027264 + 512 + 72652032 + 19650048) * 4185964 / 4161643),
+    "large:gds:58ed4c9cbe68": round((38026496 + 256 + 72660992 + 19850240) * 4185964 / 4161643),
     # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
     "large:gwr:e67855001ebf": 69737728 + 52992,
 }

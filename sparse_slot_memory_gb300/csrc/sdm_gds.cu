@@ -38,7 +38,6 @@ constexpr int kGdsThreads = 256;
 constexpr int kGdsWarps = kGdsThreads / 32;
 constexpr int kGdsTile = kGdsThreads;      // sorted read positions per scatter CTA: 32 per warp
 constexpr int kGdsRing = 8;                // in-window positions whose rows are in flight (per warp)
-constexpr int kGdsBatch = 8;               // a long group's member token rows in flight together
 constexpr uint32_t kGdsSentinel = kFirst | kLast | kInvalidBit;
 
 struct GDSArgs {
@@ -219,10 +218,14 @@ __device__ __forceinline__ QMember qmember_window(const GDSArgs& a, const int32_
     return m;
 }
 
-// A read group that starts at sorted position f and ends past its warp's 32 positions.
+// A read group that starts at sorted position f and ends past its warp's 32 positions (a hot slot):
+// windows of 32 members follow it to its LAST, the next window's scalars in flight while this one's
+// rows arrive. Per block of 16 members the token rows are cp.async-copied into the warp's idle ring
+// at once (each lane copies and reads back its own 4 columns, zeros past the row), then added in
+// member order: the same fmaf chain as the in-window groups.
 template <typename GradT, typename ValT>
 __device__ __noinline__ void open_read_group(const GDSArgs& a, const int32_t* srow, int64_t c, int cl, int f, int lane,
-                                             uint32_t* bad) {
+                                             uint32_t* bad, float4* buf) {
     GradT* const grad = static_cast<GradT*>(a.grad);
     const int hd = a.hd;
     const float* const gr_chunk = a.gr + c * a.C * static_cast<int64_t>(hd);
@@ -238,30 +241,38 @@ __device__ __noinline__ void open_read_group(const GDSArgs& a, const int32_t* sr
     for (int sl = 0; sl < a.nsl; ++sl) {
         const int col = sl * 128 + lane * 4;
         const bool on = col < hd;
+        const float* const gr_col = gr_chunk + (on ? col : 0);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        int32_t unused;
+        QMember m = qmember_window<ValT>(a, srow, f, c, lane, &unused);
         for (int q = f;; q += 32) {
-            int32_t unused;
-            const QMember m = qmember_window<ValT>(a, srow, q, c, lane, &unused);
+            QMember nm = m;
+            if (!m.last) nm = qmember_window<ValT>(a, srow, q + 32, c, lane, &unused);
             const uint32_t okm = __ballot_sync(kFull, m.ok);
-            for (int k0 = 0; k0 < m.n; k0 += kGdsBatch) {
-                float d[kGdsBatch][4];
+            for (int k0 = 0; k0 < m.n; k0 += 16) {   // k0 = 0 or 16
 #pragma unroll
-                for (int u = 0; u < kGdsBatch; ++u) {
-                    const int tk = __shfl_sync(kFull, m.tok, (k0 + u) & 31);
-                    d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
-                    if (k0 + u < m.n && ((okm >> ((k0 + u) & 31)) & 1u) && on)
-                        ld4(gr_chunk + static_cast<int64_t>(tk) * hd + col, d[u]);
+                for (int u = 0; u < 16; ++u) {
+                    const int k = k0 + u;
+                    const int tk = __shfl_sync(kFull, m.tok, k & 31);
+                    if (k < m.n && ((okm >> (k & 31)) & 1u))   // warp-uniform
+                        cp4z(reinterpret_cast<float*>(&buf[u * 32 + lane]), gr_col + static_cast<int64_t>(tk) * hd, on);
                 }
+                cp_commit();
+                cp_wait<0>();
 #pragma unroll
-                for (int u = 0; u < kGdsBatch; ++u) {
-                    const float scu = __shfl_sync(kFull, m.sc, (k0 + u) & 31);
-                    if (k0 + u < m.n && ((okm >> ((k0 + u) & 31)) & 1u)) {
+                for (int u = 0; u < 16; ++u) {
+                    const int k = k0 + u;
+                    const float scu = __shfl_sync(kFull, m.sc, k & 31);
+                    if (k < m.n && ((okm >> (k & 31)) & 1u)) {   // warp-uniform
+                        float d[4];
+                        get4(reinterpret_cast<const float*>(&buf[u * 32 + lane]), d);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[u][i], acc[i]);
+                        for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[i], acc[i]);
                     }
                 }
             }
             if (m.last) break;
+            m = nm;
         }
         if (on) {
             float g[4], o[4];
@@ -279,6 +290,8 @@ template <typename GradT>
 struct GdsRing {
     float4 gr[kGdsRing][32];
     GradT grad[kGdsRing][32][4];
+    // a hot read group's walk reuses the ring as 16 token-row slots per lane
+    float4 pad[sizeof(GradT) == 4 ? 0 : 16 - kGdsRing - kGdsRing / 2][32];
 };
 
 template <typename GradT, typename ValT>
@@ -372,7 +385,8 @@ __global__ void __launch_bounds__(kGdsThreads, 2) gds_scatter_kernel(const GDSAr
             cp_wait<0>();
         }
     }
-    if (open) open_read_group<GradT, ValT>(a, srow, c, cl, q0 + flast, lane, &bad);
+    static_assert(sizeof(GdsRing<GradT>) >= 16 * 32 * sizeof(float4), "the ring holds 16 rows per lane");
+    if (open) open_read_group<GradT, ValT>(a, srow, c, cl, q0 + flast, lane, &bad, reinterpret_cast<float4*>(&ring));
     if (bad && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
 
