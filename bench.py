@@ -148,7 +148,7 @@ def count_groups(x, w):
 
 
 def algorithmic_bytes(w, x, groups, saving=False):
-    """Bytes per forward (SURVEY section 8(d) accounting): inputs read once, outputs written once,
+    """Algorithmic bytes per forward: inputs read once, outputs written once,
     dv rows read once, per slot group one base-row read and one row write (the saving forward:
     and one snapshot row write)."""
     vt = 2 if w.val_dtype == "bf16" else 4
