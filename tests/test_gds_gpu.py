@@ -41,6 +41,9 @@ CASES = {
     "few_slots": (scaled(WORKLOADS["tiny"], P=3, T=200, C=64, S=8, hd=16, W=5, R=3, name="few_slots"), "f32"),
     # R = 20: a token's entries span two blocks of 16 dots; two slices, one with half its lanes
     "r20": (scaled(WORKLOADS["tiny"], P=2, T=130, C=64, S=300, hd=200, W=2, R=20, name="r20"), "f32"),
+    # edge shapes: rows of 4 columns (one lane), single-token chunks with one read lane
+    "edge_hd4": (scaled(WORKLOADS["tiny"], P=1, T=70, C=64, S=64, hd=4, W=2, R=2, name="edge_hd4"), "f32"),
+    "edge_c1": (scaled(WORKLOADS["tiny"], P=2, T=3, C=1, S=16, hd=8, W=3, R=1, name="edge_c1"), "bf16"),
 }
 
 

@@ -32,6 +32,9 @@ CASES = {
     "wide_ragged": (scaled(WORKLOADS["wide_ragged"], P=2, T=300, S=8192), "bf16"),
     # W = 20: two blocks of 16 write lanes; hd = 200: a second slice with half its lanes
     "w20": (scaled(WORKLOADS["tiny"], P=2, T=130, C=64, S=300, hd=200, W=20, R=2, name="w20"), "f32"),
+    # edge shapes: rows of 4 columns (one lane), single-token chunks with one read lane
+    "edge_hd4": (scaled(WORKLOADS["tiny"], P=1, T=70, C=64, S=64, hd=4, W=2, R=2, name="edge_hd4"), "f32"),
+    "edge_c1": (scaled(WORKLOADS["tiny"], P=2, T=3, C=1, S=16, hd=8, W=3, R=1, name="edge_c1"), "bf16"),
 }
 
 
