@@ -13,7 +13,8 @@ definitions (pair sums over lane pairs, the token-sequential bank recurrence, so
 Python's ``sorted``, rex/cpe closed forms, flag invariants; for Phase A a hand-worked chunk, the
 single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked chunk and the
 adjoint identity between the scatter and the weighted read; for GWR a hand-worked chunk and a
-dense gather matrix applied by a library matmul).
+dense gather matrix applied by a library matmul; GWR and Phase A's decay term also as the
+vector-Jacobian products of the forward DW oracle in the token rows and in the base rows).
 """
 
 from __future__ import annotations

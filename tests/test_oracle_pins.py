@@ -622,3 +622,66 @@ def test_gwr_matches_a_dense_gather_matrix():
     assert np.isclose(np.sum(dd * dv), np.sum(w * pd))
     valid = (k_idx >= 0) & (k_idx < S) & (np.arange(C)[:, None] < V)
     assert np.all(pd[~valid] == 0.0)
+
+
+def _dw_vjp_case(seed=21):
+    """A small chunk with repeated slots and a repeated write entry of one token, its Phase-1 rex / cpe."""
+    rng = np.random.default_rng(seed)
+    C, W, R, S, hd = 7, 3, 2, 5, 4
+    k_idx = rng.integers(0, S, size=(C, W)).astype(np.int32)
+    k_idx[2, 1] = k_idx[2, 0]                       # a token writing one slot twice
+    q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
+    k_val = rng.standard_normal((C, W)).astype(np.float32)
+    q_val = rng.standard_normal((C, R)).astype(np.float32)
+    g = (-rng.random(C) * 0.5).astype(np.float32)
+    o = oracle.phase1(k_idx[None], q_idx[None], k_val[None], q_val[None], g[None], S=S, val_dtype="f32", pairs=False)
+    return C, W, S, hd, k_idx, q_idx, k_val, q_val, g, o, rng
+
+
+def _dw(base, dv, k_idx, q_idx, k_val, q_val, g, S, C):
+    b = base.copy()
+    oracle.dw_chunk(b, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=C, val_dtype="f32", bank_dtype="f32",
+                    round_cpe=False, round_bank=False)
+    return b
+
+
+def test_gwr_is_the_vjp_of_dw_in_the_token_rows():
+    """GWR with write weights k * exp(rex) (the DW record's scale) is the vector-Jacobian product of the
+    forward DW (oracle.dw_chunk, exact arithmetic) with respect to the token rows dv: the DW is linear in
+    dv, so <grad, DW(dv + e_ti) - DW(dv)> is d_delta_v[t, i] exactly (up to rounding)."""
+    C, W, S, hd, k_idx, q_idx, k_val, q_val, g, o, rng = _dw_vjp_case()
+    base = rng.standard_normal((S, hd))
+    dv = rng.standard_normal((C, hd))
+    grad = rng.standard_normal((S, hd))
+    b0 = _dw(base, dv, k_idx, q_idx, k_val, q_val, g, S, C)
+    vjp = np.zeros((C, hd))
+    for t in range(C):
+        for i in range(hd):
+            d1 = dv.copy()
+            d1[t, i] += 1.0
+            vjp[t, i] = np.sum(grad * (_dw(base, d1, k_idx, q_idx, k_val, q_val, g, S, C) - b0))
+    write_w = k_val.astype(np.float64) * np.exp(o["rex"][0])
+    dd, *_ = oracle.gwr_chunk(grad, k_idx, write_w, dv, S=S, V=C)
+    assert np.allclose(dd, vjp, rtol=1e-9, atol=1e-9)
+
+
+def test_pa_decay_term_is_the_vjp_of_dw_in_the_base_rows():
+    """Phase A's grad update with d_dva = 0 is the vector-Jacobian product of the forward DW with
+    respect to the bank rows before the write: grad[s] * cpe_last for written slots (cpe = exp of the
+    group's gate total), grad[s] unchanged elsewhere."""
+    C, W, S, hd, k_idx, q_idx, k_val, q_val, g, o, rng = _dw_vjp_case(22)
+    base = rng.standard_normal((S, hd))
+    dv = rng.standard_normal((C, hd))
+    grad = rng.standard_normal((S, hd))
+    b0 = _dw(base, dv, k_idx, q_idx, k_val, q_val, g, S, C)
+    vjp = np.zeros((S, hd))
+    for s in range(S):
+        for i in range(hd):
+            b1 = base.copy()
+            b1[s, i] += 1.0
+            vjp[s, i] = np.sum(grad * (_dw(b1, dv, k_idx, q_idx, k_val, q_val, g, S, C) - b0))
+    slots = oracle.snapshot_slots(k_idx, S=S, V=C)
+    got = grad.copy()
+    oracle.pa_chunk(got, np.zeros((S, hd)), np.zeros((len(slots), hd)), k_idx, k_val.astype(np.float64),
+                    o["log_k"][0], o["cpe"][0], np.ones(C), np.zeros((C, hd)), S=S, V=C)
+    assert np.allclose(got, vjp, rtol=1e-9, atol=1e-9)
