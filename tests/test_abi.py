@@ -99,3 +99,22 @@ def test_no_cpu_path_for_host_tensors():
     spec = sdm.ShapeSpec(P=1, C=4, W=1, R=1, hd=4, steps=1, S=8, valid_last=4)
     with pytest.raises(TypeError):
         sdm.dw(spec, torch.zeros(4, 4), torch.zeros(8, 4), torch.zeros(1 << 16, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("fn, nptr", [("sdm_pa", 12), ("sdm_gwr", 6), ("sdm_gds", 8)])
+def test_backward_argument_errors(lib, fn, nptr):
+    """The backward entry points check shape, grad dtype, step range, null and misaligned arrays
+    before any CUDA call (the pointers below are never dereferenced)."""
+    f = getattr(lib, fn)
+    good = [ctypes.c_void_p(0x10000 + 256 * i) for i in range(nptr)]   # 16-byte aligned, never touched
+    s = shape()
+    assert f(ctypes.byref(s), 0, *([None] * nptr), 0, 32, None, None) == -1              # null arrays
+    assert f(ctypes.byref(s), 7, *good, 0, 32, None, None) == -3                         # grad dtype
+    assert f(ctypes.byref(shape(C=257)), 0, *good, 0, 32, None, None) == -2              # shape
+    assert f(ctypes.byref(shape(hd=6)), 0, *good, 0, 32, None, None) == -4               # hd % 4
+    assert f(ctypes.byref(s), 0, *good, 5, 4, None, None) == -1                          # reversed range
+    assert f(ctypes.byref(s), 0, *good, 0, 33, None, None) == -1                         # past the last step
+    bad = list(good)
+    bad[-1] = ctypes.c_void_p(0x10000 + 8)
+    assert f(ctypes.byref(s), 0, *bad, 0, 32, None, None) == -4                          # misaligned
+    assert f(ctypes.byref(s), 1, *good, 3, 3, None, None) == 0                           # empty range: no launch
