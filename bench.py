@@ -35,6 +35,11 @@ from synth import WORKLOADS, make_inputs, scaled  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 
+METRIC_FWD = "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak"
+METRIC_PA = "SDM backward Phase A (the backward of DW) tokens/sec and achieved HBM GB/s vs GB300 peak"
+METRIC_GDS = "SDM backward GDS (read-side dots + grad scatter) tokens/sec and achieved HBM GB/s vs GB300 peak"
+METRIC_GWR = "SDM backward GWR (write-side token gather) tokens/sec and achieved HBM GB/s vs GB300 peak"
+
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload, kernel and the
 # hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
 # voids the figure (reported as null).
@@ -329,7 +334,7 @@ def run_ours(args):
     if rank == 0:
         cpu = None if args.no_cpu_baseline else cpu_baseline(w, x, budget_s=args.cpu_seconds)
         result = {
-            "metric": "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "metric": METRIC_FWD,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.val_dtype, "data": "synthetic (seeded generators of the workload's distributions)",
@@ -534,7 +539,7 @@ def run_pa(args):
                                                                 make_backward_inputs(w, streams=[0]),
                                                                 budget_s=args.cpu_seconds)
         result = {
-            "metric": "SDM backward Phase A (the backward of DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "metric": METRIC_PA,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generators; Phase-1 outputs and snapshot from one saving forward)",
@@ -731,7 +736,7 @@ def run_gds(args):
             x0 = make_inputs(w, streams=[0])
             cpu = gds_cpu_baseline(w, x0, make_read_grads(w, streams=[0]).astype(np.float64), budget_s=args.cpu_seconds)
         result = {
-            "metric": "SDM backward GDS (read-side dots + grad scatter) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "metric": METRIC_GDS,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generators; sorted read rows and log_q from one Phase 1)",
@@ -899,7 +904,7 @@ def run_gwr(args):
             cpu = gwr_cpu_baseline(w, make_inputs(w, streams=[0]), make_write_weights(w, streams=[0]),
                                    budget_s=args.cpu_seconds)
         result = {
-            "metric": "SDM backward GWR (write-side token gather) tokens/sec and achieved HBM GB/s vs GB300 peak",
+            "metric": METRIC_GWR,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generators)",
@@ -960,24 +965,45 @@ def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
 
 
 def run_reference(args):
+    """The reference arm: the float64 oracle of the same mode (forward, or --pa / --gds / --gwr) on
+    bounded samples of the same workload, on this host's cores; rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
     x = make_inputs(w, streams=[0])
+    grad_sfx = "+bf16grad" if args.pa_grad == "bf16" else ""
+    if args.pa:
+        from synth import make_backward_inputs
+        b = make_backward_inputs(w, streams=[0])
+        metric, name = METRIC_PA, w.name + "+phaseA" + grad_sfx
+        sample = lambda budget, mc=None: pa_cpu_baseline(w, x, b, budget_s=budget, max_chunks=mc)   # noqa: E731
+    elif args.gds:
+        from synth import make_read_grads
+        gr = make_read_grads(w, streams=[0]).astype(np.float64)
+        metric, name = METRIC_GDS, w.name + "+gds" + grad_sfx
+        sample = lambda budget, mc=None: gds_cpu_baseline(w, x, gr, budget_s=budget, max_chunks=mc)  # noqa: E731
+    elif args.gwr:
+        from synth import make_write_weights
+        ww = make_write_weights(w, streams=[0])
+        metric, name = METRIC_GWR, w.name + "+gwr" + grad_sfx
+        sample = lambda budget, mc=None: gwr_cpu_baseline(w, x, ww, budget_s=budget, max_chunks=mc)  # noqa: E731
+    else:
+        metric, name = METRIC_FWD, w.name
+        sample = lambda budget, mc=None: cpu_baseline(w, x, budget_s=budget, max_chunks=mc)  # noqa: E731
     for _ in range(args.warmup):
-        cpu_baseline(w, x, budget_s=1.0, max_chunks=1)
+        sample(1.0, 1)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(w, x, budget_s=args.cpu_seconds / max(1, args.steps)))
+        vals.append(sample(args.cpu_seconds / max(1, args.steps)))
     el = time.perf_counter() - t0
     v = statistics.mean(r["value"] for r in vals)
     print(json.dumps({
-        "impl": "reference", "metric": "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak",
+        "impl": "reference", "metric": metric,
         "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": {"workload": w.name, **w.describe()},
+        "dtype": "f64", "data": "synthetic", "config": {**w.describe(), "workload": name},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
