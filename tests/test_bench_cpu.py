@@ -37,3 +37,19 @@ def test_traffic_keys_name_known_kernels():
         workload, dom, h = key.split(":")
         assert workload in WORKLOADS and len(h) == 12
         assert dom.split("_")[0] in ("dw", "phase1", "pa", "gds", "gwr")
+
+
+def test_reference_arm_every_mode(capsys):
+    """`bench.py --impl reference` prints one JSON line per mode with the GPU arm's metric names (tiny
+    workload, a fraction of a second of oracle time each)."""
+    import argparse
+    import json
+
+    for mode, metric in (("", bench.METRIC_FWD), ("pa", bench.METRIC_PA), ("gds", bench.METRIC_GDS),
+                         ("gwr", bench.METRIC_GWR)):
+        args = argparse.Namespace(workload="tiny", steps=1, warmup=0, cpu_seconds=0.2, pa=mode == "pa",
+                                  gds=mode == "gds", gwr=mode == "gwr", pa_grad="f32")
+        bench.run_reference(args)
+        d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert d["impl"] == "reference" and d["metric"] == metric and d["value"] > 0
+        assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
