@@ -685,3 +685,37 @@ def test_pa_decay_term_is_the_vjp_of_dw_in_the_base_rows():
     oracle.pa_chunk(got, np.zeros((S, hd)), np.zeros((len(slots), hd)), k_idx, k_val.astype(np.float64),
                     o["log_k"][0], o["cpe"][0], np.ones(C), np.zeros((C, hd)), S=S, V=C)
     assert np.allclose(got, vjp, rtol=1e-9, atol=1e-9)
+
+
+def test_gds_is_the_vjp_of_the_weighted_read():
+    """GDS is the vector-Jacobian product of the chunk's weighted read y[t] = sum_r q_w[t, r] bank[q_idx[t, r]]
+    (q_w = q exp(log_q), valid tokens only) for the loss L = sum_t <gr[t], y[t]>: the scatter's change of
+    the grad rows is dL/dbank, and d_q_w is dL/dq_w; both checked by unit perturbations of a read written
+    here as a plain double loop."""
+    rng = np.random.default_rng(13)
+    S, C, R, hd, V = 6, 5, 3, 4, 4
+    q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
+    q_val, log_q = rng.standard_normal((C, R)), -rng.random((C, R))
+    gr, bank = rng.standard_normal((C, hd)), rng.standard_normal((S, hd))
+
+    def loss(bk, qw):
+        return sum(float(np.dot(gr[t], qw[t, r] * bk[q_idx[t, r]])) for t in range(V) for r in range(R))
+
+    qw = q_val * np.exp(log_q)
+    base = loss(bank, qw)
+    d_bank = np.zeros((S, hd))
+    for s in range(S):
+        for i in range(hd):
+            b1 = bank.copy()
+            b1[s, i] += 1.0
+            d_bank[s, i] = loss(b1, qw) - base
+    d_qw = np.zeros((C, R))
+    for t in range(C):
+        for r in range(R):
+            q1 = qw.copy()
+            q1[t, r] += 1.0
+            d_qw[t, r] = loss(bank, q1) - base
+    grad = np.zeros((S, hd))
+    dq, *_ = oracle.gds_chunk(grad, bank, q_idx, q_val, log_q, gr, S=S, V=V)
+    assert np.allclose(grad, d_bank, rtol=1e-9, atol=1e-9)
+    assert np.allclose(dq, d_qw, rtol=1e-9, atol=1e-9)
