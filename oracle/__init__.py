@@ -11,8 +11,9 @@ Python loops here.
 Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
 definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
 Python's ``sorted``, rex/cpe closed forms, flag invariants; for Phase A a hand-worked chunk, the
-single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked chunk and the
-adjoint identity between the scatter and the weighted read; for GWR a hand-worked chunk and a
+single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked chunk, the
+adjoint identity between the scatter and the weighted read, and the vector-Jacobian product of a
+plain read loop; for GWR a hand-worked chunk and a
 dense gather matrix applied by a library matmul; GWR and Phase A's decay term also as the
 vector-Jacobian products of the forward DW oracle in the token rows and in the base rows).
 """
