@@ -51,7 +51,8 @@ class ShapeSpec:
     @classmethod
     def from_workload(cls, w, P=None) -> "ShapeSpec":
         return cls(P=w.P if P is None else P, C=w.C, W=w.W, R=w.R, hd=w.hd, steps=w.steps, S=w.S,
-                   valid_last=w.valid_last, val_dtype=w.val_dtype, dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype)
+                   valid_last=w.valid_last, val_dtype=w.val_dtype, dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype,
+                   gate_per_entry=bool(getattr(w, "gate_per_entry", False)))
 
 
 def _ptr(t):

@@ -7,7 +7,8 @@ docstring and ``p1_keys_zw_kernel``) lays its rows out: chunk ``c = ti * P + p``
 * ``k_idx`` int32 ``[N, C, W]``, ``q_idx`` int32 ``[N, C, R]``: stream-local slot ids in ``[0, S)``;
   tokens past the stream's end (the last step, when ``T % C != 0``) hold ``-1``.
 * ``k_val`` / ``q_val``: ``[N, C, W]`` / ``[N, C, R]`` float32, or bfloat16 kept as uint16 bit patterns.
-* ``g`` float32 ``[N, C]``: one log-decay gate per token, ``logsigmoid(N(mu, 1))``.
+* ``g`` float32 ``[N, C]``: one log-decay gate per token, ``logsigmoid(N(mu, 1))``; with
+  ``gate_per_entry`` ``[N, C, W]``, one per write entry, drawn the same way.
 * ``dv`` ``[N * C, hd]``: the value delta of every token (row ``c * C + t``).
 * bank ``[P * S, hd]``: stream ``p`` owns rows ``[p * S, (p + 1) * S)``; drawn per stream.
 
@@ -44,6 +45,7 @@ class Workload:
     gate_mu: float    # gates are logsigmoid(N(gate_mu, 1))
     seed: int
     zipf_s: float = 1.1
+    gate_per_entry: bool = False   # g [N, C, W]: one gate per write entry instead of one per token
 
     @property
     def steps(self) -> int:
@@ -139,7 +141,8 @@ def make_inputs(w: Workload, streams=None) -> dict:
     dt = np.uint16 if w.dv_dtype == "bf16" else np.float32
     k_val = np.empty((st, Ps, C, W), vt)
     q_val = np.empty((st, Ps, C, R), vt)
-    g = np.empty((st, Ps, C), np.float32)
+    gshape = (st, C, W) if w.gate_per_entry else (st, C)
+    g = np.empty((st, Ps) + gshape[1:], np.float32)
     dv = np.empty((st, Ps, C, hd), dt)
     cdf = _zipf_cdf(w.S, w.zipf_s) if w.idx == "zipf" else None
     for i, p in enumerate(streams):
@@ -153,7 +156,7 @@ def make_inputs(w: Workload, streams=None) -> dict:
             arr[:, i] = ids.astype(np.int32)
         k_val[:, i] = _vals(r_kv, (st, C, W), w.val_scale, w.val_dtype)
         q_val[:, i] = _vals(r_qv, (st, C, R), w.val_scale, w.val_dtype)
-        z = r_g.standard_normal((st, C)) + w.gate_mu
+        z = r_g.standard_normal(gshape) + w.gate_mu
         g[:, i] = (np.minimum(z, 0.0) - np.log1p(np.exp(-np.abs(z)))).astype(np.float32)
         dv[:, i] = _vals(r_dv, (st, C, hd), w.dv_scale, w.dv_dtype)
     if w.valid_last < C:   # the stream's end falls inside the last step's chunks
@@ -163,7 +166,7 @@ def make_inputs(w: Workload, streams=None) -> dict:
     return {
         "k_idx": k_idx.reshape(N, C, W), "q_idx": q_idx.reshape(N, C, R),
         "k_val": k_val.reshape(N, C, W), "q_val": q_val.reshape(N, C, R),
-        "g": g.reshape(N, C), "dv": dv.reshape(N * C, hd),
+        "g": g.reshape((N, C, W) if w.gate_per_entry else (N, C)), "dv": dv.reshape(N * C, hd),
         "streams": streams, "P": Ps, "steps": st, "valid_last": w.valid_last,
     }
 

@@ -57,15 +57,26 @@ def bf_peers(order, d):
     return sum(1 for i in same if i < r), sum(1 for i in same if i > r)
 
 
+def token_gate(k_idx, g, t, s):
+    """Token t's gate on slot s: g[t] (one gate per token), or with one gate per write entry
+    (g [C, W]) the gate of t's first write lane on s -- a later lane of t on s is a repeat and
+    adds nothing."""
+    if np.ndim(g) == 1:
+        return float(g[t])
+    first = min(a for a in range(k_idx.shape[1]) if int(k_idx[t, a]) == s)
+    return float(g[t, first])
+
+
 def token_G(k_idx, g, V):
-    """G[s][t] = sum of g over tokens t' <= t (t' < V) that write slot s (each token once)."""
+    """G[s][t] = sum of the gates of the tokens t' <= t (t' < V) that write slot s (each token once,
+    with its gate on s)."""
     C, W = k_idx.shape
     G = {}
     for s in set(int(x) for x in k_idx[:V].ravel()):
         run, col = 0.0, []
         for t in range(C):
             if t < V and s in set(int(x) for x in k_idx[t]):
-                run += float(g[t])
+                run += token_gate(k_idx, g, t, s)
             col.append(run)
         G[s] = col
     return G
@@ -75,14 +86,14 @@ def Gs(G, s, t):
     return G[s][t] if s in G else 0.0
 
 
-def random_chunk(rng, C, W, R, S, V):
+def random_chunk(rng, C, W, R, S, V, per_entry=False):
     k_idx = rng.integers(0, S, size=(C, W)).astype(np.int32)
     q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
     k_idx[V:] = -1
     q_idx[V:] = -1
     k_val = rng.standard_normal((C, W)).astype(np.float32)
     q_val = rng.standard_normal((C, R)).astype(np.float32)
-    z = rng.standard_normal(C) + 1.0
+    z = rng.standard_normal((C, W) if per_entry else C) + 1.0
     g = (np.minimum(z, 0) - np.log1p(np.exp(-np.abs(z)))).astype(np.float32)
     return k_idx, q_idx, k_val, q_val, g
 
@@ -90,6 +101,9 @@ def random_chunk(rng, C, W, R, S, V):
 CASES = [  # (C, W, R, S, V): small S gives collisions and repeated slots within a token
     (8, 3, 2, 5, 8), (8, 3, 2, 5, 6), (6, 4, 4, 3, 6), (10, 2, 3, 7, 4), (5, 1, 1, 2, 5), (7, 5, 1, 4, 7),
 ]
+# the same shapes with one gate per write entry (g [C, W]); the repeated slots within a token make
+# "which lane's gate" observable
+GATES = ["token", "entry"]
 
 
 def run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V, lib=None):
@@ -99,8 +113,9 @@ def run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V, lib=None):
 
 # ---------------------------------------------------------------- pins
 
-def test_hand_chunk_golden():
-    fx = json.load(open(os.path.join(HERE, "golden", "hand_chunk.json")))
+@pytest.mark.parametrize("fixture", ["hand_chunk.json", "hand_chunk_per_entry.json"])
+def test_hand_chunk_golden(fixture):
+    fx = json.load(open(os.path.join(HERE, "golden", fixture)))
     ev = lambda s: eval(s, {"exp": math.exp})  # noqa: E731  (expressions written in the fixture)
     k_idx = np.array(fx["k_idx"], np.int32)
     q_idx = np.array(fx["q_idx"], np.int32)
@@ -158,11 +173,12 @@ def test_sort_positions_and_rows_bruteforce(case):
     assert o["repeats"] == reps
 
 
+@pytest.mark.parametrize("gate", GATES)
 @pytest.mark.parametrize("case", CASES)
-def test_logs_rex_cpe_token_form(case):
+def test_logs_rex_cpe_token_form(case, gate):
     C, W, R, S, V = case
     rng = np.random.default_rng(1 + hash(case) % 2**32)
-    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V, per_entry=gate == "entry")
     o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V)
     G = token_G(k_idx, g, V)
     for t in range(C):
@@ -209,11 +225,12 @@ def bf_pairs(k_idx, q_idx, k_val, q_val, g, V):
     return A, QK
 
 
+@pytest.mark.parametrize("gate", GATES)
 @pytest.mark.parametrize("case", CASES)
-def test_pairs_bruteforce(case):
+def test_pairs_bruteforce(case, gate):
     C, W, R, S, V = case
     rng = np.random.default_rng(2 + hash(case) % 2**32)
-    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+    k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V, per_entry=gate == "entry")
     o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V)
     A, QK = bf_pairs(k_idx, q_idx, k_val, q_val, g, V)
     np.testing.assert_allclose(o["A"][0], A, rtol=1e-12, atol=1e-12)
@@ -224,13 +241,14 @@ def test_pairs_bruteforce(case):
 def token_recurrence(bank, k_idx, k_val, g, dv, V):
     for t in range(V):
         for s in set(int(x) for x in k_idx[t]):
-            bank[s] *= math.exp(float(g[t]))
+            bank[s] *= math.exp(token_gate(k_idx, g, t, s))
         for a in range(k_idx.shape[1]):
             bank[int(k_idx[t, a])] += float(k_val[t, a]) * dv[t]
 
 
+@pytest.mark.parametrize("gate", GATES)
 @pytest.mark.parametrize("case", CASES)
-def test_dw_token_recurrence(case):
+def test_dw_token_recurrence(case, gate):
     C, W, R, S, V = case
     hd = 4
     rng = np.random.default_rng(3 + hash(case) % 2**32)
@@ -238,7 +256,7 @@ def test_dw_token_recurrence(case):
     want = bank.copy()
     for step in range(3):   # a stream of three chunks, the last one ragged when V < C
         Vs = V if step == 2 else C
-        k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, Vs)
+        k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, Vs, per_entry=gate == "entry")
         dv = rng.standard_normal((C, hd)).astype(np.float32).astype(np.float64)
         oracle.dw_chunk(bank, k_idx, q_idx, k_val, q_val, g, dv, S=S, V=Vs, val_dtype="f32",
                         bank_dtype="f32", round_cpe=False, round_bank=False)
@@ -362,15 +380,26 @@ MUTATIONS = {
     "dw_rex_dropped": ("const double sc = ch.val[e] * exp(ch.rex[e])", "const double sc = ch.val[e]"),
     "after_count_off_by_one": ("ch->ka[e] = nk - kseen;", "ch->ka[e] = nk - kseen + 1;"),
     "group_total_drops_last": ("tot += xe;", "tot += (s + 1 < r1) ? xe : 0.0;"),
+    # per-entry gates: the gate of the token's last write lane (every entry reads lane W - 1) ...
+    "gate_lane_last": ("g[ch->tok[e] * g_width + ch->lane[e] * g_lane_stride]",
+                       "g[ch->tok[e] * g_width + (W - 1) * g_lane_stride]"),
+    # ... of lane 0 whatever the entry's lane ...
+    "gate_lane_zero": ("g[ch->tok[e] * g_width + ch->lane[e] * g_lane_stride]", "g[ch->tok[e] * g_width]"),
+    # ... or of a token's LAST write entry on the slot (the repeat rule looking forward, not back)
+    "gate_of_last_repeat": (
+        "const int prev_same = s > r && !ch->isq[ch->order[s - 1]] && ch->valid[ch->order[s - 1]] &&\n"
+        "                                      ch->tok[ch->order[s - 1]] == ch->tok[e];",
+        "const int prev_same = s + 1 < r1 && !ch->isq[ch->order[s + 1]] && ch->valid[ch->order[s + 1]] &&\n"
+        "                                      ch->tok[ch->order[s + 1]] == ch->tok[e];"),
 }
 
 
 def _pins_pass(lib):
     try:
-        for case in CASES[:4]:
+        for case, per_entry in [(c, pe) for c in CASES[:4] for pe in (False, True)]:
             C, W, R, S, V = case
             rng = np.random.default_rng(11 + hash(case) % 2**32)
-            k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V)
+            k_idx, q_idx, k_val, q_val, g = random_chunk(rng, C, W, R, S, V, per_entry=per_entry)
             o = run_oracle_chunk(k_idx, q_idx, k_val, q_val, g, S, V, lib=lib)
             A, QK = bf_pairs(k_idx, q_idx, k_val, q_val, g, V)
             if not (np.allclose(o["A"][0], A, 1e-12, 1e-12) and np.allclose(o["QK"][0], QK, 1e-12, 1e-12)):
