@@ -83,6 +83,15 @@ typedef struct {
     int32_t dv_dtype;       /* sdm_dtype of dv */
     int32_t bank_dtype;     /* sdm_dtype of the bank */
     int32_t gate_per_entry; /* 0: g [N, C]; 1: g [N, C, W] */
+    /* Launch geometry of the forward's kernels, 0 = chosen from the shape (the backward's entry
+     * points ignore both). Neither changes any output bit (every sum is taken in an order fixed by
+     * the input), only how the work is split:
+     *   dw_log_buckets 1..11 (<= ceil(log2 S)): the DW walk's hashed slot buckets per stream, 2^k
+     *                  (changes sdm_workspace_bytes);
+     *   p1_warps       the automatic count .. 32: warps of a Phase-1 block (extra warps hold
+     *                  padding entries; more shared memory per block). */
+    int32_t dw_log_buckets;
+    int32_t p1_warps;
 } sdm_shape;
 
 /*
@@ -219,8 +228,10 @@ sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const int32_t* k_id
  *     with SDM_ERR_WORKSPACE before any launch; use sdm_forward_chunks with a caller workspace.
  *   - status_out (nullable): one device int32 that receives the call's device status word
  *     (SDM_DEV_* bits, 0 = fine), copied on `stream` after the kernels.
- *   - The first call on a device looks up the scratch's device address (once per device, with
- *     that device current); make that first call before any stream capture.
+ *   - A call outside stream capture looks up the scratch's device address (with the calling
+ *     thread's current device), so a device context created again (after cudaDeviceReset) is
+ *     picked up; a call inside a stream capture reuses the address of the last call on that device
+ *     outside capture: make at least one call before any capture, and again after a device reset.
  *   - Every call shares the one scratch and clears its header first. Calls whose kernels overlap
  *     on the GPU (different streams, or concurrent host threads) race on it: serialize them.
  */

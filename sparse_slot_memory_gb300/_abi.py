@@ -24,7 +24,7 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 class Shape(ctypes.Structure):
     _fields_ = [("P", c_i32), ("C", c_i32), ("W", c_i32), ("R", c_i32), ("hd", c_i32), ("valid_last", c_i32),
                 ("steps", c_i64), ("S", c_i64), ("val_dtype", c_i32), ("dv_dtype", c_i32), ("bank_dtype", c_i32),
-                ("gate_per_entry", c_i32)]
+                ("gate_per_entry", c_i32), ("dw_log_buckets", c_i32), ("p1_warps", c_i32)]
 
 
 P1_FIELDS = ("log_k", "rex", "cpe", "k_eff", "is_last", "is_only", "pos_k", "log_q", "q_w", "pos_q", "q_last",

@@ -39,6 +39,9 @@ class ShapeSpec:
     dv_dtype: str = "bf16"
     bank_dtype: str = "bf16"
     gate_per_entry: bool = False
+    # launch geometry (0: chosen from the shape); neither changes any output bit
+    dw_log_buckets: int = 0
+    p1_warps: int = 0
 
     @property
     def N(self) -> int:
@@ -46,7 +49,8 @@ class ShapeSpec:
 
     def c(self) -> _abi.Shape:
         return _abi.Shape(self.P, self.C, self.W, self.R, self.hd, self.valid_last, self.steps, self.S,
-                          _DT[self.val_dtype], _DT[self.dv_dtype], _DT[self.bank_dtype], int(self.gate_per_entry))
+                          _DT[self.val_dtype], _DT[self.dv_dtype], _DT[self.bank_dtype], int(self.gate_per_entry),
+                          int(self.dw_log_buckets), int(self.p1_warps))
 
     @classmethod
     def from_workload(cls, w, P=None) -> "ShapeSpec":

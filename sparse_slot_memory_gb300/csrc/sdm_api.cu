@@ -2,6 +2,7 @@
 // workspace layout and the launches. Every check runs before any launch; nothing here allocates.
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "sdm_internal.cuh"
@@ -51,10 +52,14 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     int kb = 1;
     while ((int64_t(1) << kb) < s->S) ++kb;
     g->key_bits = kb;
-    g->passes = (kb + kMaxDigitBits - 1) / kMaxDigitBits;
-    g->digit_bits = (kb + g->passes - 1) / g->passes;
+    g->passes = (kb + kSortDigitBits - 1) / kSortDigitBits;
+    g->digit_bits = kSortDigitBits;
     int threads = static_cast<int>((n + kItems - 1) / kItems);
     threads = static_cast<int>(round_up(static_cast<size_t>(threads), 32));
+    if (s->p1_warps != 0) {   // a wider block: the extra warps hold padding entries
+        if (s->p1_warps < threads / 32 || s->p1_warps > kMaxThreads / 32) return SDM_ERR_SHAPE;
+        threads = s->p1_warps * 32;
+    }
     g->threads = threads;
     g->npad = threads * kItems;
     g->nwarps = threads / 32;
@@ -64,6 +69,10 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     int64_t want = kDwTargetItems / (static_cast<int64_t>(s->P) * g->nsl);
     int lb = 0;
     while ((int64_t(1) << lb) < want && lb < kMaxLogBuckets && lb < kb) ++lb;
+    if (s->dw_log_buckets != 0) {
+        if (s->dw_log_buckets < 1 || s->dw_log_buckets > kMaxLogBuckets || s->dw_log_buckets > kb) return SDM_ERR_SHAPE;
+        lb = s->dw_log_buckets;
+    }
     g->logB = lb;
     g->B = 1 << lb;
     // workspace: header | DW records [N, C*W] | bucket bounds [P, B + 1, steps]
@@ -100,20 +109,29 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_bcnt = off;
     off += round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16);
+    // The dense pair path keeps its groups' vectors (3 * C floats each, after kHotMax 16-byte
+    // descriptors) in the rex .. scratch region, free by then: the rex / cpe / write-row arrays, the
+    // bucket counters and kHotExtra bytes more. How many groups it takes must not depend on the
+    // launch geometry (the DW bucket count changes that region), or other geometries would round
+    // some A / QK cells differently: it is derived from the part every geometry has.
     g->sm_zero = off;
-    // the sort's digit counters [2^digit_bits][warps + 1] (uint16) reuse the position-pack region
-    // onwards, idle until the scans
-    g->sm_hist = g->sm_pos;
-    const size_t hist_end = g->sm_hist + round_up((size_t(1) << g->digit_bits) * (g->nwarps + 1) * 2, 16);
-    for (int zb : {kZeroBufBig, kZeroBufSmall}) {
-        size_t o = off + zb;
-        g->sm_scr = o;
-        o += 64 * 16 + 64 * 4;
-        if (hist_end > g->sm_scr) o += hist_end - g->sm_scr;
-        g->zero_bytes = zb;
-        g->smem_bytes = round_up(o, 128);
-        if (g->smem_bytes + 6144 <= kSmemOptin) break;   // room for the static arrays too
+    off += kHotExtra;
+    {
+        const size_t room = 3 * round_up(static_cast<size_t>(g->nk) * 4, 16) + kHotExtra - kHotMax * 16;
+        g->hot_cap = static_cast<int>(std::min<size_t>(kHotMax, room / (12 * static_cast<size_t>(g->C))));
     }
+    // the sort's words go back and forth between the log-cumsum and the position-pack regions (idle
+    // until the scans); its count table ([digit][32] warp counts and [digit] totals, uint32) reuses
+    // the write-before-count region when that is large enough, else it follows the scan scratch
+    const size_t tab_bytes = (kSortDigits * 32 + kSortDigits) * 4;
+    g->sm_scr = off;
+    off += 64 * 16 + 64 * 4;
+    g->sm_hist = g->sm_kb;
+    if (tab_bytes > np * 2) {
+        g->sm_hist = round_up(off, 16);
+        off = g->sm_hist + tab_bytes;
+    }
+    g->smem_bytes = round_up(off, 128);
     return SDM_OK;
 }
 
@@ -183,7 +201,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.sm_kslot = static_cast<uint32_t>(g.sm_kslot);
     a.sm_bcnt = static_cast<uint32_t>(g.sm_bcnt);
     a.sm_zero = static_cast<uint32_t>(g.sm_zero);
-    a.zero_bytes = g.zero_bytes;
+    a.hot_cap = g.hot_cap;
     a.sm_scr = static_cast<uint32_t>(g.sm_scr);
     const cudaError_t err =
         launch_phase1(a, s->val_dtype == SDM_BF16, ordinals, (e - b) * g.P, g.threads, g.smem_bytes, stream);
@@ -258,7 +276,8 @@ sdm_status check_smem(const Geometry& g) {
     if (cudaGetDevice(&dev) != cudaSuccess) return SDM_ERR_CUDA;
     size_t lim = 0;
     if (phase1_smem_limit(dev, &lim) != cudaSuccess) return SDM_ERR_CUDA;
-    return g.smem_bytes <= lim ? SDM_OK : SDM_ERR_SMEM;
+    // the kernel's static shared arrays (flag words, counters: under kP1StaticSmem) come on top
+    return g.smem_bytes + kP1StaticSmem <= lim ? SDM_OK : SDM_ERR_SMEM;
 }
 
 }  // namespace
@@ -380,20 +399,24 @@ extern "C" sdm_status sdm_forward_chunks_saving(const sdm_shape* shape, const in
 
 // ---- the no-allocation forward ----------------------------------------------------------------
 // Scratch for callers that cannot allocate device memory: a file-scope device array that every GPU
-// loading this library holds until the process exits. Its address is looked up once per device
-// (host code must not use the array's name as a device address) and then reused by every call.
+// loading this library holds until the process exits. Host code must not use the array's name as a
+// device address: its address is looked up with cudaGetSymbolAddress, on every call made outside a
+// stream capture (a device context created again after cudaDeviceReset gets a new address) and
+// remembered per device for calls made inside a capture.
 namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[SDM_NOALLOC_SCRATCH_BYTES];
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-sdm_status noalloc_scratch(void** out) {
+sdm_status noalloc_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SDM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SDM_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SDM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone || g_noalloc_ptr[dev] == nullptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SDM_ERR_CUDA;
         g_noalloc_ptr[dev] = p;
@@ -416,9 +439,9 @@ extern "C" sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const i
     if (!aligned16(dv) || !aligned16(bank)) return SDM_ERR_ALIGN;
     if (geo.ws_bytes > SDM_NOALLOC_SCRATCH_BYTES) return SDM_ERR_WORKSPACE;
     if ((st = check_smem(geo)) != SDM_OK) return st;
-    void* ws = nullptr;
-    if ((st = noalloc_scratch(&ws)) != SDM_OK) return st;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    if ((st = noalloc_scratch(cs, &ws)) != SDM_OK) return st;
     // the scratch keeps the previous call's bytes: the status word and the work counter restart at 0
     if (cudaMemsetAsync(ws, 0, kHdrBytes, cs) != cudaSuccess) return SDM_ERR_CUDA;
     if (step_begin < step_end) {

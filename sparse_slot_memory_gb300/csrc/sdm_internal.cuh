@@ -35,12 +35,18 @@ constexpr int kItems = 8;               // sorted positions per thread in the Ph
 constexpr int kMaxThreads = 1024;
 constexpr int kMaxRow = kItems * kMaxThreads;   // entries of one chunk held on chip
 constexpr uint32_t kKeyInvalid = 1u << 31;       // key word flag: not a valid entry
-constexpr int kMaxDigitBits = 8;                // radix digit of the Phase-1 sort
-// zero source of the A / QK bulk zero fill: 16 KB pieces where the chunk's shared memory has room,
-// else 4 KB; the pieces are issued in kZeroStages portions spread over the Phase-1 phases
-constexpr int kZeroBufBig = 16384;
-constexpr int kZeroBufSmall = 4096;
-constexpr int kZeroStages = 8;
+constexpr int kSortDigitBits = 4;               // radix digit of the Phase-1 sort
+constexpr int kSortDigits = 1 << kSortDigitBits;
+// a sort word between passes: the entry in the low kSortWordEntryBits bits (kMaxRow entries), the
+// key bits still to sort above it once they fit
+constexpr int kSortWordEntryBits = 13;
+constexpr uint32_t kSortWordEntryMask = (1u << kSortWordEntryBits) - 1u;
+constexpr int kSortWordKeyBits = 32 - kSortWordEntryBits;
+static_assert(kMaxRow <= (1 << kSortWordEntryBits), "a sort word holds an entry index");
+// bytes of the Phase-1 shared memory after the bucket counters, part of the dense pair path's room
+constexpr int kHotExtra = 4096;
+// bound on the Phase-1 kernel's static shared memory (its flag words and counters)
+constexpr size_t kP1StaticSmem = 6144;
 // dense pair path: slot groups with at least kHotMin write entries, at most kHotMax per chunk,
 // whose log-cumsums span at most kHotSpan
 constexpr uint32_t kHotMin = 16;
@@ -86,7 +92,7 @@ struct Geometry {
     int maxL;              // long groups per chunk at most: max(1, C*W / kLongMin)
     int rstride;           // records per chunk: C*W + maxL (a long group adds its reference record)
     size_t smem_bytes;
-    int zero_bytes;        // bulk zero-fill piece (and zero buffer) size
+    int hot_cap;           // dense pair groups per chunk at most (from the shape alone)
     // Phase-1 shared-memory carve (byte offsets)
     size_t sm_keys, sm_vals, sm_sidx, sm_regd, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt,
         sm_zero, sm_scr;
@@ -116,7 +122,7 @@ struct P1Args {
     uint32_t w_magic, r_magic;   // the same for W and R (entry-order output index -> token)
     int P, logB;
     int64_t steps;
-    int zero_bytes;         // bulk zero-fill piece size (the zero buffer's size)
+    int hot_cap;            // dense pair groups per chunk at most
     uint32_t sm_keys, sm_vals, sm_sidx, sm_pong, sm_hist, sm_pos, sm_kb, sm_rex, sm_tot, sm_kslot, sm_bcnt, sm_zero,
         sm_scr, sm_lv;
 };

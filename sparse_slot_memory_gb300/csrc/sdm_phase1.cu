@@ -12,18 +12,21 @@
 // GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
 // memory from load to the last output byte:
 //   0. load ids and values (coalesced) into entry-indexed arrays;
-//   1. stable LSD radix sort of entry indices by slot in passes of up to 8-bit digits (three passes
-//      for 2^20 slots): warps rank their 256 positions (lanes of equal digit found with one ballot
-//      per digit bit) against per-warp 16-bit digit counters (padded rows: conflict-free), one
-//      block scan of the counters, one scatter (no global round trips, no merge);
+//   1. stable LSD radix sort of entry indices by slot in 4-bit digits (five passes for 2^20 slots):
+//      each lane ranks its 8 consecutive positions with digit counters in registers, one warp scan
+//      of the byte-packed counts and one block scan of the per-warp totals place them, one scatter
+//      moves a word holding the entry and the key bits still to sort (no ballots, no shared
+//      counters per item, no key gathers after the first pass, no global round trips, no merge);
 //   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
 //      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
 //      the sorted rows in sorted order, then the DW records partitioned into hashed slot buckets;
-//   3. every entry-order output written from shared memory by consecutive threads;
-//   4. pair triangles: A and QK are zero-filled by TMA bulk stores issued at the start (they drain
-//      while the sort and scans compute); then one warp per (row, triangle) walks: 32
-//      earlier positions per step, lanes of one cell summed by a fixed shuffle tree, one lane adds
-//      the cell's partial to the warp's row buffer; only rows with terms are rewritten.
+//   3. every entry-order output written from shared memory by consecutive threads (4 entries per
+//      thread, vector loads and stores, when W and R are multiples of 4);
+//   4. pair triangles: A and QK are zero-filled by 16-byte streaming stores of every thread, a few
+//      at each phase boundary (they drain while the sort and scans compute); then one warp per
+//      (row, triangle) walks: 32 earlier positions per step, lanes of one cell summed by a fixed
+//      shuffle tree, one lane adds the cell's partial to the warp's row buffer; only rows with
+//      terms are rewritten.
 #include <cuda_bf16.h>
 
 #include "sdm_internal.cuh"
@@ -42,11 +45,6 @@ __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
 __device__ __forceinline__ uint32_t lanemask_le() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_le;" : "=r"(m));
@@ -230,17 +228,6 @@ __device__ __noinline__ void block_exscan_padded(T* a, int cnt, int group, uint3
     }
 }
 
-// TMA bulk store (shared -> global) of `bytes` (a multiple of 16; both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(ssrc));
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(s), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 // A / QK of chunk c set to zero by the block with plain stores (the triangles are not a whole
 // number of 16-byte units, so the TMA bulk fill does not apply). Out of line: rarely used.
 __device__ __noinline__ void zero_triangles(float* A, float* QK, int64_t c, int64_t cells) {
@@ -257,6 +244,32 @@ __device__ __forceinline__ void st_stream(T* p, T v) {
     __stcs(p, v);
 }
 
+// Four consecutive values of the value type: loaded from shared memory as one vector (8 bytes for
+// bfloat16, 16 for float32), stored to global memory as one streaming vector store.
+__device__ __forceinline__ void ld4(const float* p, float (&v)[4]) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+__device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(x.x << 16); v[1] = __uint_as_float(x.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(x.y << 16); v[3] = __uint_as_float(x.y & 0xFFFF0000u);
+}
+__device__ __forceinline__ void st4(float* p, const float (&v)[4]) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&v)[4]) {
+    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
+                        static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16;
+    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2]))) |
+                        static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[3]))) << 16;
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(lo, hi));
+}
+// Four int8 flags packed into one 4-byte streaming store.
+__device__ __forceinline__ void st4_flags(int8_t* p, uint32_t f0, uint32_t f1, uint32_t f2, uint32_t f3) {
+    __stcs(reinterpret_cast<uint32_t*>(p), f0 | f1 << 8 | f2 << 16 | f3 << 24);
+}
+
 // ORD: the saving forward's Phase 1 -- each group's FIRST record also carries its dense ordinal
 // and out.ngroups is written (a separate instantiation: the plain forward's kernel is unchanged)
 template <typename ValT, bool ORD>
@@ -265,8 +278,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     uint32_t* const keys = reinterpret_cast<uint32_t*>(smem + a.sm_keys);   // entry -> key word
     ValT* const vals = reinterpret_cast<ValT*>(smem + a.sm_vals);          // entry -> value
     uint16_t* const sidx = reinterpret_cast<uint16_t*>(smem + a.sm_sidx);  // sorted position -> entry
-    uint16_t* const pong = reinterpret_cast<uint16_t*>(smem + a.sm_pong);
-    uint16_t* const hist = reinterpret_cast<uint16_t*>(smem + a.sm_hist);   // [digit][warp + 1 pad]
     float* const lv = reinterpret_cast<float*>(smem + a.sm_lv);            // entry -> log-cumsum
     uint32_t* const posv = reinterpret_cast<uint32_t*>(smem + a.sm_pos);   // entry -> position pack
     uint16_t* const kbv = reinterpret_cast<uint16_t*>(smem + a.sm_kb);     // entry -> K entries before
@@ -310,15 +321,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // use by the sort's barriers
     const int nbk = 1 << a.logB;
     for (int b = tid; b < 2 * nbk + 1; b += nthr) bcnt[b] = 0u;
-    // A and QK start as zeros written by the TMA engine from a zeroed shared buffer (when the chunk's
-    // triangles are a whole number of 16-byte units); the rows with terms are rewritten at the end.
+    // A and QK start as zeros (16-byte stores spread over the phases when the chunk's triangles are
+    // a whole number of 16-byte units, else plain stores at the start); rows with terms are
+    // rewritten at the end.
     const int64_t cells = static_cast<int64_t>(a.C) * a.C;
     const bool bulk_zero = (cells & 3) == 0 && (a.out.A != nullptr || a.out.QK != nullptr);
-    uint4* const zbuf = reinterpret_cast<uint4*>(smem + a.sm_zero);
-    if (bulk_zero) {
-        for (int i = tid; i < a.zero_bytes / 16; i += nthr) zbuf[i] = make_uint4(0u, 0u, 0u, 0u);
-        fence_async_shared();   // the zeros are visible to the bulk copies issued after the next barrier
-    }
     auto bucket_of = [&](uint32_t key) -> uint32_t {
         return a.logB == 0 ? 0u : (key * 0x9E3779B1u) >> (32 - a.logB);
     };
@@ -383,94 +390,181 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     }
     if (!bulk_zero && (a.out.A != nullptr || a.out.QK != nullptr)) zero_triangles(a.out.A, a.out.QK, c, cells);
     __syncthreads();
-    // The zero pieces of both triangles go out in kZeroStages portions, one at the start of each
-    // phase (issued by the lanes of warp 0): issuing them all at once stalls warp 0, and with it
-    // the block, until the store engine has taken most of them.
-    int zero_next = 0;   // the next portion to issue (warp 0)
-    auto zero_upto = [&](int k) {
-        if (!bulk_zero || warp != 0) return;
-        const int64_t bytes = cells * 4, zb = a.zero_bytes;
-        const int64_t pieces = (bytes + zb - 1) / zb;
-        for (; zero_next <= k; ++zero_next) {
-            const int64_t i0 = 2 * pieces * zero_next / kZeroStages, i1 = 2 * pieces * (zero_next + 1) / kZeroStages;
-            for (int64_t i = i0 + lane; i < i1; i += 32) {
-                const int m = i < pieces ? 0 : 1;
-                float* const mat = m == 0 ? a.out.A : a.out.QK;
-                if (mat == nullptr) continue;
-                const int64_t o = (i - m * pieces) * zb;
-                bulk_store(reinterpret_cast<char*>(mat + c * cells) + o, zbuf,
-                           static_cast<uint32_t>(bytes - o < zb ? bytes - o : zb));
-            }
-            bulk_commit();
+    // A and QK of the chunk start as zeros written by every thread with 16-byte streaming stores, a
+    // few per thread at each phase boundary below (spread over the kernel, the stores drain while
+    // the block computes); rows with terms are written again in phase 4, after a block barrier.
+    const int zunits = bulk_zero ? static_cast<int>(cells / 2) : 0;   // float4 units of both triangles
+    const int zper = (zunits + nthr - 1) / nthr;
+    int zero_next = 0;   // this thread's next unit
+    auto zero_tick = [&](int most, bool flush = false) {
+        const int stop = flush ? zper : min(zper, zero_next + most);
+        for (; zero_next < stop; ++zero_next) {
+            const int u = zero_next * nthr + tid;
+            if (u >= zunits) break;
+            const int mi = u < zunits / 2 ? 0 : 1;
+            float* const mat = mi == 0 ? a.out.A : a.out.QK;
+            if (mat != nullptr)
+                __stcs(reinterpret_cast<float4*>(mat + c * cells) + (u - mi * (zunits / 2)), make_float4(0.f, 0.f, 0.f, 0.f));
         }
     };
-    zero_upto(0);
+    zero_tick(2);
 
-    // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits) ---------------------
+    // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits), 4-bit digits -------
+    // Every lane ranks its kItems consecutive positions (p0 = tid * kItems ...) with lane-private
+    // digit counters held in registers (16 nibbles of one 64-bit word). A warp scan of the
+    // byte-packed counts gives each lane the count of every digit over the warp's earlier lanes;
+    // one block scan of the [digit][warp] totals gives each warp its digit bases. Positions follow
+    // (digit, warp, lane, item) order, which within a digit is the position order: the sort is
+    // stable. No ballots, no shared counters per item. Between passes a position holds a word: the
+    // entry (13 bits) and, once they fit in the other 19, the key bits still to sort, so later
+    // passes read their digits with the word instead of gathering the entry's key.
     {
-        const uint32_t lt = lanemask_lt();
+        uint32_t* const tab = reinterpret_cast<uint32_t*>(smem + a.sm_hist);   // [digit][32]: warp counts
+        uint32_t* const dtot = tab + kSortDigits * 32;                          // [digit]: block totals
+        uint32_t* const wa = reinterpret_cast<uint32_t*>(smem + a.sm_pong);     // words after even passes
+        uint32_t* const wb = reinterpret_cast<uint32_t*>(smem + a.sm_pos);      // words after odd passes
+        const int p0 = tid * kItems;
+        auto sel4 = [](const uint32_t (&w)[4], uint32_t i) -> uint32_t {
+            return (i & 2u) ? ((i & 1u) ? w[3] : w[2]) : ((i & 1u) ? w[1] : w[0]);
+        };
+#pragma unroll 1
         for (int pass = 0; pass < a.passes; ++pass) {
-            const int sh = pass * a.digit_bits;
-            const int nb = min(a.digit_bits, a.key_bits - sh);
-            const int nbins = 1 << nb;
-            const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-            // the last pass writes sidx
-            uint16_t* const dst = ((a.passes - 1 - pass) & 1) ? pong : sidx;
-            const uint16_t* const src = ((a.passes - pass) & 1) ? pong : sidx;
-            const int hs = nw + 1;   // padded row: lanes of different digits fall in different banks
-            {
-                uint32_t* const h32 = reinterpret_cast<uint32_t*>(hist);
-                for (int i = tid; i < (nbins * hs + 1) / 2; i += nthr) h32[i] = 0u;
-            }
-            __syncthreads();
-            if (pass < 3) zero_upto(1 + pass);
-            uint32_t mer[kItems];   // entry | rank among the warp's equal digits << 13 | digit << 21
-            // Not unrolled (code size): each item's word enters at the top of mer[], which shifts down
-            // one place per iteration, so after kItems iterations mer[k] is item k's.
-#pragma unroll 1
-            for (int k = 0; k < kItems; ++k) {
-                const int p = warp * (32 * kItems) + k * 32 + lane;
-                const uint32_t e = pass == 0 ? static_cast<uint32_t>(p) : src[p];
-                const uint32_t d = (keys[e] >> sh) & dmask;
-                // lanes holding the same digit: one ballot per digit bit
-                uint32_t peers = kFull;
-#pragma unroll 1
-                for (int bit = 0; bit < nb; ++bit) {
-                    const bool on = (d >> bit) & 1u;
-                    const uint32_t bal = __ballot_sync(kFull, on);
-                    peers &= on ? bal : ~bal;
+            const int sh = pass * kSortDigitBits;
+            const int left = a.key_bits - sh - kSortDigitBits;   // key bits still to sort after this pass
+            const uint32_t dmask = (1u << min(kSortDigitBits, a.key_bits - sh)) - 1u;
+            const bool last = pass == a.passes - 1;              // the last pass writes sidx
+            const bool src_packed = a.key_bits - sh <= kSortWordKeyBits;
+            const bool dst_packed = left <= kSortWordKeyBits;
+            const uint32_t rmask = left > 0 ? (1u << left) - 1u : 0u;
+            const uint32_t* const src = (pass & 1) ? wa : wb;
+            uint32_t* const dst = (pass & 1) ? wb : wa;
+            zero_tick(2);
+            uint32_t kr[kItems];   // the entries' key bits sh and up
+            uint32_t wv[kItems];   // the entries (low 13 bits of the words)
+            if (pass == 0) {
+                const uint4 k0 = *reinterpret_cast<const uint4*>(keys + p0);
+                const uint4 k1 = *reinterpret_cast<const uint4*>(keys + p0 + 4);
+                kr[0] = k0.x; kr[1] = k0.y; kr[2] = k0.z; kr[3] = k0.w;
+                kr[4] = k1.x; kr[5] = k1.y; kr[6] = k1.z; kr[7] = k1.w;
+#pragma unroll
+                for (int k = 0; k < kItems; ++k) wv[k] = static_cast<uint32_t>(p0 + k);
+            } else {
+                const uint4 v0 = *reinterpret_cast<const uint4*>(src + p0);
+                const uint4 v1 = *reinterpret_cast<const uint4*>(src + p0 + 4);
+                wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
+                wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+#pragma unroll
+                for (int k = 0; k < kItems; ++k) {
+                    kr[k] = src_packed ? wv[k] >> kSortWordEntryBits : keys[wv[k] & kSortWordEntryMask] >> sh;
+                    wv[k] &= kSortWordEntryMask;
                 }
-                const uint32_t rin = __popc(peers & lt);
-                uint16_t* const h = hist + d * hs + warp;
-                const uint32_t base = *h;
-                __syncwarp();
-                if (rin == 0) *h = static_cast<uint16_t>(base + __popc(peers));
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < kItems - 1; ++q) mer[q] = mer[q + 1];
-                mer[kItems - 1] = e | (base + rin) << 13 | d << 21;   // entry | rank (< 256) | digit
             }
-            __syncthreads();
-            block_exscan_padded(hist, nbins * nw, nw, uscr, lane, warp, nw);
-            __syncthreads();
+            // digit d's count among the lane's items so far: nibble d & 7 of clo (d < 8) or chi
+            uint32_t clo = 0u, chi = 0u;
+            uint32_t dr[2] = {0u, 0u};   // per item: digit | rank among the lane's equal digits << 4 (a byte)
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
-                const uint32_t e = mer[k] & 0x1FFFu;
-                dst[hist[(mer[k] >> 21) * hs + warp] + ((mer[k] >> 13) & 0xFFu)] = static_cast<uint16_t>(e);
+                const uint32_t d = kr[k] & dmask;
+                const uint32_t s4 = (d & 7u) << 2;
+                const bool hi = d >= 8u;
+                const uint32_t r = ((hi ? chi : clo) >> s4) & 15u;
+                const uint32_t one = 1u << s4;
+                clo += hi ? 0u : one;
+                chi += hi ? one : 0u;
+                dr[k >> 2] |= (d | r << 4) << (8 * (k & 3));
+                // the word this position moves: the entry and, packed, the key bits after this digit
+                if (!last && dst_packed) wv[k] |= ((kr[k] >> kSortDigitBits) & rmask) << kSortWordEntryBits;
+            }
+            const uint64_t cnt = static_cast<uint64_t>(chi) << 32 | clo;
+            // the counts as bytes (digits 4j .. 4j+3 in word j), then their inclusive scan over the
+            // lanes: a byte never carries below lane 31 (at most 31 * kItems = 248)
+            auto bytes_of = [&](int j) -> uint32_t {   // digits 4j .. 4j+3 of cnt, one per byte
+                uint32_t t = static_cast<uint32_t>(cnt >> (16 * j)) & 0xFFFFu;
+                t = (t | (t << 8)) & 0x00FF00FFu;
+                return (t | (t << 4)) & 0x0F0F0F0Fu;
+            };
+            uint32_t inc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) inc[j] = bytes_of(j);
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t y = __shfl_up_sync(kFull, inc[j], dd);
+                    if (lane >= dd) inc[j] += y;
+                }
+            }
+            // exclusive counts (the word subtraction is exact: every true byte lies in 0 .. 248)
+            uint32_t exl[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) exl[j] = inc[j] - bytes_of(j);
+            {   // the warp's count of each digit, from lane 31: lane d < 16 stores digit d's
+                uint32_t xs[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xs[j] = __shfl_sync(kFull, exl[j], 31);
+                const uint32_t clo = __shfl_sync(kFull, static_cast<uint32_t>(cnt), 31);
+                const uint32_t chi = __shfl_sync(kFull, static_cast<uint32_t>(cnt >> 32), 31);
+                if (lane < kSortDigits) {
+                    const uint32_t u = static_cast<uint32_t>(lane);
+                    const uint32_t cw = u < 8u ? clo : chi;
+                    tab[lane * 32 + warp] = __byte_perm(sel4(xs, u >> 2), 0u, 0x4440u | (u & 3u)) +
+                                            ((cw >> (4u * (u & 7u))) & 15u);
+                }
             }
             __syncthreads();
-        }
-        if (a.passes == 0) {
-            for (int p = tid; p < npad; p += nthr) sidx[p] = static_cast<uint16_t>(p);
+            zero_tick(2);
+            // block scan of the counts in (digit, warp) order: warp d scans digit d over the warps
+            for (int d = warp; d < kSortDigits; d += nw) {
+                const uint32_t v = lane < nw ? tab[d * 32 + lane] : 0u;
+                uint32_t x = v;
+#pragma unroll
+                for (int dd = 1; dd < 32; dd <<= 1) {
+                    const uint32_t y = __shfl_up_sync(kFull, x, dd);
+                    if (lane >= dd) x += y;
+                }
+                if (lane < nw) tab[d * 32 + lane] = x - v;
+                if (lane == 31) dtot[d] = x;
+            }
+            __syncthreads();
+            zero_tick(2);
+            // lane d < 16: this warp's first position of digit d (earlier digits, then earlier warps)
+            uint32_t bd;
+            {
+                const uint32_t t = lane < kSortDigits ? dtot[lane] : 0u;
+                uint32_t x = t;
+#pragma unroll
+                for (int dd = 1; dd < kSortDigits; dd <<= 1) {
+                    const uint32_t y = __shfl_up_sync(kFull, x, dd);
+                    if (lane >= dd) x += y;
+                }
+                bd = lane < kSortDigits ? x - t + tab[lane * 32 + warp] : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const uint32_t b = (dr[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+                const uint32_t d = b & 15u;
+                const uint32_t pos = __shfl_sync(kFull, bd, static_cast<int>(d)) +
+                                     __byte_perm(sel4(exl, d >> 2), 0u, 0x4440u | (d & 3u)) + (b >> 4);
+                if (pos < static_cast<uint32_t>(npad)) {
+                    if (last)
+                        sidx[pos] = static_cast<uint16_t>(wv[k]);
+                    else
+                        dst[pos] = wv[k];
+                }
+            }
             __syncthreads();
         }
     }
 
     // ---- 2. segmented scans over the sorted row -------------------------------------------------
     const int r0 = tid * kItems;
-    uint32_t ke[kItems];   // entry at each of this thread's sorted positions
+    uint32_t ke[kItems];   // entry at each of this thread's sorted positions (one 16-byte load)
+    {
+        const uint4 v = *reinterpret_cast<const uint4*>(sidx + r0);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < kItems; ++k) ke[k] = sidx[r0 + k];
+        for (int k = 0; k < kItems; ++k) ke[k] = (w4[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+    }
     auto tok_of = [&](uint32_t e) { return __umulhi(e, a.wr_magic); };
     auto is_q_of = [&](uint32_t e) { return static_cast<int>(e - tok_of(e) * wr) >= W; };
     // head / tail bits, gates (a token's repeated write entry of a group adds 0)
@@ -528,7 +622,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
-        zero_upto(4);
+        zero_tick(2);
         // Not unrolled (code size): item k's gate and entry are taken from the bottom of x[] / ke[],
         // which shift down one place per iteration (after kItems shifts they are back in order).
 #pragma unroll 1
@@ -574,7 +668,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == kItems - 1 ? it : bcomb(agg, it);
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
-        zero_upto(5);
+        zero_tick(2);
         const int64_t kbase = c * nk, qbase = c * nq;
         // Not unrolled (the body is large): item k's gate and entry are taken from the top of
         // x[] / ke[], which shift up one place per iteration (register moves, no local memory).
@@ -651,7 +745,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         uint32_t* const fill = bcnt + B + 1; // [B]
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
-        zero_upto(6);
+        zero_tick(2);
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
         // a warp takes 32 consecutive write-row positions
@@ -727,49 +821,103 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 3. entry-order outputs -------------------------------------------------------------------
     {
-        zero_upto(kZeroStages - 1);
+        zero_tick(2);
         const int64_t kbase = c * nk;
         ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
         ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);
-        for (int o = tid; o < nk; o += nthr) {
-            const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.w_magic)), e = t * wr + (o - t * W);
-            const uint32_t pk = posv[e];
-            const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
-            const bool valid = size != 0u;
-            const float lg = lv[e];
-            if (a.out.log_k) st_stream(a.out.log_k + kbase + o, lg);
-            if (a.out.rex) st_stream(a.out.rex + kbase + o, rexv[o]);
-            if (cpe_o) st_stream(cpe_o + kbase + o, from_f<ValT>(cpev[o]));
-            if (keff_o) st_stream(keff_o + kbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
-            if (a.out.is_last)
-                st_stream(a.out.is_last + kbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
-            if (a.out.is_only) st_stream(a.out.is_only + kbase + o, static_cast<int8_t>(size == 1u));
-            if (a.out.pos_k) st_stream(a.out.pos_k + kbase + o, static_cast<int32_t>(pk));
-        }
         const int64_t qbase = c * nq;
         ValT* const qw_o = static_cast<ValT*>(a.out.q_w);
-        for (int o = tid; o < nq; o += nthr) {
-            const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
-            const uint32_t pk = posv[e];
-            const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
-            const bool valid = size != 0u;
-            const float lg = lv[e];
-            if (a.out.log_q) st_stream(a.out.log_q + qbase + o, lg);
-            if (qw_o) st_stream(qw_o + qbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
-            if (a.out.q_last)
-                st_stream(a.out.q_last + qbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
-            if (a.out.q_only) st_stream(a.out.q_only + qbase + o, static_cast<int8_t>(size == 1u));
-            if (a.out.pos_q) st_stream(a.out.pos_q + qbase + o, static_cast<int32_t>(pk));
+        if ((W & 3) == 0 && (R & 3) == 0) {
+            // four consecutive entries of one token per thread: vector loads from shared memory
+            // (their entry indices are consecutive and a multiple of 4) and vector stores
+            for (int o = 4 * tid; o < nk; o += 4 * nthr) {
+                const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.w_magic)), e = t * wr + (o - t * W);
+                const uint4 pk = *reinterpret_cast<const uint4*>(posv + e);
+                float lg[4], v[4];
+                ld4(lv + e, lg);
+                const uint32_t p4[4] = {pk.x, pk.y, pk.z, pk.w};
+                if (a.out.log_k) st4(a.out.log_k + kbase + o, lg);
+                if (a.out.rex) {
+                    float r4[4];
+                    ld4(rexv + o, r4);
+                    st4(a.out.rex + kbase + o, r4);
+                }
+                if (cpe_o) {
+                    float c4[4];
+                    ld4(cpev + o, c4);
+                    st4(cpe_o + kbase + o, c4);
+                }
+                if (keff_o) {
+                    ld4(vals + e, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = ((p4[q] >> kPosSizeShift) & kPosCountMax) != 0u ? v[q] * expf(lg[q]) : 0.f;
+                    st4(keff_o + kbase + o, v);
+                }
+                auto last = [&](int q) -> uint32_t {
+                    return ((p4[q] >> kPosSizeShift) & kPosCountMax) != 0u && ((p4[q] >> kPosAfterShift) & kPosCountMax) == 0u;
+                };
+                auto only = [&](int q) -> uint32_t { return ((p4[q] >> kPosSizeShift) & kPosCountMax) == 1u; };
+                if (a.out.is_last) st4_flags(a.out.is_last + kbase + o, last(0), last(1), last(2), last(3));
+                if (a.out.is_only) st4_flags(a.out.is_only + kbase + o, only(0), only(1), only(2), only(3));
+                if (a.out.pos_k) __stcs(reinterpret_cast<uint4*>(a.out.pos_k + kbase + o), pk);
+            }
+            for (int o = 4 * tid; o < nq; o += 4 * nthr) {
+                const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
+                const uint4 pk = *reinterpret_cast<const uint4*>(posv + e);
+                float lg[4], v[4];
+                ld4(lv + e, lg);
+                const uint32_t p4[4] = {pk.x, pk.y, pk.z, pk.w};
+                if (a.out.log_q) st4(a.out.log_q + qbase + o, lg);
+                if (qw_o) {
+                    ld4(vals + e, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = ((p4[q] >> kPosSizeShift) & kPosCountMax) != 0u ? v[q] * expf(lg[q]) : 0.f;
+                    st4(qw_o + qbase + o, v);
+                }
+                auto last = [&](int q) -> uint32_t {
+                    return ((p4[q] >> kPosSizeShift) & kPosCountMax) != 0u && ((p4[q] >> kPosAfterShift) & kPosCountMax) == 0u;
+                };
+                auto only = [&](int q) -> uint32_t { return ((p4[q] >> kPosSizeShift) & kPosCountMax) == 1u; };
+                if (a.out.q_last) st4_flags(a.out.q_last + qbase + o, last(0), last(1), last(2), last(3));
+                if (a.out.q_only) st4_flags(a.out.q_only + qbase + o, only(0), only(1), only(2), only(3));
+                if (a.out.pos_q) __stcs(reinterpret_cast<uint4*>(a.out.pos_q + qbase + o), pk);
+            }
+        } else {
+            for (int o = tid; o < nk; o += nthr) {
+                const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.w_magic)), e = t * wr + (o - t * W);
+                const uint32_t pk = posv[e];
+                const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
+                const bool valid = size != 0u;
+                const float lg = lv[e];
+                if (a.out.log_k) st_stream(a.out.log_k + kbase + o, lg);
+                if (a.out.rex) st_stream(a.out.rex + kbase + o, rexv[o]);
+                if (cpe_o) st_stream(cpe_o + kbase + o, from_f<ValT>(cpev[o]));
+                if (keff_o) st_stream(keff_o + kbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
+                if (a.out.is_last)
+                    st_stream(a.out.is_last + kbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
+                if (a.out.is_only) st_stream(a.out.is_only + kbase + o, static_cast<int8_t>(size == 1u));
+                if (a.out.pos_k) st_stream(a.out.pos_k + kbase + o, static_cast<int32_t>(pk));
+            }
+            for (int o = tid; o < nq; o += nthr) {
+                const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
+                const uint32_t pk = posv[e];
+                const uint32_t size = (pk >> kPosSizeShift) & kPosCountMax;
+                const bool valid = size != 0u;
+                const float lg = lv[e];
+                if (a.out.log_q) st_stream(a.out.log_q + qbase + o, lg);
+                if (qw_o) st_stream(qw_o + qbase + o, from_f<ValT>(valid ? to_f(vals[e]) * expf(lg) : 0.f));
+                if (a.out.q_last)
+                    st_stream(a.out.q_last + qbase + o, static_cast<int8_t>(valid && ((pk >> kPosAfterShift) & kPosCountMax) == 0u));
+                if (a.out.q_only) st_stream(a.out.q_only + qbase + o, static_cast<int8_t>(size == 1u));
+                if (a.out.pos_q) st_stream(a.out.pos_q + qbase + o, static_cast<int32_t>(pk));
+            }
         }
     }
 
     // ---- 4. pair triangles --------------------------------------------------------------------------
     if (tid == 0) a.lcnt[c] = static_cast<int32_t>(lcnt_s);   // final since the DW split's barrier
     if (a.out.A == nullptr && a.out.QK == nullptr) return;
-    if (bulk_zero && warp == 0) {
-        bulk_wait_all();        // this lane's zero pieces are written (and the zero buffer is no longer read)
-        fence_async_global();   // ... and ordered before the generic stores of the rows below
-    }
+    zero_tick(0, true);   // the zeros not yet stored; the barrier orders them before the rows' stores
     __syncthreads();   // the key array becomes the row buffers
     float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
     const uint32_t le = lanemask_le();
@@ -789,10 +937,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         int r0, r1, ok;
         float ref;
     };
+    static_assert(sizeof(HotMeta) == 16, "the host sizes the dense path's region with 16-byte descriptors");
     HotMeta* const meta = reinterpret_cast<HotMeta*>(smem + a.sm_rex);   // rex .. zero buffer: free now
     float* const hvec = reinterpret_cast<float*>(smem + a.sm_rex + kHotMax * sizeof(HotMeta));
-    const int hot_cap = min(kHotMax, (static_cast<int>(a.sm_scr - a.sm_rex) - kHotMax * static_cast<int>(sizeof(HotMeta))) /
-                                         (12 * C));
+    const int hot_cap = a.hot_cap;   // from the shape alone: the same groups go dense for any geometry
     if (warp == 0) {   // the first hot_cap candidates in position order
         const int nwords = npad >> 5;
         uint32_t cnt = 0;

@@ -48,6 +48,11 @@ def test_workspace_bytes(lib):
     assert lib.sdm_workspace_bytes(ctypes.byref(shape(W=17, R=16))) == 0   # C * (W + R) > 8192
     assert lib.sdm_workspace_bytes(ctypes.byref(shape(hd=6))) == 0
     assert lib.sdm_workspace_bytes(None) == 0
+    # the DW bucket count is part of the workspace layout (its per-step bucket bounds)
+    b3 = lib.sdm_workspace_bytes(ctypes.byref(shape(dw_log_buckets=3)))
+    b11 = lib.sdm_workspace_bytes(ctypes.byref(shape(dw_log_buckets=11)))
+    assert 0 < b3 < b11
+    assert lib.sdm_workspace_bytes(ctypes.byref(shape(p1_warps=32))) == n
 
 
 FAKE = 0x100000  # never dereferenced: every case fails a host check first
@@ -57,7 +62,8 @@ FAKE = 0x100000  # never dereferenced: every case fails a host check first
     (dict(C=0), -2), (dict(C=300), -2), (dict(W=0), -2), (dict(R=300), -2), (dict(W=20, R=20), -2),
     (dict(valid_last=0), -2), (dict(valid_last=257), -2), (dict(steps=0), -2), (dict(S=0), -2),
     (dict(S=1 << 31), -2), (dict(val_dtype=7), -3), (dict(bank_dtype=-1), -3), (dict(hd=126), -4),
-    (dict(gate_per_entry=2), -2),
+    (dict(gate_per_entry=2), -2), (dict(dw_log_buckets=12), -2), (dict(dw_log_buckets=-1), -2),
+    (dict(S=16, dw_log_buckets=5), -2), (dict(p1_warps=33), -2), (dict(p1_warps=31), -2),
 ])
 def test_shape_errors(lib, kw, code):
     st = lib.sdm_phase1(ctypes.byref(shape(**kw)), FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 1, FAKE, 1 << 40, None)
