@@ -10,7 +10,8 @@ import torch
 
 import oracle
 import sparse_slot_memory_gb300 as sdm
-from sdm_testlib import compare_p1, host, inputs_to_dev, ulp_bf16
+from oracle import bounds
+from sdm_testlib import BankStats, compare_p1, host, inputs_to_dev
 from synth import WORKLOADS, bf16_bits_to_f32, make_bank_stream, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -65,24 +66,23 @@ def test_fullsize_sampled_parity(name):
                             valid_last=w.valid_last)
         compare_p1({k: v[c:c + 1] for k, v in out.items() if k != "repeats"}, orc, 0, 1, w.val_dtype)
 
-    # DW: the sampled stream's whole bank after every step
+    # DW: the sampled stream's whole bank after every step, against the carried rounding intervals
     slots, xs = _stream_compact(w, x, p_chk)
     ref = init_p[slots].astype(np.float64)
-    alt, amb, touched, mag = oracle.dw_stream(ref, xs, p_chk, S=len(slots), C=w.C, P=P, steps=w.steps,
-                                              valid_last=w.valid_last, val_dtype=w.val_dtype, dv_dtype=w.dv_dtype,
-                                              bank_dtype=w.bank_dtype, track=True)
+    b = bounds.dw_stream_bounds(ref, xs, p_chk, S=len(slots), C=w.C, P=P, steps=w.steps, valid_last=w.valid_last,
+                                val_dtype=w.val_dtype, dv_dtype=w.dv_dtype, bank_dtype=w.bank_dtype)
     got = host(bank[torch.from_numpy(p_chk * S + slots.astype(np.int64)).cuda()]).astype(np.float64)
-    t = touched > 0
+    t = b["writes"] > 0
     assert np.array_equal(got[~t], init_p[slots][~t].astype(np.float64))
-    k = touched[t][:, None].astype(np.float64)
-    u = ulp_bf16(ref[t])
-    tol = k * (u + 2.0 ** -17 * mag[t])
-    dlt = np.abs(got[t] - ref[t])
-    ok = (dlt <= tol) | ((amb[t, None] > 0) & (np.abs(got[t] - alt[t]) <= tol))
-    assert ok.all(), f"{name}: {int((~ok).sum())} bank elements of stream {p_chk} beyond tolerance"
+    last = {"y": b["y"][t], "lo": b["lo"][t], "hi": b["hi"][t], "relaxed": b["relaxed"][t]}
+    r = bounds.check_rows(got[t], last, w.bank_dtype)
+    assert r["ok"].all(), f"{name}: {int((~r['ok']).sum())} bank elements of stream {p_chk} outside their interval"
+    once = b["writes"][t] == 1
+    r1 = bounds.check_rows(got[t][once], {k: v[once] for k, v in last.items()}, w.bank_dtype)
+    stats = BankStats(f"{name}_fullsize", "end_to_end", w.bank_dtype)
+    stats.add(r, once=r1)
+    stats.finish()
     others = np.setdiff1d(rng.integers(0, S, size=4096), slots)
     assert np.array_equal(host(bank[torch.from_numpy(p_chk * S + others.astype(np.int64)).cuda()]),
                           init_p[others].astype(np.float64))
     assert bool(torch.isfinite(bank.float()).all())
-    print(name, "bank: max ulp", float(np.max(dlt / u)) if dlt.size else 0.0, "> 1 ulp:", int((dlt > u).sum()),
-          "of", int(dlt.size))
