@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 from synth import WORKLOADS, make_inputs, scaled  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # the GB300's nominal HBM3e bandwidth (the measured copy peak is the roofline)
 
 METRIC_FWD = "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 peak"
 METRIC_PA = "SDM backward Phase A (the backward of DW) tokens/sec and achieved HBM GB/s vs GB300 peak"
@@ -41,10 +42,10 @@ METRIC_GDS = "SDM backward GDS (read-side dots + grad scatter) tokens/sec and ac
 METRIC_GWR = "SDM backward GWR (write-side token gather) tokens/sec and achieved HBM GB/s vs GB300 peak"
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload, kernel and the
-# hash of the CUDA sources at capture time (profiles/ holds the summaries). A source change
-# voids the figure (reported as null).
+# hash of the kernel's CUDA sources at capture time. A source change voids the figure: the bench
+# line then reports null traffic.
 NCU_TRAFFIC = {
-    "large:dw:c28e9f58496b": 1178147328 + 981000192,        # profiles/dram_traffic_large.md
+    "large:dw:c28e9f58496b": 1178147328 + 981000192,
     "large:phase1:6922acd872e5": 55624960 + 718927616,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
@@ -76,6 +77,12 @@ def src_hash(dom: str) -> str:
     return h.hexdigest()[:12]
 
 
+def traffic_source(key: str, traffic) -> str:
+    if traffic is None:
+        return f"null: no ncu capture of these sources ({key})"
+    return f"ncu dram__bytes_read.sum + dram__bytes_write.sum, one capture of sources {key} (profiles/)"
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -90,12 +97,18 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock and throttle reasons around and during the timed region.
+
+    The sampler runs every 5 ms from before the warm-up to after the timed region; ``mark`` records
+    the host time at the start and end of the timed region. The summary takes the samples inside
+    that window, or, when the window is shorter than the sampling period, the nearest sample on each
+    side of it (both taken with the GPU busy: the warm-up before, the last launches after)."""
 
     def __init__(self, index: int):
         self.index = index
         self.rows = []
         self.proc = None
+        self.window = None
 
     def __enter__(self):
         q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -103,24 +116,27 @@ class Clocks:
              "clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "5"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
-            t_end = time.time() + 3.0   # sampling is live before the timed region starts
+            t_end = time.time() + 3.0   # sampling is live before the work starts
             while not self.rows and time.time() < t_end:
                 time.sleep(0.01)
-            self.rows.clear()
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.rows.append([c.strip() for c in line.split(",")])
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.02)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -128,15 +144,27 @@ class Clocks:
                 self.proc.kill()
             self.t.join(timeout=2)
 
-    def summary(self):
-        if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+    def summary(self, busy_ms: float | None = None):
+        rows = list(self.rows)
+        if not rows or self.window is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        t0, t1 = self.window
+        inside = [r for (t, r) in rows if t0 <= t <= t1]
+        how = "inside the timed region"
+        if not inside:
+            before = [r for (t, r) in rows if t < t0][-1:]
+            after = [r for (t, r) in rows if t > t1][:1]
+            inside = before + after
+            how = "nearest sample before and after the timed region (shorter than the 5 ms sampling period)"
+        sm = [float(r[0]) for r in inside if r and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in inside if len(r) > 1 and r[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4) if len(r) > 3 + i and r[3 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+        reasons = sorted({names[i] for r in inside for i in range(4) if len(r) > 3 + i and r[3 + i] == "Active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": reasons, "samples": len(inside), "how": how}
+        if busy_ms is not None and sm:
+            out["ms_x_mhz"] = busy_ms * statistics.median(sm)
+        return out
 
 
 def count_groups(x, w):
@@ -236,6 +264,7 @@ def run_ours(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
+        h0 = time.time()
         t0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -245,6 +274,7 @@ def run_ours(args):
             ev[i][2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(h0, time.time())
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
@@ -332,7 +362,10 @@ def run_ours(args):
     traffic = NCU_TRAFFIC.get(key)
     result = None
     if rank == 0:
-        cpu = None if args.no_cpu_baseline else cpu_baseline(w, x, budget_s=args.cpu_seconds)
+        cpu = None
+        if not args.no_cpu_baseline:
+            x0 = make_inputs(w, streams=[0])
+            cpu = cpu_baselines("fwd", args, w, cpu_baseline(w, x0, budget_s=args.cpu_seconds))
         result = {
             "metric": METRIC_FWD,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -346,11 +379,14 @@ def run_ours(args):
             "algorithmic_bytes": ab, "groups": groups,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "total_frac": ab["total"] / (ms / 1e3) / 1e9 / peak},
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,
+                         "traffic_source": traffic_source(key, traffic),
+                         "total_frac": ab["total"] / (ms / 1e3) / 1e9 / peak,
+                         "total_frac_nominal": ab["total"] / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,   # per forward: Phase 1, the long-group sums, the DW
-            "clocks": clk.summary(),
+            "clocks": clk.summary(ms * args.steps),
             "impl": "ours",
         }
         print(json.dumps(result))
@@ -478,11 +514,13 @@ def run_pa(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
+        h0 = time.time()
         t0.record(stream)
         for _ in range(args.steps):
             step()
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(h0, time.time())
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
@@ -535,9 +573,9 @@ def run_pa(args):
     key = f"{args.workload}:pa{'_bf16grad' if args.pa_grad == 'bf16' else ''}:{src_hash('pa')}"
     result = None
     if rank == 0:
-        cpu = None if args.no_cpu_baseline else pa_cpu_baseline(w, make_inputs(w, streams=[0]),
-                                                                make_backward_inputs(w, streams=[0]),
-                                                                budget_s=args.cpu_seconds)
+        cpu = None if args.no_cpu_baseline else cpu_baselines(
+            "pa", args, w, pa_cpu_baseline(w, make_inputs(w, streams=[0]), make_backward_inputs(w, streams=[0]),
+                                           budget_s=args.cpu_seconds))
         result = {
             "metric": METRIC_PA,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -551,10 +589,11 @@ def run_pa(args):
             "kernels_ms": {"pa_per_launch": kern_ms}, "algorithmic_bytes": ab, "groups": groups,
             "roofline": {"bound": "hbm", "kernel": "pa", "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": NCU_TRAFFIC.get(key)},
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": NCU_TRAFFIC.get(key),
+                         "traffic_source": traffic_source(key, NCU_TRAFFIC.get(key))},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": w.steps * args.steps,
-            "clocks": clk.summary(), "impl": "ours",
+            "clocks": clk.summary(ms * args.steps), "impl": "ours",
         }
         print(json.dumps(result))
     if world > 1:
@@ -676,11 +715,13 @@ def run_gds(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
+        h0 = time.time()
         t0.record(stream)
         for _ in range(args.steps):
             step()
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(h0, time.time())
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
@@ -734,7 +775,8 @@ def run_gds(args):
         cpu = None
         if not args.no_cpu_baseline:
             x0 = make_inputs(w, streams=[0])
-            cpu = gds_cpu_baseline(w, x0, make_read_grads(w, streams=[0]).astype(np.float64), budget_s=args.cpu_seconds)
+            cpu = cpu_baselines("gds", args, w, gds_cpu_baseline(w, x0, make_read_grads(w, streams=[0]).astype(np.float64),
+                                                                 budget_s=args.cpu_seconds))
         result = {
             "metric": METRIC_GDS,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -748,10 +790,11 @@ def run_gds(args):
             "kernels_ms": {"gds_per_workload_step": step_ms}, "algorithmic_bytes": ab, "read_groups": qgroups,
             "roofline": {"bound": "hbm", "kernel": "gds (dots + scatter launches of one step)", "achieved": achieved,
                          "peak": peak, "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(key)},
+                         "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                         "traffic": NCU_TRAFFIC.get(key), "traffic_source": traffic_source(key, NCU_TRAFFIC.get(key))},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * w.steps * args.steps,
-            "clocks": clk.summary(), "impl": "ours",
+            "clocks": clk.summary(ms * args.steps), "impl": "ours",
         }
         print(json.dumps(result))
     if world > 1:
@@ -847,11 +890,13 @@ def run_gwr(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
+        h0 = time.time()
         t0.record(stream)
         for _ in range(args.steps):
             step()
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(h0, time.time())
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
@@ -901,8 +946,9 @@ def run_gwr(args):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline:
-            cpu = gwr_cpu_baseline(w, make_inputs(w, streams=[0]), make_write_weights(w, streams=[0]),
-                                   budget_s=args.cpu_seconds)
+            cpu = cpu_baselines("gwr", args, w, gwr_cpu_baseline(w, make_inputs(w, streams=[0]),
+                                                                 make_write_weights(w, streams=[0]),
+                                                                 budget_s=args.cpu_seconds))
         result = {
             "metric": METRIC_GWR,
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -916,10 +962,11 @@ def run_gwr(args):
             "kernels_ms": {"gwr_per_launch": kern_ms}, "algorithmic_bytes": ab,
             "roofline": {"bound": "hbm", "kernel": "gwr", "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": NCU_TRAFFIC.get(key)},
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": NCU_TRAFFIC.get(key),
+                         "traffic_source": traffic_source(key, NCU_TRAFFIC.get(key))},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": w.steps * args.steps,
-            "clocks": clk.summary(), "impl": "ours",
+            "clocks": clk.summary(ms * args.steps), "impl": "ours",
         }
         print(json.dumps(result))
     if world > 1:
@@ -964,6 +1011,96 @@ def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
                       f"{dt:.1f} s single-threaded"}
 
 
+def host_cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+_WORKER = {}
+
+
+def _stream_sample(job):
+    """One process of the all-cores CPU baseline: the single-thread oracle sample of mode ``kind`` on
+    stream ``p`` of the workload for ``budget`` seconds (the stream's inputs are drawn once per
+    process and kept)."""
+    kind, wname, over, p, budget, mc = job
+    key = (kind, wname, over, p)
+    if key not in _WORKER:
+        w = scaled(WORKLOADS[wname], **dict(over)) if over else WORKLOADS[wname]
+        x = make_inputs(w, streams=[p])
+        extra = None
+        if kind == "pa":
+            from synth import make_backward_inputs
+            extra = make_backward_inputs(w, streams=[p])
+        elif kind == "gds":
+            from synth import make_read_grads
+            extra = make_read_grads(w, streams=[p]).astype(np.float64)
+        elif kind == "gwr":
+            from synth import make_write_weights
+            extra = make_write_weights(w, streams=[p])
+        _WORKER[key] = (w, x, extra)
+    w, x, extra = _WORKER[key]
+    if kind == "pa":
+        return pa_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
+    if kind == "gds":
+        return gds_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
+    if kind == "gwr":
+        return gwr_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
+    return cpu_baseline(w, x, budget_s=budget, max_chunks=mc)
+
+
+class CpuPool:
+    """Every host core running the oracle at once: one spawned process per core, each timing its own
+    single-thread sample on its own stream; the aggregate is the sum of their rates."""
+
+    def __init__(self, kind: str, wname: str, over: tuple, P: int):
+        import multiprocessing as mp
+
+        self.kind, self.wname, self.over, self.P = kind, wname, over, P
+        self.n = os.cpu_count() or 1
+        self.pool = mp.get_context("spawn").Pool(self.n)
+        self.sample(1.0, 1)   # each process draws its stream and loads the oracle first (untimed)
+
+    def sample(self, budget: float, max_chunks=None) -> dict:
+        jobs = [(self.kind, self.wname, self.over, i % self.P, budget, max_chunks) for i in range(self.n)]
+        res = self.pool.map(_stream_sample, jobs, chunksize=1)
+        return {"value": sum(r["value"] for r in res), "unit": "tokens/s", "cores": self.n, "kind": "oracle",
+                "cpu_count": os.cpu_count(), "cpu_model": host_cpu_model(),
+                "sample": f"{self.n} processes at once (one per host core), each on its own stream: "
+                          + res[0]["sample"].replace("stream 0", "its stream").replace(" single-threaded", "")}
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baselines(kind: str, args, w, single: dict) -> dict:
+    """The two CPU rows of a GPU arm's line: the oracle on all host cores (the row's value) and on one
+    core (``single_core``)."""
+    over = tuple(sorted({k: v for k, v in (("P", args.streams), ("S", args.slots)) if v}.items()))
+    pool = CpuPool(kind, args.workload, over, w.P)
+    try:
+        allc = pool.sample(args.cpu_seconds)
+    finally:
+        pool.close()
+    single = dict(single, cpu_count=os.cpu_count(), cpu_model=host_cpu_model())
+    return dict(allc, single_core=single)
+
+
 def run_reference(args):
     """The reference arm: the float64 oracle of the same mode (forward, or --pa / --gds / --gwr) on
     bounded samples of the same workload, on this host's cores; rank 0 only."""
@@ -971,40 +1108,35 @@ def run_reference(args):
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
-    x = make_inputs(w, streams=[0])
     grad_sfx = "+bf16grad" if args.pa_grad == "bf16" else ""
     if args.pa:
-        from synth import make_backward_inputs
-        b = make_backward_inputs(w, streams=[0])
         metric, name = METRIC_PA, w.name + "+phaseA" + grad_sfx
-        sample = lambda budget, mc=None: pa_cpu_baseline(w, x, b, budget_s=budget, max_chunks=mc)   # noqa: E731
     elif args.gds:
-        from synth import make_read_grads
-        gr = make_read_grads(w, streams=[0]).astype(np.float64)
         metric, name = METRIC_GDS, w.name + "+gds" + grad_sfx
-        sample = lambda budget, mc=None: gds_cpu_baseline(w, x, gr, budget_s=budget, max_chunks=mc)  # noqa: E731
     elif args.gwr:
-        from synth import make_write_weights
-        ww = make_write_weights(w, streams=[0])
         metric, name = METRIC_GWR, w.name + "+gwr" + grad_sfx
-        sample = lambda budget, mc=None: gwr_cpu_baseline(w, x, ww, budget_s=budget, max_chunks=mc)  # noqa: E731
     else:
         metric, name = METRIC_FWD, w.name
-        sample = lambda budget, mc=None: cpu_baseline(w, x, budget_s=budget, max_chunks=mc)  # noqa: E731
-    for _ in range(args.warmup):
-        sample(1.0, 1)
-    vals = []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        vals.append(sample(args.cpu_seconds / max(1, args.steps)))
-    el = time.perf_counter() - t0
+    kind = "pa" if args.pa else "gds" if args.gds else "gwr" if args.gwr else "fwd"
+    pool = CpuPool(kind, args.workload, (), w.P)   # every host core, one stream each
+    try:
+        for _ in range(args.warmup):
+            pool.sample(1.0, 1)
+        vals = []
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            vals.append(pool.sample(args.cpu_seconds / max(1, args.steps)))
+        el = time.perf_counter() - t0
+    finally:
+        pool.close()
     v = statistics.mean(r["value"] for r in vals)
     print(json.dumps({
         "impl": "reference", "metric": metric,
         "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic", "config": {**w.describe(), "workload": name},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "cpu_count": vals[0]["cpu_count"], "cpu_model": vals[0]["cpu_model"],
                          "sample": vals[0]["sample"]},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
