@@ -63,6 +63,11 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     g->threads = threads;
     g->npad = threads * kItems;
     g->nwarps = threads / 32;
+    {   // the sort's bucket counts (uint32) lie in the position-pack region of npad words
+        int lg = 0;
+        while ((2 << lg) <= g->npad) ++lg;
+        g->bucket_bits = std::min(std::min(kb, kBucketBits), lg);
+    }
     g->nsl = (s->hd + 127) / 128;
     // DW buckets per stream: about kDwTargetItems items per launch, at most 2^11 and no more
     // buckets than 2^key_bits
@@ -121,15 +126,17 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
         g->hot_cap = static_cast<int>(std::min<size_t>(kHotMax, room / (12 * static_cast<size_t>(g->C))));
     }
     // the sort's words go back and forth between the log-cumsum and the position-pack regions (idle
-    // until the scans); its count table ([digit][32] warp counts and [digit] totals, uint32) reuses
-    // the write-before-count region when that is large enough, else it follows the scan scratch
-    const size_t tab_bytes = (kSortDigits * 32 + kSortDigits) * 4;
+    // until the scans); its two digit-counter arrays ([digit][thread] uint16 each: 8 bytes per
+    // position) lie over the regions from the write-before counts to the scratch (idle until the
+    // scans; the bucket counters are zeroed after the sort), or after the scratch where those are
+    // too small
+    const size_t cnt_bytes = np * 8;
     g->sm_scr = off;
     off += 64 * 16 + 64 * 4;
     g->sm_hist = g->sm_kb;
-    if (tab_bytes > np * 2) {
+    if (g->sm_kb + cnt_bytes > g->sm_scr) {
         g->sm_hist = round_up(off, 16);
-        off = g->sm_hist + tab_bytes;
+        off = g->sm_hist + cnt_bytes;
     }
     g->smem_bytes = round_up(off, 128);
     return SDM_OK;
@@ -176,6 +183,7 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
     a.key_bits = g.key_bits;
     a.passes = g.passes;
     a.digit_bits = g.digit_bits;
+    a.bucket_bits = g.bucket_bits;
     a.S = g.S;
     a.c0 = b * g.P;
     a.first_partial = (g.steps - 1) * g.P;

@@ -29,6 +29,7 @@
 #include <type_traits>
 
 #include "sdm_internal.cuh"
+#include "sdm_rows.cuh"
 
 namespace sdm {
 namespace {
@@ -43,47 +44,6 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// A lane's 4 columns of a row, kept in the storage type until used: 8 bytes (bf16) / 16 bytes (f32).
-template <typename T>
-struct Raw4;
-template <>
-struct Raw4<float> {
-    float4 v;
-    __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
-    __device__ __forceinline__ void ld_nc(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
-    __device__ __forceinline__ void ld_cg(const float* p) { v = __ldcg(reinterpret_cast<const float4*>(p)); }
-    __device__ __forceinline__ float operator[](int i) const { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
-};
-template <>
-struct Raw4<__nv_bfloat16> {
-    uint2 v;
-    __device__ __forceinline__ void zero() { v = make_uint2(0u, 0u); }
-    __device__ __forceinline__ void ld_nc(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
-    __device__ __forceinline__ void ld_cg(const __nv_bfloat16* p) { v = __ldcg(reinterpret_cast<const uint2*>(p)); }
-    __device__ __forceinline__ float operator[](int i) const {
-        const uint32_t w = i < 2 ? v.x : v.y;
-        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
-    }
-};
-
-// the row's raw bytes (the dense snapshot is a copy of the base row)
-__device__ __forceinline__ void st_raw(float* p, const Raw4<float>& r) { *reinterpret_cast<float4*>(p) = r.v; }
-__device__ __forceinline__ void st_raw(__nv_bfloat16* p, const Raw4<__nv_bfloat16>& r) {
-    *reinterpret_cast<uint2*>(p) = r.v;
-}
-
-__device__ __forceinline__ void st4(float* p, const float (&o)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
-}
-__device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&lo);
-    u.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p) = u;
-}
-
 // Long groups (at least kLongMin write entries in one chunk, e.g. the hot slots of a skewed
 // stream): one warp per (group, 128-column slice) sums the group's tail records in order,
 // acc = fmaf(sc_m, dv[tok_m], acc) from 0 -- the very chain of the DW walk -- with the token rows of
@@ -111,11 +71,11 @@ __global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
             if (in) r = __ldcg(rec + base + lane);
             const uint32_t lastm = __ballot_sync(kFull, in && (static_cast<uint32_t>(r.x) & kLast));
             const int n = lastm ? __ffs(lastm) : 16;   // the group's records in this batch
-            Raw4<DvT> dvv[16];
+            rows::Raw4<DvT> dvv[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const uint32_t w0 = __shfl_sync(kFull, static_cast<uint32_t>(r.x), k);
-                if (k < n && active && base + k < a.rstride) dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
+                if (k < n && active && base + k < a.rstride) dvv[k].ld(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
             }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -131,6 +91,12 @@ __global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
             __stcg(reinterpret_cast<float4*>(a.lacc + (static_cast<int64_t>(c) * a.maxL + li) * a.hd + col),
                    make_float4(acc[0], acc[1], acc[2], acc[3]));
     }
+}
+
+// the row's raw bytes (the dense snapshot is a copy of the base row)
+__device__ __forceinline__ void raw_st(float* p, const rows::Raw4<float>& r) { *reinterpret_cast<float4*>(p) = r.v; }
+__device__ __forceinline__ void raw_st(__nv_bfloat16* p, const rows::Raw4<__nv_bfloat16>& r) {
+    *reinterpret_cast<uint2*>(p) = r.v;
 }
 
 // SNAP: the saving forward (a.snap is the dense compact snapshot)
@@ -224,14 +190,14 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                 // first, then the FMA chain in order.
                 auto sub = [&](int m, int cnt, auto kw) {
                     constexpr int K = decltype(kw)::value;
-                    Raw4<DvT> dvv[K];
-                    Raw4<BankT> bv[K];
+                    rows::Raw4<DvT> dvv[K];
+                    rows::Raw4<BankT> bv[K];
 #pragma unroll
                     for (int k = 0; k < K; ++k) {
                         const int4 r = rs[m + k];
                         const uint32_t w0 = static_cast<uint32_t>(r.x);
                         if (k < cnt && active) {
-                            dvv[k].ld_nc(dv_lane + static_cast<uint64_t>(ds[m + k] + (w0 & kRecTokMask)) * hdu);
+                            dvv[k].ld(dv_lane + static_cast<uint64_t>(ds[m + k] + (w0 & kRecTokMask)) * hdu);
                             if (w0 & kLast) bv[k].ld_cg(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu);
                         }
                     }
@@ -247,7 +213,7 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                             for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
                             if (w0 & kLast) {
                                 if (SNAP && active)   // saving forward: the base row, raw
-                                    st_raw(static_cast<BankT*>(a.snap) +
+                                    raw_st(static_cast<BankT*>(a.snap) +
                                                (static_cast<uint64_t>(ds[m + k]) * a.W + gord) * hdu + col,
                                            bv[k]);
                                 if (active) {
@@ -255,7 +221,7 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                                     float o[4];
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
-                                    st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
+                                    rows::st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
                                 }
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
@@ -269,18 +235,18 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
                     const int4 r = rs[m];
                     if (active) {
                         BankT* const row = bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu;
-                        Raw4<BankT> bv;
+                        rows::Raw4<BankT> bv;
                         bv.ld_cg(row);
                         const float4 la = __ldcg(reinterpret_cast<const float4*>(
                             a.lacc + static_cast<uint64_t>(static_cast<uint32_t>(r.z)) * hdu + col));
                         if constexpr (SNAP)
-                            st_raw(static_cast<BankT*>(a.snap) +
+                            raw_st(static_cast<BankT*>(a.snap) +
                                        (static_cast<uint64_t>(ds[m]) * a.W + ((static_cast<uint32_t>(r.x) >> kRecOrdShift) & kRecOrdMask)) * hdu + col,
                                    bv);
                         const float cp = __int_as_float(r.w);
                         const float o[4] = {fmaf(bv[0], cp, la.x), fmaf(bv[1], cp, la.y), fmaf(bv[2], cp, la.z),
                                             fmaf(bv[3], cp, la.w)};
-                        st4(row, o);
+                        rows::st4(row, o);
                     }
                 };
                 const uint32_t longm = __ballot_sync(kFull, lane < n && (static_cast<uint32_t>(rs[lane].x) & kRecLong));

@@ -43,6 +43,10 @@ constexpr int kSortWordEntryBits = 13;
 constexpr uint32_t kSortWordEntryMask = (1u << kSortWordEntryBits) - 1u;
 constexpr int kSortWordKeyBits = 32 - kSortWordEntryBits;
 static_assert(kMaxRow <= (1 << kSortWordEntryBits), "a sort word holds an entry index");
+// the Phase-1 sort's fast path: a counting sort by the key's top kBucketBits bits (buckets of 32-bit
+// counts in the position-pack region), taken when no bucket holds more than kBucketMax entries
+constexpr int kBucketBits = 13;
+constexpr int kBucketMax = 16;
 // bytes of the Phase-1 shared memory after the bucket counters, part of the dense pair path's room
 constexpr int kHotExtra = 4096;
 // bound on the Phase-1 kernel's static shared memory (its flag words and counters)
@@ -85,6 +89,7 @@ struct Geometry {
     int C, W, R, wr, n, nk, nq, P, hd;
     int64_t steps, N, S;
     int key_bits, passes, digit_bits;
+    int bucket_bits;       // min(key_bits, kBucketBits, floor(log2(npad)))
     int threads, npad, nwarps;
     int B, logB;           // DW buckets per stream, B = 2^logB: a slot group's bucket is a hash of its slot
     int nsl;               // DW column slices of 128 columns
@@ -113,6 +118,7 @@ struct P1Args {
     uint32_t* status;
     int C, W, R, wr, n, nk, nq, npad, nwarps;
     int key_bits, passes, digit_bits;
+    int bucket_bits;        // the sort's fast path: buckets of the key's top bucket_bits bits
     int64_t S;
     int64_t c0;             // first chunk of the launch
     int64_t first_partial;  // first chunk whose tokens t >= valid_last are invalid

@@ -317,10 +317,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     if constexpr (ORD)
         for (int i = tid; i < kMaxRow / 32; i += blockDim.x) khead[i] = 0u;
     for (int i = tid; i < 2 * kMaxC; i += blockDim.x) hotrow[i / kMaxC][i % kMaxC] = 0u;
-    // DW bucket sizes (counted by the reverse scan) and fill counters, ordered before their first
-    // use by the sort's barriers
-    const int nbk = 1 << a.logB;
-    for (int b = tid; b < 2 * nbk + 1; b += nthr) bcnt[b] = 0u;
+    const int nbk = 1 << a.logB;   // DW buckets per stream (their counters are zeroed after the sort)
     // A and QK start as zeros (16-byte stores spread over the phases when the chunk's triangles are
     // a whole number of 16-byte units, else plain stores at the start); rows with terms are
     // rewritten at the end.
@@ -389,6 +386,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
     }
     if (!bulk_zero && (a.out.A != nullptr || a.out.QK != nullptr)) zero_triangles(a.out.A, a.out.QK, c, cells);
+    {   // the sort's bucket counts and first digit counters (this thread's scan segment) start at zero
+        uint4* const seg = reinterpret_cast<uint4*>(smem + a.sm_hist) + 2 * tid;
+        seg[0] = make_uint4(0u, 0u, 0u, 0u);
+        seg[1] = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t* const bc = reinterpret_cast<uint32_t*>(smem + a.sm_pos);
+        for (int b = tid; b < (1 << a.bucket_bits); b += nthr) bc[b] = 0u;
+    }
     __syncthreads();
     // A and QK of the chunk start as zeros written by every thread with 16-byte streaming stores, a
     // few per thread at each phase boundary below (spread over the kernel, the stores drain while
@@ -409,24 +413,162 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     };
     zero_tick(2);
 
-    // ---- 1. stable LSD radix sort of entry indices by key (low key_bits bits), 4-bit digits -------
-    // Every lane ranks its kItems consecutive positions (p0 = tid * kItems ...) with lane-private
-    // digit counters held in registers (16 nibbles of one 64-bit word). A warp scan of the
-    // byte-packed counts gives each lane the count of every digit over the warp's earlier lanes;
-    // one block scan of the [digit][warp] totals gives each warp its digit bases. Positions follow
-    // (digit, warp, lane, item) order, which within a digit is the position order: the sort is
-    // stable. No ballots, no shared counters per item. Between passes a position holds a word: the
-    // entry (13 bits) and, once they fit in the other 19, the key bits still to sort, so later
-    // passes read their digits with the word instead of gathering the entry's key.
+    // ---- 1. stable sort of the entries by key --------------------------------------------------
+    // Fast path, a counting sort by the top bits of the key (the bucket): each valid entry counts
+    // into its bucket with a shared atomic, one block scan turns the counts into bucket starts, each
+    // entry takes a place in its bucket with a second atomic (in whatever order the atomics run),
+    // and then every bucket's entries are ranked inside it by (key, entry), which is unique: the
+    // result is the stable order whatever the atomics did. Invalid entries go after every valid one
+    // in entry order. A chunk with a bucket of more than kBucketMax entries (skewed slots) takes the
+    // LSD radix sort instead. The entries move as words: entry (13 bits) | the key's bits under
+    // the bucket << 13.
+    uint32_t* const bstart = reinterpret_cast<uint32_t*>(smem + a.sm_pos);   // [2^bbits] counts -> starts -> ends
+    uint32_t* const bword = reinterpret_cast<uint32_t*>(smem + a.sm_pong);   // words by sorted position
+    const int bbits = a.bucket_bits;   // <= key_bits, and 2^bbits <= npad: the counts fit their region
+    const int bsh = a.key_bits - bbits;                                      // bucket = key >> bsh
+    const int nbuck = 1 << bbits;
+    bool fast;
     {
-        uint32_t* const tab = reinterpret_cast<uint32_t*>(smem + a.sm_hist);   // [digit][32]: warp counts
-        uint32_t* const dtot = tab + kSortDigits * 32;                          // [digit]: block totals
+        const int p0 = tid * kItems;
+        uint32_t kw[kItems];
+        {
+            const uint4 k0 = *reinterpret_cast<const uint4*>(keys + p0);
+            const uint4 k1 = *reinterpret_cast<const uint4*>(keys + p0 + 4);
+            kw[0] = k0.x; kw[1] = k0.y; kw[2] = k0.z; kw[3] = k0.w;
+            kw[4] = k1.x; kw[5] = k1.y; kw[6] = k1.z; kw[7] = k1.w;
+        }
+        uint32_t ninv = 0;
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            if (kw[k] >> 31) ++ninv;
+            else atomicAdd(&bstart[kw[k] >> bsh], 1u);
+        }
+        __syncthreads();
+        // block scan of the counts: thread t owns buckets [bt0, bt1), a contiguous segment
+        const int per = (nbuck + nthr - 1) / nthr;
+        const int bt0 = min(nbuck, tid * per), bt1 = min(nbuck, bt0 + per);
+        const bool vseg = per == 8 && bt1 - bt0 == 8;   // the usual case: two 16-byte loads
+        uint32_t sv[8];
+        uint32_t seg = 0;
+        bool big = false;
+        if (vseg) {
+            const uint4 v0 = *reinterpret_cast<const uint4*>(bstart + bt0);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(bstart + bt0 + 4);
+            sv[0] = v0.x; sv[1] = v0.y; sv[2] = v0.z; sv[3] = v0.w;
+            sv[4] = v1.x; sv[5] = v1.y; sv[6] = v1.z; sv[7] = v1.w;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                seg += sv[q];
+                big |= sv[q] > static_cast<uint32_t>(kBucketMax);
+            }
+        } else {
+            for (int b = bt0; b < bt1; ++b) {
+                const uint32_t v = bstart[b];
+                seg += v;
+                big |= v > static_cast<uint32_t>(kBucketMax);
+            }
+        }
+        uint32_t xs = seg, xi = ninv;   // inclusive over the warp: bucket counts, invalid entries
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            const uint32_t ys = __shfl_up_sync(kFull, xs, dd), yi = __shfl_up_sync(kFull, xi, dd);
+            if (lane >= dd) {
+                xs += ys;
+                xi += yi;
+            }
+        }
+        if (lane == 31) {
+            uscr[warp] = xs;
+            uscr[32 + warp] = xi;
+        }
+        fast = !__syncthreads_or(big);
+        zero_tick(4);
+        // every warp: the totals of the warps before it, and of all warps
+        uint32_t ws = lane < nw ? uscr[lane] : 0u, wi = lane < nw ? uscr[32 + lane] : 0u;
+        const uint32_t ws0 = ws, wi0 = wi;
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            const uint32_t ys = __shfl_up_sync(kFull, ws, dd), yi = __shfl_up_sync(kFull, wi, dd);
+            if (lane >= dd) {
+                ws += ys;
+                wi += yi;
+            }
+        }
+        const uint32_t nvalid = __shfl_sync(kFull, ws, 31);
+        const uint32_t s_before = __shfl_sync(kFull, ws - ws0, warp) + xs - seg;     // bucket entries before mine
+        const uint32_t i_before = __shfl_sync(kFull, wi - wi0, warp) + xi - ninv;    // invalid entries before mine
+        if (fast) {
+            uint32_t run = s_before;
+            if (vseg) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t v = sv[q];
+                    sv[q] = run;
+                    run += v;
+                }
+                *reinterpret_cast<uint4*>(bstart + bt0) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
+                *reinterpret_cast<uint4*>(bstart + bt0 + 4) = make_uint4(sv[4], sv[5], sv[6], sv[7]);
+            } else {
+                for (int b = bt0; b < bt1; ++b) {
+                    const uint32_t v = bstart[b];
+                    bstart[b] = run;
+                    run += v;
+                }
+            }
+        }
+        __syncthreads();
+        if (fast) {
+            zero_tick(4);
+            const uint32_t lowm = bsh > 0 ? (1u << bsh) - 1u : 0u;
+            uint32_t ipos = nvalid + i_before;
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const uint32_t e = static_cast<uint32_t>(p0 + k);
+                if (kw[k] >> 31) {   // invalid: after every valid entry, in entry order (final)
+                    if (ipos < static_cast<uint32_t>(npad)) sidx[ipos] = static_cast<uint16_t>(e);
+                    ++ipos;
+                } else {
+                    const uint32_t pos = atomicAdd(&bstart[kw[k] >> bsh], 1u);   // bstart becomes the end
+                    if (pos < static_cast<uint32_t>(npad)) bword[pos] = e | (kw[k] & lowm) << kSortWordEntryBits;
+                }
+            }
+            __syncthreads();
+            zero_tick(4);
+            // each valid entry's place: the start of its bucket (the previous bucket's end) plus the
+            // number of the bucket's words below its own (key bits under the bucket, then entry)
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                if (kw[k] >> 31) continue;
+                const uint32_t e = static_cast<uint32_t>(p0 + k);
+                const uint32_t b = kw[k] >> bsh;
+                const uint32_t en = bstart[b];
+                const uint32_t st = b > 0 ? bstart[b - 1] : 0u;
+                uint32_t r = st;
+                if (en - st > 1u) {
+                    const uint32_t w = e | (kw[k] & lowm) << kSortWordEntryBits;
+                    for (uint32_t j = st; j < en; ++j) r += bword[j] < w ? 1u : 0u;
+                }
+                if (r < static_cast<uint32_t>(npad)) sidx[r] = static_cast<uint16_t>(e);
+            }
+            __syncthreads();
+        }
+    }
+    // Fallback: a stable LSD radix sort of entry indices by key (low key_bits bits), 4-bit digits.
+    // Every thread ranks its kItems consecutive positions (p0 = tid * kItems ...) with its own digit
+    // counters in shared memory, cnt[digit][thread] (uint16); one block scan of the counters in
+    // (digit, thread) order -- each thread a segment of 16 consecutive counters -- turns them into
+    // first positions; one scatter. Positions follow (digit, thread, item) order, which within a
+    // digit is the position order: the sort is stable. The counters alternate between two arrays
+    // so that the next pass's are cleared while this pass uses its own. Between passes a position
+    // holds a word: the entry (13 bits) and, once they fit in the other 19, the key bits still to
+    // sort, so later passes read their digits with the word instead of gathering the entry's key.
+    if (!fast) {
         uint32_t* const wa = reinterpret_cast<uint32_t*>(smem + a.sm_pong);     // words after even passes
         uint32_t* const wb = reinterpret_cast<uint32_t*>(smem + a.sm_pos);      // words after odd passes
+        uint16_t* const cnt0 = reinterpret_cast<uint16_t*>(smem + a.sm_hist);   // [digit][thread], twice
+        uint32_t* const wtot = uscr;                                            // per-warp totals
         const int p0 = tid * kItems;
-        auto sel4 = [](const uint32_t (&w)[4], uint32_t i) -> uint32_t {
-            return (i & 2u) ? ((i & 1u) ? w[3] : w[2]) : ((i & 1u) ? w[1] : w[0]);
-        };
+        const int ncnt = kSortDigits * nthr;
 #pragma unroll 1
         for (int pass = 0; pass < a.passes; ++pass) {
             const int sh = pass * kSortDigitBits;
@@ -438,9 +580,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             const uint32_t rmask = left > 0 ? (1u << left) - 1u : 0u;
             const uint32_t* const src = (pass & 1) ? wa : wb;
             uint32_t* const dst = (pass & 1) ? wb : wa;
+            uint16_t* const cnt = cnt0 + (pass & 1) * ncnt;        // this pass's counters (zero)
+            uint16_t* const nxt = cnt0 + ((pass + 1) & 1) * ncnt;  // the next pass's
             zero_tick(2);
             uint32_t kr[kItems];   // the entries' key bits sh and up
-            uint32_t wv[kItems];   // the entries (low 13 bits of the words)
+            uint32_t wv[kItems];   // the words this thread's positions move
             if (pass == 0) {
                 const uint4 k0 = *reinterpret_cast<const uint4*>(keys + p0);
                 const uint4 k1 = *reinterpret_cast<const uint4*>(keys + p0 + 4);
@@ -459,92 +603,70 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     wv[k] &= kSortWordEntryMask;
                 }
             }
-            // digit d's count among the lane's items so far: nibble d & 7 of clo (d < 8) or chi
-            uint32_t clo = 0u, chi = 0u;
-            uint32_t dr[2] = {0u, 0u};   // per item: digit | rank among the lane's equal digits << 4 (a byte)
+            // rank among this thread's earlier items of the same digit: its counter, then + 1
+            uint32_t dn = 0u, rn = 0u;   // per item a nibble: digit, rank
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
                 const uint32_t d = kr[k] & dmask;
-                const uint32_t s4 = (d & 7u) << 2;
-                const bool hi = d >= 8u;
-                const uint32_t r = ((hi ? chi : clo) >> s4) & 15u;
-                const uint32_t one = 1u << s4;
-                clo += hi ? 0u : one;
-                chi += hi ? one : 0u;
-                dr[k >> 2] |= (d | r << 4) << (8 * (k & 3));
+                uint16_t* const cp = cnt + d * nthr + tid;
+                const uint32_t r = *cp;
+                *cp = static_cast<uint16_t>(r + 1u);
+                dn |= d << (4 * k);
+                rn |= r << (4 * k);
                 // the word this position moves: the entry and, packed, the key bits after this digit
                 if (!last && dst_packed) wv[k] |= ((kr[k] >> kSortDigitBits) & rmask) << kSortWordEntryBits;
             }
-            const uint64_t cnt = static_cast<uint64_t>(chi) << 32 | clo;
-            // the counts as bytes (digits 4j .. 4j+3 in word j), then their inclusive scan over the
-            // lanes: a byte never carries below lane 31 (at most 31 * kItems = 248)
-            auto bytes_of = [&](int j) -> uint32_t {   // digits 4j .. 4j+3 of cnt, one per byte
-                uint32_t t = static_cast<uint32_t>(cnt >> (16 * j)) & 0xFFFFu;
-                t = (t | (t << 8)) & 0x00FF00FFu;
-                return (t | (t << 4)) & 0x0F0F0F0Fu;
-            };
-            uint32_t inc[4];
+            {   // clear this thread's segment of the next pass's counters (their last reader was the
+                // previous pass's scatter, before its closing barrier)
+                uint4* const seg = reinterpret_cast<uint4*>(nxt + kSortDigits * tid);
+                seg[0] = make_uint4(0u, 0u, 0u, 0u);
+                seg[1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+            zero_tick(2);
+            // block scan of the counters in (digit, thread) order: this thread's segment holds the
+            // counters [16 tid, 16 tid + 16), two per word
+            uint4* const seg = reinterpret_cast<uint4*>(cnt + kSortDigits * tid);
+            uint32_t sw[8];
+            {
+                const uint4 s0 = seg[0], s1 = seg[1];
+                sw[0] = s0.x; sw[1] = s0.y; sw[2] = s0.z; sw[3] = s0.w;
+                sw[4] = s1.x; sw[5] = s1.y; sw[6] = s1.z; sw[7] = s1.w;
+            }
+            uint32_t run = 0;   // exclusive prefixes within the segment (sums < 2^16: no carries)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) inc[j] = bytes_of(j);
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t lo = sw[j] & 0xFFFFu, hi = sw[j] >> 16;
+                sw[j] = run | (run + lo) << 16;
+                run += lo + hi;
+            }
+            uint32_t x = run;
 #pragma unroll
             for (int dd = 1; dd < 32; dd <<= 1) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t y = __shfl_up_sync(kFull, inc[j], dd);
-                    if (lane >= dd) inc[j] += y;
-                }
+                const uint32_t y = __shfl_up_sync(kFull, x, dd);
+                if (lane >= dd) x += y;
             }
-            // exclusive counts (the word subtraction is exact: every true byte lies in 0 .. 248)
-            uint32_t exl[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) exl[j] = inc[j] - bytes_of(j);
-            {   // the warp's count of each digit, from lane 31: lane d < 16 stores digit d's
-                uint32_t xs[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) xs[j] = __shfl_sync(kFull, exl[j], 31);
-                const uint32_t clo = __shfl_sync(kFull, static_cast<uint32_t>(cnt), 31);
-                const uint32_t chi = __shfl_sync(kFull, static_cast<uint32_t>(cnt >> 32), 31);
-                if (lane < kSortDigits) {
-                    const uint32_t u = static_cast<uint32_t>(lane);
-                    const uint32_t cw = u < 8u ? clo : chi;
-                    tab[lane * 32 + warp] = __byte_perm(sel4(xs, u >> 2), 0u, 0x4440u | (u & 3u)) +
-                                            ((cw >> (4u * (u & 7u))) & 15u);
-                }
-            }
+            if (lane == 31) wtot[warp] = x;
             __syncthreads();
-            zero_tick(2);
-            // block scan of the counts in (digit, warp) order: warp d scans digit d over the warps
-            for (int d = warp; d < kSortDigits; d += nw) {
-                const uint32_t v = lane < nw ? tab[d * 32 + lane] : 0u;
-                uint32_t x = v;
+            {   // every warp: the totals of the warps before it
+                const uint32_t t = lane < nw ? wtot[lane] : 0u;
+                uint32_t y = t;
 #pragma unroll
                 for (int dd = 1; dd < 32; dd <<= 1) {
-                    const uint32_t y = __shfl_up_sync(kFull, x, dd);
-                    if (lane >= dd) x += y;
+                    const uint32_t z = __shfl_up_sync(kFull, y, dd);
+                    if (lane >= dd) y += z;
                 }
-                if (lane < nw) tab[d * 32 + lane] = x - v;
-                if (lane == 31) dtot[d] = x;
+                const uint32_t off = __shfl_sync(kFull, y - t, warp) + x - run;   // before this segment
+                const uint32_t o2 = off | off << 16;
+                seg[0] = make_uint4(sw[0] + o2, sw[1] + o2, sw[2] + o2, sw[3] + o2);
+                seg[1] = make_uint4(sw[4] + o2, sw[5] + o2, sw[6] + o2, sw[7] + o2);
             }
             __syncthreads();
             zero_tick(2);
-            // lane d < 16: this warp's first position of digit d (earlier digits, then earlier warps)
-            uint32_t bd;
-            {
-                const uint32_t t = lane < kSortDigits ? dtot[lane] : 0u;
-                uint32_t x = t;
-#pragma unroll
-                for (int dd = 1; dd < kSortDigits; dd <<= 1) {
-                    const uint32_t y = __shfl_up_sync(kFull, x, dd);
-                    if (lane >= dd) x += y;
-                }
-                bd = lane < kSortDigits ? x - t + tab[lane * 32 + warp] : 0u;
-            }
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
-                const uint32_t b = (dr[k >> 2] >> (8 * (k & 3))) & 0xFFu;
-                const uint32_t d = b & 15u;
-                const uint32_t pos = __shfl_sync(kFull, bd, static_cast<int>(d)) +
-                                     __byte_perm(sel4(exl, d >> 2), 0u, 0x4440u | (d & 3u)) + (b >> 4);
+                const uint32_t d = (dn >> (4 * k)) & 15u;
+                const uint32_t pos = static_cast<uint32_t>(cnt[d * nthr + tid]) + ((rn >> (4 * k)) & 15u);
                 if (pos < static_cast<uint32_t>(npad)) {
                     if (last)
                         sidx[pos] = static_cast<uint16_t>(wv[k]);
@@ -555,6 +677,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             __syncthreads();
         }
     }
+    // the DW bucket counters lay under the sort's digit counters: zeroed now, ordered before their
+    // first use (the reverse scan) by the forward scan's barriers
+    for (int b = tid; b < 2 * nbk + 1; b += nthr) bcnt[b] = 0u;
 
     // ---- 2. segmented scans over the sorted row -------------------------------------------------
     const int r0 = tid * kItems;
@@ -622,7 +747,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
-        zero_tick(2);
+        zero_tick(4);
         // Not unrolled (code size): item k's gate and entry are taken from the bottom of x[] / ke[],
         // which shift down one place per iteration (after kItems shifts they are back in order).
 #pragma unroll 1
@@ -668,7 +793,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == kItems - 1 ? it : bcomb(agg, it);
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
-        zero_tick(2);
+        zero_tick(4);
         const int64_t kbase = c * nk, qbase = c * nq;
         // Not unrolled (the body is large): item k's gate and entry are taken from the top of
         // x[] / ke[], which shift up one place per iteration (register moves, no local memory).
@@ -745,7 +870,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         uint32_t* const fill = bcnt + B + 1; // [B]
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
-        zero_tick(2);
+        zero_tick(4);
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
         // a warp takes 32 consecutive write-row positions
@@ -821,7 +946,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 3. entry-order outputs -------------------------------------------------------------------
     {
-        zero_tick(2);
+        zero_tick(4);
         const int64_t kbase = c * nk;
         ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
         ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);

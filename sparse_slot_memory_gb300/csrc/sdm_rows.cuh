@@ -1,4 +1,4 @@
-// sdm_rows.cuh -- row helpers of the backward kernels: a lane's 4 columns of a row (f32 or bf16),
+// sdm_rows.cuh -- row helpers of the DW and backward kernels: a lane's 4 or 8 columns of a row (f32 or bf16),
 // per-lane cp.async copies into shared memory, and the lane tree that sums a dot's 32 lane partials.
 #pragma once
 
@@ -52,16 +52,59 @@ struct Raw4<float> {
     float4 v;
     __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ void ld(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+    __device__ __forceinline__ void ld_cg(const float* p) { v = __ldcg(reinterpret_cast<const float4*>(p)); }
     __device__ __forceinline__ void get(float (&o)[4]) const { o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w; }
+    __device__ __forceinline__ float operator[](int i) const { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 };
 template <>
 struct Raw4<__nv_bfloat16> {
     uint2 v;
     __device__ __forceinline__ void zero() { v = make_uint2(0u, 0u); }
     __device__ __forceinline__ void ld(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+    __device__ __forceinline__ void ld_cg(const __nv_bfloat16* p) { v = __ldcg(reinterpret_cast<const uint2*>(p)); }
     __device__ __forceinline__ void get(float (&o)[4]) const {
         o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
         o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+    __device__ __forceinline__ float operator[](int i) const {
+        const uint32_t w = i < 2 ? v.x : v.y;
+        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+};
+// A lane's 8 columns kept in the storage type (16 bytes bf16 / 32 bytes f32 of registers): one
+// 16-byte vector access per lane for bfloat16 rows, two for float32.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void ld(const float* p) {
+        a = __ldg(reinterpret_cast<const float4*>(p));
+        b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void ld_cg(const float* p) {
+        a = __ldcg(reinterpret_cast<const float4*>(p));
+        b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    }
+    __device__ __forceinline__ void st(float* p) const {
+        reinterpret_cast<float4*>(p)[0] = a;
+        reinterpret_cast<float4*>(p)[1] = b;
+    }
+    __device__ __forceinline__ float operator[](int i) const {
+        const float4& q = i < 4 ? a : b;
+        const int j = i & 3;
+        return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+    }
+};
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 v;
+    __device__ __forceinline__ void ld(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ void ld_cg(const __nv_bfloat16* p) { v = __ldcg(reinterpret_cast<const uint4*>(p)); }
+    __device__ __forceinline__ void st(__nv_bfloat16* p) const { *reinterpret_cast<uint4*>(p) = v; }
+    __device__ __forceinline__ float operator[](int i) const {
+        const uint32_t w = i < 2 ? v.x : i < 4 ? v.y : i < 6 ? v.z : v.w;
+        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
     }
 };
 
@@ -76,6 +119,22 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
     u.x = *reinterpret_cast<const uint32_t*>(&lo);
     u.y = *reinterpret_cast<const uint32_t*>(&hi);
     *reinterpret_cast<uint2*>(p) = u;
+}
+
+// store 8 columns: f32 as is, bf16 rounded to nearest even
+__device__ __forceinline__ void st8(float* p, const float (&o)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&o)[8]) {
+    uint4 u;
+    uint32_t* const w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 x = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    *reinterpret_cast<uint4*>(p) = u;
 }
 
 // Per-lane asynchronous copy of a lane's 4 columns (16 bytes f32, 8 bytes bf16) into shared memory;

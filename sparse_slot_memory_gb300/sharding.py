@@ -17,11 +17,3 @@ def shard_streams(P: int, rank: int, world: int) -> range:
     base, extra = divmod(P, world)
     start = rank * base + min(rank, extra)
     return range(start, start + base + (1 if rank < extra else 0))
-
-
-def aggregate_throughput(units_total: float, seconds_local: float, max_reduce) -> tuple:
-    """Whole-job throughput of a weak-scaling run: the units every rank processed over the
-    slowest rank's time (``max_reduce(x)`` = the max of x over ranks). Returns
-    (units per second, slowest seconds)."""
-    t = max_reduce(seconds_local)
-    return units_total / t, t

@@ -206,15 +206,17 @@ def _forward_bits(w, shape, d, init, split=None):
 
 @pytest.mark.parametrize("name", ["uniform_c128", "zipf_c256", "few_slots", "tiny_pe", "wide_hot"])
 def test_launch_geometry_does_not_change_bits(name):
-    """The same forward with other launch geometries: every Phase-1 block widened to 32 warps (the
-    extra warps hold padding entries: other scan trees over the warps, other warps taking the pair
-    rows and the dense groups) and the DW walk over 2 hashed slot buckets per stream, or the most
-    the shape allows (each bucket a different warp's walk). Every output bit and the bank agree."""
+    """The same forward with other launch geometries: every Phase-1 block widened by a quarter of its
+    warps (at least one; the extra warps hold padding entries: other scan trees over the warps,
+    other warps taking the pair rows and the dense groups) and the DW walk over 2 hashed slot buckets per stream, or the
+    most the shape allows (each bucket a different warp's walk). Every output bit and the bank agree."""
     w, x, shape, d, ws = _setup(name)
     init = _init_bank(w, x["P"]).reshape(x["P"] * w.S, w.hd)
     ref = _forward_bits(w, shape, d, init)
     kb = max(1, int(np.ceil(np.log2(w.S))))
-    for geo in (dict(p1_warps=32, dw_log_buckets=1), dict(dw_log_buckets=min(11, kb))):
+    warps = -(-w.C * (w.W + w.R) // (8 * 32))   # the automatic Phase-1 warps per block
+    for geo in (dict(p1_warps=min(32, warps + max(1, warps // 4)), dw_log_buckets=1),
+                dict(dw_log_buckets=min(11, kb))):
         other = _forward_bits(w, dataclasses.replace(shape, **geo), d, init)
         for k in ref:
             assert np.array_equal(ref[k], other[k]), f"{k} differs with geometry {geo}"
