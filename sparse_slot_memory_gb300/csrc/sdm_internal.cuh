@@ -43,10 +43,19 @@ constexpr int kSortWordEntryBits = 13;
 constexpr uint32_t kSortWordEntryMask = (1u << kSortWordEntryBits) - 1u;
 constexpr int kSortWordKeyBits = 32 - kSortWordEntryBits;
 static_assert(kMaxRow <= (1 << kSortWordEntryBits), "a sort word holds an entry index");
+// Phase 1's word per write-row position: the entry (13 bits), LAST, FIRST, VALID and, from bit
+// 16, the group's size (FIRST; later the group's first record) or the valid write entries before
+// the entry in its group
+constexpr uint32_t kKrEntry = 0x1FFFu;
+constexpr uint32_t kKrLast = 1u << 13;
+constexpr uint32_t kKrFirst = 1u << 14;
+constexpr uint32_t kKrValid = 1u << 15;
 // the Phase-1 sort's fast path: a counting sort by the key's top kBucketBits bits (buckets of 32-bit
 // counts in the position-pack region), taken when no bucket holds more than kBucketMax entries
 constexpr int kBucketBits = 13;
 constexpr int kBucketMax = 16;
+// Phase 1: SM clock cycles between a warp's zero stores of A / QK (one 16-byte unit per thread)
+constexpr uint32_t kZeroPeriod = 1400u;
 // bytes of the Phase-1 shared memory after the bucket counters, part of the dense pair path's room
 constexpr int kHotExtra = 4096;
 // bound on the Phase-1 kernel's static shared memory (its flag words and counters)

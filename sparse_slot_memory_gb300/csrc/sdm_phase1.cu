@@ -336,7 +336,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const int32_t* qid = a.q_idx + c * nq;
     const float* gch = a.g + c * C * a.g_width;
 
-    // ---- 0. load: every id and value of the chunk, all loads of a thread in flight together ------
+    // ---- 0. load: every id and value of the chunk, all loads of a thread in flight together; the
+    // chunk's gates go to the rex region (idle until the reverse scan; the LSD sort's counters, where
+    // they lie over it, bring them back after the sort)
+    float* const gs = rexv;
+    const int ngate = C * a.g_width;
+    auto load_gates = [&]() {
+        for (int i = tid; i < ngate; i += nthr) gs[i] = __ldg(gch + i);
+    };
+    load_gates();
     {
         bool bad = false;
         const int total = nk + nq;
@@ -386,32 +394,38 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.status, kDevBadSlot);
     }
     if (!bulk_zero && (a.out.A != nullptr || a.out.QK != nullptr)) zero_triangles(a.out.A, a.out.QK, c, cells);
-    {   // the sort's bucket counts and first digit counters (this thread's scan segment) start at zero
-        uint4* const seg = reinterpret_cast<uint4*>(smem + a.sm_hist) + 2 * tid;
-        seg[0] = make_uint4(0u, 0u, 0u, 0u);
-        seg[1] = make_uint4(0u, 0u, 0u, 0u);
+    {   // the counting sort's bucket counts start at zero
         uint32_t* const bc = reinterpret_cast<uint32_t*>(smem + a.sm_pos);
         for (int b = tid; b < (1 << a.bucket_bits); b += nthr) bc[b] = 0u;
     }
     __syncthreads();
-    // A and QK of the chunk start as zeros written by every thread with 16-byte streaming stores, a
-    // few per thread at each phase boundary below (spread over the kernel, the stores drain while
-    // the block computes); rows with terms are written again in phase 4, after a block barrier.
-    const int zunits = bulk_zero ? static_cast<int>(cells / 2) : 0;   // float4 units of both triangles
-    const int zper = (zunits + nthr - 1) / nthr;
+    // A and QK of the chunk start as zeros written by every thread with 16-byte streaming stores,
+    // paced by the SM clock: a warp stores one unit per thread each kZeroPeriod cycles (the warps
+    // a 1/32 period apart), checked once per item in the per-item loops below. The stores so form
+    // a steady stream under the block's compute; issued in bursts at the phase boundaries they
+    // stalled the block (about 20 us more per Phase 1 on the large workload). Rows with terms are
+    // written again in phase 4, after the flush of the units left and a block barrier. Thread
+    // tid's units of a triangle are tid, tid + nthr, ... (A's, then QK's).
+    const int zper_m = bulk_zero ? static_cast<int>(cells / 4) : 0;   // 16-byte units per triangle
+    const int zka = a.out.A != nullptr && zper_m > tid ? (zper_m - tid + nthr - 1) / nthr : 0;
+    const int zkq = a.out.QK != nullptr && zper_m > tid ? (zper_m - tid + nthr - 1) / nthr : 0;
+    float* const za = a.out.A != nullptr ? a.out.A + c * cells + static_cast<int64_t>(tid) * 4 : nullptr;
+    float* const zq = a.out.QK != nullptr ? a.out.QK + c * cells + static_cast<int64_t>(tid) * 4 : nullptr;
+    const int zstride = nthr * 4;
     int zero_next = 0;   // this thread's next unit
-    auto zero_tick = [&](int most, bool flush = false) {
-        const int stop = flush ? zper : min(zper, zero_next + most);
-        for (; zero_next < stop; ++zero_next) {
-            const int u = zero_next * nthr + tid;
-            if (u >= zunits) break;
-            const int mi = u < zunits / 2 ? 0 : 1;
-            float* const mat = mi == 0 ? a.out.A : a.out.QK;
-            if (mat != nullptr)
-                __stcs(reinterpret_cast<float4*>(mat + c * cells) + (u - mi * (zunits / 2)), make_float4(0.f, 0.f, 0.f, 0.f));
+    uint32_t zdl = static_cast<uint32_t>(clock()) + static_cast<uint32_t>(warp) * (kZeroPeriod / 32u);
+    auto zero_store = [&]() {
+        float* const p = zero_next < zka ? za + zero_next * zstride : zq + (zero_next - zka) * zstride;
+        __stcs(reinterpret_cast<float4*>(p), make_float4(0.f, 0.f, 0.f, 0.f));
+        ++zero_next;
+    };
+    auto zpace = [&]() {   // one unit when this warp's next time has come
+        if (zero_next < zka + zkq && static_cast<int32_t>(static_cast<uint32_t>(clock()) - zdl) >= 0) {
+            zero_store();
+            zdl += kZeroPeriod;
         }
     };
-    zero_tick(2);
+    zpace();
 
     // ---- 1. stable sort of the entries by key --------------------------------------------------
     // Fast path, a counting sort by the top bits of the key (the bucket): each valid entry counts
@@ -442,6 +456,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         for (int k = 0; k < kItems; ++k) {
             if (kw[k] >> 31) ++ninv;
             else atomicAdd(&bstart[kw[k] >> bsh], 1u);
+            zpace();
         }
         __syncthreads();
         // block scan of the counts: thread t owns buckets [bt0, bt1), a contiguous segment
@@ -482,7 +497,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             uscr[32 + warp] = xi;
         }
         fast = !__syncthreads_or(big);
-        zero_tick(4);
+        zpace();
         // every warp: the totals of the warps before it, and of all warps
         uint32_t ws = lane < nw ? uscr[lane] : 0u, wi = lane < nw ? uscr[32 + lane] : 0u;
         const uint32_t ws0 = ws, wi0 = wi;
@@ -518,11 +533,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         __syncthreads();
         if (fast) {
-            zero_tick(4);
+            zpace();
             const uint32_t lowm = bsh > 0 ? (1u << bsh) - 1u : 0u;
             uint32_t ipos = nvalid + i_before;
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
+                zpace();
                 const uint32_t e = static_cast<uint32_t>(p0 + k);
                 if (kw[k] >> 31) {   // invalid: after every valid entry, in entry order (final)
                     if (ipos < static_cast<uint32_t>(npad)) sidx[ipos] = static_cast<uint16_t>(e);
@@ -533,11 +549,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 }
             }
             __syncthreads();
-            zero_tick(4);
+            zpace();
             // each valid entry's place: the start of its bucket (the previous bucket's end) plus the
             // number of the bucket's words below its own (key bits under the bucket, then entry)
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
+                zpace();
                 if (kw[k] >> 31) continue;
                 const uint32_t e = static_cast<uint32_t>(p0 + k);
                 const uint32_t b = kw[k] >> bsh;
@@ -569,6 +586,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         uint32_t* const wtot = uscr;                                            // per-warp totals
         const int p0 = tid * kItems;
         const int ncnt = kSortDigits * nthr;
+        {   // this thread's scan segment of the first pass's counters starts at zero
+            uint4* const seg = reinterpret_cast<uint4*>(cnt0) + 2 * tid;
+            seg[0] = make_uint4(0u, 0u, 0u, 0u);
+            seg[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
 #pragma unroll 1
         for (int pass = 0; pass < a.passes; ++pass) {
             const int sh = pass * kSortDigitBits;
@@ -582,7 +605,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             uint32_t* const dst = (pass & 1) ? wb : wa;
             uint16_t* const cnt = cnt0 + (pass & 1) * ncnt;        // this pass's counters (zero)
             uint16_t* const nxt = cnt0 + ((pass + 1) & 1) * ncnt;  // the next pass's
-            zero_tick(2);
+            zpace();
             uint32_t kr[kItems];   // the entries' key bits sh and up
             uint32_t wv[kItems];   // the words this thread's positions move
             if (pass == 0) {
@@ -623,7 +646,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 seg[1] = make_uint4(0u, 0u, 0u, 0u);
             }
             __syncthreads();
-            zero_tick(2);
+            zpace();
             // block scan of the counters in (digit, thread) order: this thread's segment holds the
             // counters [16 tid, 16 tid + 16), two per word
             uint4* const seg = reinterpret_cast<uint4*>(cnt + kSortDigits * tid);
@@ -662,7 +685,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 seg[1] = make_uint4(sw[4] + o2, sw[5] + o2, sw[6] + o2, sw[7] + o2);
             }
             __syncthreads();
-            zero_tick(2);
+            zpace();
 #pragma unroll
             for (int k = 0; k < kItems; ++k) {
                 const uint32_t d = (dn >> (4 * k)) & 15u;
@@ -676,6 +699,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
             __syncthreads();
         }
+        load_gates();   // the counters may have covered them
+        __syncthreads();
     }
     // the DW bucket counters lay under the sort's digit counters: zeroed now, ordered before their
     // first use (the reverse scan) by the forward scan's barriers
@@ -704,6 +729,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
+            zpace();
             const uint32_t e = ke[k], key = keys[e];
             const bool inv = key >> 31, pinv = pk >> 31;
             const bool head = (r0 + k == 0) || inv || pinv || (key != pk);
@@ -717,7 +743,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             padm |= (e >= static_cast<uint32_t>(n) ? 1u : 0u) << k;
             const bool rep = !head && !isq && !is_q_of(pe) && tok_of(pe) == t;
             repc += rep ? 1u : 0u;
-            x[k] = (!inv && !isq && !rep) ? __ldg(gch + t * a.g_width + j * a.g_lane_stride) : 0.f;
+            x[k] = (!inv && !isq && !rep) ? gs[t * a.g_width + j * a.g_lane_stride] : 0.f;
             pk = key;
             pe = e;
         }
@@ -747,11 +773,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == 0 ? it : fcomb(agg, it);
         }
         Fwd run = fwd_block_prefix(agg, fscr, lane, warp, nw);
-        zero_tick(4);
+        zpace();
         // Not unrolled (code size): item k's gate and entry are taken from the bottom of x[] / ke[],
         // which shift down one place per iteration (after kItems shifts they are back in order).
 #pragma unroll 1
         for (int k = 0; k < kItems; ++k) {
+            zpace();
             const float xk = x[0];
             const uint32_t e = ke[0];
 #pragma unroll
@@ -793,7 +820,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             agg = k == kItems - 1 ? it : bcomb(agg, it);
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
-        zero_tick(4);
+        zpace();
         const int64_t kbase = c * nk, qbase = c * nq;
         // Not unrolled (the body is large): item k's gate and entry are taken from the top of
         // x[] / ke[], which shift up one place per iteration (register moves, no local memory).
@@ -801,6 +828,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
             const Bwd ex = run;
+            zpace();
             const float xk = x[kItems - 1];
             const uint32_t e = ke[kItems - 1];
 #pragma unroll
@@ -812,8 +840,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             run = bcomb(run, it);
             if (e >= static_cast<uint32_t>(n)) continue;
             const int r = r0 + k;
-            const uint32_t key = keys[e];
-            const bool valid = !(key >> 31);
+            const bool valid = (validm >> k) & 1u;
             const uint32_t t = tok_of(e);
             const int j = static_cast<int>(e - t * wr);
             const bool isq = j >= W;
@@ -842,10 +869,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 const float cpe_f = valid ? to_f(from_f<ValT>(expf(run.tot))) : 1.0f;
                 rexv[o] = rex;
                 cpev[o] = cpe_f;
-                if (a.out.sorted_k != nullptr) st_stream(a.out.sorted_k + kbase + jx, static_cast<int32_t>(el));
-                krpos[jx] = e | ((valid && before == 0) ? (after + 1u) << 16 : 0u);
+                // the write row's word: entry | VALID | LAST | FIRST | (FIRST: the group's size,
+                // else the valid write entries before it in the group) << 16
+                krpos[jx] = valid ? (e | kKrValid | (after == 0 ? kKrLast : 0u) |
+                                     (before == 0 ? kKrFirst | (after + 1u) << 16 : before << 16))
+                                  : e;
                 if (valid && before == 0)   // the group's records in its bucket: a long group has one
-                    atomicAdd(&bcnt[bucket_of(key)], after + 1u >= static_cast<uint32_t>(kLongMin) ? 1u : after + 1u);
+                    atomicAdd(&bcnt[bucket_of(keys[e])], after + 1u >= static_cast<uint32_t>(kLongMin) ? 1u : after + 1u);
                 if constexpr (ORD)   // the saving forward: group heads by write-row position
                     if (valid && before == 0) atomicOr(&khead[jx >> 5], 1u << (jx & 31u));
                 if (valid && before == 0 && after + 1u >= kHotMin) atomicOr(&hotmask[r >> 5], 1u << (r & 31));
@@ -870,15 +900,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         uint32_t* const fill = bcnt + B + 1; // [B]
         block_exscan_padded(off, B + 1, B + 1, uscr, lane, warp, nw);
         __syncthreads();
-        zero_tick(4);
+        zpace();
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
         // a warp takes 32 consecutive write-row positions
         for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
             const int j = j0 + lane;
+            zpace();
             const uint32_t kp = j < nk ? krpos[j] : 0u;
-            if (kp >> 16) {
-                const uint32_t b = bucket_of(keys[kp & 0xFFFFu]);
+            if (kp & kKrFirst) {
+                const uint32_t b = bucket_of(keys[kp & kKrEntry]);
                 const uint32_t size = kp >> 16;
                 uint32_t base;
                 if (size >= static_cast<uint32_t>(kLongMin)) {
@@ -888,7 +919,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     const uint32_t ref = off[b] + atomicAdd(&fill[b], 1u);
                     base = off[B] + atomicAdd(&ltail_s, size);
                     a.ldesc[c * a.maxL + li] = static_cast<int32_t>(base);
-                    const uint32_t e = kp & 0xFFFFu;
+                    const uint32_t e = kp & kKrEntry;
                     const uint32_t t = tok_of(e);
                     uint32_t w0 = li | kRecLong | kFirst | kLast;
                     if constexpr (ORD) {   // the group's dense ordinal (khead is complete: reverse scan)
@@ -902,7 +933,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 } else {
                     base = off[b] + atomicAdd(&fill[b], size);
                 }
-                krpos[j] = (kp & 0xFFFFu) | base << 16;
+                krpos[j] = (kp & 0xFFFFu) | base << 16;   // FIRST: the group's first record
             }
         }
         __syncthreads();
@@ -917,6 +948,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
         }
         for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
+            zpace();
             uint32_t gpre = 0;   // ORD: groups before this warp's word (the dense ordinal of a group starting in it)
             if constexpr (ORD) {
                 for (int wi = lane; wi < (j0 >> 5); wi += 32) gpre += __popc(khead[wi]);
@@ -924,15 +956,22 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
             const int j = j0 + lane;
             if (j >= nk) continue;
-            const uint32_t e = krpos[j] & 0xFFFFu;
-            const uint32_t key = keys[e];
-            if (key >> 31) continue;   // invalid entries have no record
-            const uint32_t kb = kbv[e];
-            const uint32_t rec = (krpos[j - kb] >> 16) + kb;
+            const uint32_t kp = krpos[j];
+            const uint32_t e = kp & kKrEntry;
             const uint32_t t = tok_of(e);
-            const int o = static_cast<int>(t) * W + static_cast<int>(e - t * wr);
-            const bool last = ((posv[e] >> kPosAfterShift) & kPosCountMax) == 0u;
-            uint32_t w0 = t | (last ? kLast : 0u);
+            const uint32_t ln = e - t * wr;
+            const uint32_t kb = (kp & kKrFirst) ? 0u : kp >> 16;   // valid write entries before it in the group
+            if (a.out.sorted_k != nullptr)   // the sorted write row, coalesced: its element from the word
+                st_stream(a.out.sorted_k + c * nk + j,
+                          static_cast<int32_t>((kp & kKrValid)
+                                                   ? (t << kTokenShift | ln | min(kb, kDistMax) << kDistShift |
+                                                      ((kp & kKrFirst) ? kFirst : 0u) | ((kp & kKrLast) ? kLast : 0u))
+                                                   : ((t << kTokenShift | ln | kInvalidBit) | kFirst | kLast)));
+            if (!(kp & kKrValid)) continue;   // invalid entries have no record
+            const uint32_t key = keys[e];
+            const uint32_t rec = (krpos[j - kb] >> 16) + kb;
+            const int o = static_cast<int>(t * W + ln);
+            uint32_t w0 = t | ((kp & kKrLast) ? kLast : 0u);
             if (kb == 0u) {
                 w0 |= kFirst;
                 if constexpr (ORD)   // the group's dense ordinal
@@ -946,7 +985,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 3. entry-order outputs -------------------------------------------------------------------
     {
-        zero_tick(4);
+        zpace();
         const int64_t kbase = c * nk;
         ValT* const cpe_o = static_cast<ValT*>(a.out.cpe);
         ValT* const keff_o = static_cast<ValT*>(a.out.k_eff);
@@ -957,6 +996,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             // (their entry indices are consecutive and a multiple of 4) and vector stores
             for (int o = 4 * tid; o < nk; o += 4 * nthr) {
                 const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.w_magic)), e = t * wr + (o - t * W);
+                zpace();
                 const uint4 pk = *reinterpret_cast<const uint4*>(posv + e);
                 float lg[4], v[4];
                 ld4(lv + e, lg);
@@ -988,6 +1028,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             }
             for (int o = 4 * tid; o < nq; o += 4 * nthr) {
                 const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
+                zpace();
                 const uint4 pk = *reinterpret_cast<const uint4*>(posv + e);
                 float lg[4], v[4];
                 ld4(lv + e, lg);
@@ -1042,7 +1083,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     // ---- 4. pair triangles --------------------------------------------------------------------------
     if (tid == 0) a.lcnt[c] = static_cast<int32_t>(lcnt_s);   // final since the DW split's barrier
     if (a.out.A == nullptr && a.out.QK == nullptr) return;
-    zero_tick(0, true);   // the zeros not yet stored; the barrier orders them before the rows' stores
+    while (zero_next < zka + zkq) zero_store();   // the units left; the barrier orders them before the rows' stores
     __syncthreads();   // the key array becomes the row buffers
     float* const rowbuf = reinterpret_cast<float*>(smem + a.sm_keys) + warp * C;
     const uint32_t le = lanemask_le();
