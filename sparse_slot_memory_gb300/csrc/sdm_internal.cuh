@@ -50,6 +50,9 @@ constexpr uint32_t kKrEntry = 0x1FFFu;
 constexpr uint32_t kKrLast = 1u << 13;
 constexpr uint32_t kKrFirst = 1u << 14;
 constexpr uint32_t kKrValid = 1u << 15;
+// set by the DW split in a long group's FIRST word, whose bits 16..30 then hold the group's first
+// record in the chunk's tail
+constexpr uint32_t kKrLong = 1u << 31;
 // the Phase-1 sort's fast path: a counting sort by the key's top kBucketBits bits (buckets of 32-bit
 // counts in the position-pack region), taken when no bucket holds more than kBucketMax entries
 constexpr int kBucketBits = 13;
@@ -84,6 +87,7 @@ constexpr uint32_t kRecTokMask = 0xFFFFu;
 constexpr uint32_t kRecLong = 1u << 29;
 constexpr int kLongMin = 32;
 constexpr int kMaxLong = kMaxRow / kLongMin;   // long groups per chunk at most
+static_assert(kMaxRow + kMaxLong < (1 << 15), "a chunk's record places fit bits 16..30 of a write-row word");
 // the group's dense ordinal in its chunk (valid write groups before it in sorted order), carried by
 // the group's FIRST record: the row of the dense compact snapshot
 constexpr int kRecOrdShift = 16;

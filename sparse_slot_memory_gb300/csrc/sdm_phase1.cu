@@ -814,10 +814,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         Bwd run = bwd_block_prefix(agg, bscr, lane, warp, nw);
         zpace();
-        const int64_t kbase = c * nk, qbase = c * nq;
-        // Not unrolled (the body is large): item k's gate and entry are taken from the top of
-        // x[] / ke[], which shift up one place per iteration (register moves, no local memory).
-#pragma unroll 1
+        const int64_t qbase = c * nq;
+        // Unrolled by two only (the body is large; fully unrolled it spills): item k's gate and
+        // entry are taken from the top of x[] / ke[], which shift up one place per iteration
+        // (register moves, no local memory).
+#pragma unroll 2
         for (int k = kItems - 1; k >= 0; --k) {
             const bool tail = (tailm >> k) & 1u;
             const Bwd ex = run;
@@ -896,23 +897,52 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         zpace();
         const int64_t p = c % a.P, ti = c / a.P;
         for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
-        // a warp takes 32 consecutive write-row positions
+        const int64_t kbase = c * a.rstride;
+        // record of the write entry with word kpi at place rec: {token | LAST | extra, slot, sc, cpe}
+        auto put_record = [&](uint32_t kpi, uint32_t rec, uint32_t key, uint32_t extra) {
+            const uint32_t e = kpi & kKrEntry;
+            const uint32_t t = tok_of(e);
+            const int o = static_cast<int>(t * W + (e - t * wr));
+            const uint32_t w0 = t | ((kpi & kKrLast) ? kLast : 0u) | extra;
+            const float sc = __fmul_rn(to_f(vals[e]), expf(rexv[o]));
+            st_stream(a.krec + kbase + rec, make_int4(static_cast<int>(w0), static_cast<int>(key), __float_as_int(sc),
+                                                      __float_as_int(cpev[o])));
+        };
+        // A warp takes 32 consecutive write-row positions: each writes its sorted write-row element
+        // (coalesced, derived from the word); a group's first entry claims the group's place in its
+        // bucket and writes the group's records (its members are the next positions of the row).
         for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
             const int j = j0 + lane;
             zpace();
+            uint32_t gpre = 0;   // ORD: groups before this warp's word (the dense ordinal of a group starting in it)
+            if constexpr (ORD) {
+                for (int wi = lane; wi < (j0 >> 5); wi += 32) gpre += __popc(khead[wi]);
+                gpre = __reduce_add_sync(kFull, gpre);
+            }
             const uint32_t kp = j < nk ? krpos[j] : 0u;
+            if (j < nk && a.out.sorted_k != nullptr) {
+                const uint32_t e = kp & kKrEntry;
+                const uint32_t t = tok_of(e);
+                const uint32_t ln = e - t * wr;
+                const uint32_t kb = (kp & kKrFirst) ? 0u : kp >> 16;   // valid write entries before it in the group
+                st_stream(a.out.sorted_k + c * nk + j,
+                          static_cast<int32_t>((kp & kKrValid)
+                                                   ? (t << kTokenShift | ln | min(kb, kDistMax) << kDistShift |
+                                                      ((kp & kKrFirst) ? kFirst : 0u) | ((kp & kKrLast) ? kLast : 0u))
+                                                   : ((t << kTokenShift | ln | kInvalidBit) | kFirst | kLast)));
+            }
             if (kp & kKrFirst) {
-                const uint32_t b = bucket_of(keys[kp & kKrEntry]);
+                const uint32_t e = kp & kKrEntry;
+                const uint32_t key = keys[e];
+                const uint32_t b = bucket_of(key);
                 const uint32_t size = kp >> 16;
-                uint32_t base;
                 if (size >= static_cast<uint32_t>(kLongMin)) {
                     // long: its reference record in the bucket {index | kRecLong | FIRST | LAST (| ordinal),
-                    // slot, row of the sums, cpe}; its own records in the chunk's tail
+                    // slot, row of the sums, cpe}; its own records in the chunk's tail (below)
                     const uint32_t li = atomicAdd(&lcnt_s, 1u);   // < C*W / kLongMin
                     const uint32_t ref = off[b] + atomicAdd(&fill[b], 1u);
-                    base = off[B] + atomicAdd(&ltail_s, size);
+                    const uint32_t base = off[B] + atomicAdd(&ltail_s, size);
                     a.ldesc[c * a.maxL + li] = static_cast<int32_t>(base);
-                    const uint32_t e = kp & kKrEntry;
                     const uint32_t t = tok_of(e);
                     uint32_t w0 = li | kRecLong | kFirst | kLast;
                     if constexpr (ORD) {   // the group's dense ordinal (khead is complete: reverse scan)
@@ -920,17 +950,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                         for (int wi = 0; wi < (j >> 5); ++wi) g += __popc(khead[wi]);
                         w0 |= g << kRecOrdShift;
                     }
-                    st_stream(a.krec + c * a.rstride + ref,
-                              make_int4(static_cast<int>(w0), static_cast<int>(keys[e]), static_cast<int>(c * a.maxL + li),
+                    st_stream(a.krec + kbase + ref,
+                              make_int4(static_cast<int>(w0), static_cast<int>(key), static_cast<int>(c * a.maxL + li),
                                         __float_as_int(cpev[static_cast<int>(t) * W + static_cast<int>(e - t * wr)])));
+                    krpos[j] = (kp & 0xFFFFu) | base << 16 | kKrLong;   // the group's first tail record
                 } else {
-                    base = off[b] + atomicAdd(&fill[b], size);
+                    const uint32_t base = off[b] + atomicAdd(&fill[b], size);
+                    uint32_t first = kFirst;
+                    if constexpr (ORD)   // the group's dense ordinal
+                        first |= (gpre + __popc(khead[j0 >> 5] & ((1u << lane) - 1u))) << kRecOrdShift;
+                    put_record(kp, base, key, first);
+                    for (uint32_t q = 1; q < size; ++q) put_record(krpos[j + q], base + q, key, 0u);
                 }
-                krpos[j] = (kp & 0xFFFFu) | base << 16;   // FIRST: the group's first record
             }
         }
         __syncthreads();
-        const int64_t kbase = c * a.rstride;
         if constexpr (ORD) {
             if (warp == 0 && a.out.ngroups != nullptr) {   // the chunk's valid write groups
                 const int nwords = (nk + 31) >> 5;
@@ -940,39 +974,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 if (lane == 0) a.out.ngroups[c] = static_cast<int32_t>(cnt);
             }
         }
-        for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
-            zpace();
-            uint32_t gpre = 0;   // ORD: groups before this warp's word (the dense ordinal of a group starting in it)
-            if constexpr (ORD) {
-                for (int wi = lane; wi < (j0 >> 5); wi += 32) gpre += __popc(khead[wi]);
-                gpre = __reduce_add_sync(kFull, gpre);
+        if (lcnt_s != 0u) {   // long groups: every member writes its own record in the chunk's tail
+            for (int j0 = warp * 32; j0 < nk; j0 += nthr) {
+                uint32_t gpre = 0;
+                if constexpr (ORD) {
+                    for (int wi = lane; wi < (j0 >> 5); wi += 32) gpre += __popc(khead[wi]);
+                    gpre = __reduce_add_sync(kFull, gpre);
+                }
+                const int j = j0 + lane;
+                if (j >= nk) continue;
+                const uint32_t kp = krpos[j];
+                if (!(kp & kKrValid)) continue;
+                const uint32_t kb = (kp & kKrFirst) ? 0u : kp >> 16;
+                const uint32_t f = krpos[j - kb];
+                if (!(f & kKrLong)) continue;
+                uint32_t first = 0u;
+                if (kb == 0u) {
+                    first = kFirst;
+                    if constexpr (ORD) first |= (gpre + __popc(khead[j0 >> 5] & ((1u << lane) - 1u))) << kRecOrdShift;
+                }
+                put_record(kp, ((f & ~kKrLong) >> 16) + kb, keys[kp & kKrEntry], first);
             }
-            const int j = j0 + lane;
-            if (j >= nk) continue;
-            const uint32_t kp = krpos[j];
-            const uint32_t e = kp & kKrEntry;
-            const uint32_t t = tok_of(e);
-            const uint32_t ln = e - t * wr;
-            const uint32_t kb = (kp & kKrFirst) ? 0u : kp >> 16;   // valid write entries before it in the group
-            if (a.out.sorted_k != nullptr)   // the sorted write row, coalesced: its element from the word
-                st_stream(a.out.sorted_k + c * nk + j,
-                          static_cast<int32_t>((kp & kKrValid)
-                                                   ? (t << kTokenShift | ln | min(kb, kDistMax) << kDistShift |
-                                                      ((kp & kKrFirst) ? kFirst : 0u) | ((kp & kKrLast) ? kLast : 0u))
-                                                   : ((t << kTokenShift | ln | kInvalidBit) | kFirst | kLast)));
-            if (!(kp & kKrValid)) continue;   // invalid entries have no record
-            const uint32_t key = keys[e];
-            const uint32_t rec = (krpos[j - kb] >> 16) + kb;
-            const int o = static_cast<int>(t * W + ln);
-            uint32_t w0 = t | ((kp & kKrLast) ? kLast : 0u);
-            if (kb == 0u) {
-                w0 |= kFirst;
-                if constexpr (ORD)   // the group's dense ordinal
-                    w0 |= (gpre + __popc(khead[j0 >> 5] & ((1u << lane) - 1u))) << kRecOrdShift;
-            }
-            const float sc = __fmul_rn(to_f(vals[e]), expf(rexv[o]));
-            st_stream(a.krec + kbase + rec, make_int4(static_cast<int>(w0), static_cast<int>(key), __float_as_int(sc),
-                                                      __float_as_int(cpev[o])));
         }
     }
 
