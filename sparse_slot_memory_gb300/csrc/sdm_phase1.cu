@@ -11,19 +11,20 @@
 //
 // GB300 design (not the pages' kernels): the whole chunk (up to 8192 entries) stays in shared
 // memory from load to the last output byte:
-//   0. load ids and values (coalesced) into entry-indexed arrays;
-//   1. stable LSD radix sort of entry indices by slot in 4-bit digits (five passes for 2^20 slots):
-//      each lane ranks its 8 consecutive positions with digit counters in registers, one warp scan
-//      of the byte-packed counts and one block scan of the per-warp totals place them, one scatter
-//      moves a word holding the entry and the key bits still to sort (no ballots, no shared
-//      counters per item, no key gathers after the first pass, no global round trips, no merge);
+//   0. load ids, values and gates (coalesced, all of a thread's loads in flight together) into
+//      entry-indexed arrays;
+//   1. stable sort of entry indices by slot: a counting sort by the key's top bits (shared-memory
+//      bucket counts, one block scan, an atomic scatter, then each entry ranks itself inside its
+//      bucket by (key, entry)), or, when a bucket is crowded (skewed slots), an LSD radix sort in
+//      4-bit digits with per-thread digit counters;
 //   2. a forward and a reverse segmented block scan with TwoSum-compensated f32 sums (fixed
-//      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and
-//      the sorted rows in sorted order, then the DW records partitioned into hashed slot buckets;
+//      tree: bitwise reproducible), emitting the per-entry results into entry-indexed arrays and a
+//      word per write-row position; one pass over the write row then writes the sorted write row
+//      and the DW records, partitioned into hashed slot buckets;
 //   3. every entry-order output written from shared memory by consecutive threads (4 entries per
 //      thread, vector loads and stores, when W and R are multiples of 4);
-//   4. pair triangles: A and QK are zero-filled by 16-byte streaming stores of every thread, a few
-//      at each phase boundary (they drain while the sort and scans compute); then one warp per
+//   4. pair triangles: A and QK are zero-filled by 16-byte streaming stores of every thread, paced
+//      by the SM clock over phases 0-3 (a steady stream under the compute); then one warp per
 //      (row, triangle) walks: 32 earlier positions per step, lanes of one cell summed by a fixed
 //      shuffle tree, one lane adds the cell's partial to the warp's row buffer; only rows with
 //      terms are rewritten.
