@@ -69,6 +69,47 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _need(t, dtype, numel: int, name: str):
+    """A caller tensor the library reads or writes ``numel`` elements of ``dtype`` through: checked
+    here, because the C ABI takes bare pointers (a smaller or differently typed buffer would be
+    accessed out of bounds)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: expected at least {numel} elements, got {t.numel()}")
+
+
+def _need_inputs(shape: "ShapeSpec", k_idx, q_idx, k_val, q_val, g):
+    N, C, W, R = shape.N, shape.C, shape.W, shape.R
+    vt = _TORCH_DT[shape.val_dtype]
+    _need(k_idx, torch.int32, N * C * W, "k_idx")
+    _need(q_idx, torch.int32, N * C * R, "q_idx")
+    _need(k_val, vt, N * C * W, "k_val")
+    _need(q_val, vt, N * C * R, "q_val")
+    _need(g, torch.float32, N * C * (W if shape.gate_per_entry else 1), "g")
+
+
+def _need_outputs(shape: "ShapeSpec", out):
+    if not out:
+        return
+    for f, (shp, dt) in _out_spec(shape).items():
+        if out.get(f) is not None:
+            n = 1
+            for d in shp:
+                n *= d
+            _need(out[f], dt, n, f"out[{f!r}]")
+
+
+def _need_rows(shape: "ShapeSpec", dv, bank, snap=None):
+    _need(dv, _TORCH_DT[shape.dv_dtype], shape.N * shape.C * shape.hd, "dv")
+    _need(bank, _TORCH_DT[shape.bank_dtype], shape.P * shape.S * shape.hd, "bank")
+    _need(snap, _TORCH_DT[shape.bank_dtype], shape.N * shape.C * shape.W * shape.hd, "snap")
+
+
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -98,10 +139,10 @@ def alloc_workspace(shape: ShapeSpec, device="cuda", stream=None) -> torch.Tenso
 PLAIN_FIELDS = tuple(f for f in _abi.P1_FIELDS if f != "ngroups")
 
 
-def alloc_outputs(shape: ShapeSpec, device="cuda", fields=PLAIN_FIELDS) -> dict:
+def _out_spec(shape: ShapeSpec) -> dict:
     N, C, W, R = shape.N, shape.C, shape.W, shape.R
     vt = _TORCH_DT[shape.val_dtype]
-    spec = {
+    return {
         "log_k": ((N, C, W), torch.float32), "rex": ((N, C, W), torch.float32), "cpe": ((N, C, W), vt),
         "k_eff": ((N, C, W), vt), "is_last": ((N, C, W), torch.int8), "is_only": ((N, C, W), torch.int8),
         "pos_k": ((N, C, W), torch.int32), "log_q": ((N, C, R), torch.float32), "q_w": ((N, C, R), vt),
@@ -110,6 +151,10 @@ def alloc_outputs(shape: ShapeSpec, device="cuda", fields=PLAIN_FIELDS) -> dict:
         "sorted_k": ((N, C * W), torch.int32), "sorted_q": ((N, C * R), torch.int32), "repeats": ((2,), torch.int64),
         "ngroups": ((N,), torch.int32),
     }
+
+
+def alloc_outputs(shape: ShapeSpec, device="cuda", fields=PLAIN_FIELDS) -> dict:
+    spec = _out_spec(shape)
     out = {}
     for f in fields:
         shp, dt = spec[f]
@@ -127,6 +172,8 @@ def _p1out(out):
 
 
 def phase1(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws, step_begin=0, step_end=None, stream=None):
+    _need_inputs(shape, k_idx, q_idx, k_val, q_val, g)
+    _need_outputs(shape, out)
     step_end = shape.steps if step_end is None else step_end
     o = _p1out(out)
     st = _abi.load().sdm_phase1(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val), _ptr(g),
@@ -135,6 +182,7 @@ def phase1(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws, step_
 
 
 def dw(shape: ShapeSpec, dv, bank, ws, step_begin=0, step_end=None, stream=None):
+    _need_rows(shape, dv, bank)
     step_end = shape.steps if step_end is None else step_end
     st = _abi.load().sdm_dw(ctypes.byref(shape.c()), _ptr(dv), _ptr(bank), step_begin, step_end, _ptr(ws), ws.numel(),
                             _stream(stream))
@@ -143,6 +191,9 @@ def dw(shape: ShapeSpec, dv, bank, ws, step_begin=0, step_end=None, stream=None)
 
 def forward_chunks(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, out, ws, step_begin=0, step_end=None,
                    stream=None):
+    _need_inputs(shape, k_idx, q_idx, k_val, q_val, g)
+    _need_outputs(shape, out)
+    _need_rows(shape, dv, bank)
     step_end = shape.steps if step_end is None else step_end
     o = _p1out(out)
     st = _abi.load().sdm_forward_chunks(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val),
@@ -159,6 +210,8 @@ def alloc_snapshot(shape: ShapeSpec, device="cuda") -> torch.Tensor:
 def phase1_saving(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws, step_begin=0, step_end=None,
                   stream=None):
     """sdm_phase1_saving: Phase 1 whose records carry the groups' dense ordinals (for dw_saving)."""
+    _need_inputs(shape, k_idx, q_idx, k_val, q_val, g)
+    _need_outputs(shape, out)
     step_end = shape.steps if step_end is None else step_end
     o = _p1out(out)
     st = _abi.load().sdm_phase1_saving(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val), _ptr(q_val),
@@ -169,6 +222,7 @@ def phase1_saving(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, out: dict, ws
 
 def dw_saving(shape: ShapeSpec, dv, bank, snap, ws, step_begin=0, step_end=None, stream=None):
     """sdm_dw_saving: the DW, also writing each group's pre-write base row to ``snap``."""
+    _need_rows(shape, dv, bank, snap)
     step_end = shape.steps if step_end is None else step_end
     st = _abi.load().sdm_dw_saving(ctypes.byref(shape.c()), _ptr(dv), _ptr(bank), _ptr(snap), step_begin, step_end,
                                    _ptr(ws), ws.numel(), _stream(stream))
@@ -178,6 +232,9 @@ def dw_saving(shape: ShapeSpec, dv, bank, snap, ws, step_begin=0, step_end=None,
 def forward_chunks_saving(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, bank, snap, out, ws, step_begin=0,
                           step_end=None, stream=None):
     """sdm_forward_chunks_saving: Phase 1, then the DW writing the dense compact snapshot."""
+    _need_inputs(shape, k_idx, q_idx, k_val, q_val, g)
+    _need_outputs(shape, out)
+    _need_rows(shape, dv, bank, snap)
     step_end = shape.steps if step_end is None else step_end
     o = _p1out(out)
     st = _abi.load().sdm_forward_chunks_saving(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val),
@@ -191,6 +248,9 @@ def forward_chunks_noalloc(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, 
                            step_end=None, stream=None):
     """sdm_forward_chunks_noalloc: the forward on the library's own scratch (no workspace).
     ``status`` (optional) is a CUDA int32 tensor of one element that receives the device status."""
+    _need_inputs(shape, k_idx, q_idx, k_val, q_val, g)
+    _need_outputs(shape, out)
+    _need_rows(shape, dv, bank)
     step_end = shape.steps if step_end is None else step_end
     o = _p1out(out)
     st = _abi.load().sdm_forward_chunks_noalloc(ctypes.byref(shape.c()), _ptr(k_idx), _ptr(q_idx), _ptr(k_val),

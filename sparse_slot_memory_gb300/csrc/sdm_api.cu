@@ -11,7 +11,7 @@ namespace sdm {
 namespace {
 
  // DW work items (stream, slot bucket, column slice) aimed at per launch: ~3x the warps a GB300 holds.
-constexpr int64_t kDwTargetItems = 16384;
+constexpr int64_t kDwTargetItems = 32768;
 constexpr int kMaxLogBuckets = 11;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -80,7 +80,7 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     }
     g->logB = lb;
     g->B = 1 << lb;
-    // workspace: header | DW records [N, C*W] | bucket bounds [P, B + 1, steps]
+    // workspace: header | DW records [N, C*W] | bucket bounds [P, steps, B + 1]
     g->maxL = g->nk / kLongMin > 0 ? g->nk / kLongMin : 1;
     g->rstride = g->nk + g->maxL;
     if (N > (int64_t(1) << 31) / g->maxL) return SDM_ERR_SHAPE;   // long-group sum rows are int32-indexed
@@ -219,8 +219,6 @@ sdm_status run_phase1(const sdm_shape* s, const Geometry& g, const int32_t* k_id
 sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* bank, void* snap, int64_t b, int64_t e,
                   void* ws, cudaStream_t stream) {
     unsigned char* const w = static_cast<unsigned char*>(ws);
-    // the work counter starts at zero for every launch (the status word is kept)
-    if (cudaMemsetAsync(w + kHdrClaim, 0, sizeof(uint32_t), stream) != cudaSuccess) return SDM_ERR_CUDA;
     DWArgs a;
     memset(&a, 0, sizeof(a));
     a.krec = reinterpret_cast<const int4*>(w + g.krec_off);
@@ -251,6 +249,7 @@ sdm_status run_dw(const sdm_shape* s, const Geometry& g, const void* dv, void* b
     la.ldesc = reinterpret_cast<const int32_t*>(w + g.ldesc_off);
     la.dv = dv;
     la.lacc = reinterpret_cast<float*>(w + g.lacc_off);
+    la.claim = a.claim;   // the work counter starts at zero for every DW launch (the status word is kept)
     la.C = g.C;
     la.maxL = g.maxL;
     la.rstride = g.rstride;

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include <type_traits>
+#include <utility>
 
 #include "sdm_internal.cuh"
 #include "sdm_rows.cuh"
@@ -52,6 +53,11 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // groups of all steps are summed in parallel.
 template <typename DvT>
 __global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
+    // Launched as a programmatic dependent of the kernel before it (Phase 1): nothing is read or
+    // written before that grid completes and its memory is visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.claim = 0u;   // the DW's work counter (the DW waits for this grid)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t c = a.c0 + blockIdx.x;   // one block per chunk
     const int nl = a.lcnt[c];
@@ -102,6 +108,8 @@ __device__ __forceinline__ void raw_st(__nv_bfloat16* p, const rows::Raw4<__nv_b
 // SNAP: the saving forward (a.snap is the dense compact snapshot)
 template <typename BankT, typename DvT, bool SNAP>
 __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
+    // a programmatic dependent of the long-group kernel: nothing is touched before it completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int kSub = 8;   // entries per sub-batch (3 blocks of 8 warps per SM, 80 registers)
     // per warp three window buffers of 32 records (+ 8 slots read by the unrolled loads, never
     // used) and each record's first dv row (its chunk * C)
@@ -126,16 +134,17 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
         const bool active = col < a.hd;
         BankT* const bank_lane = bank + static_cast<int64_t>(p) * a.S * a.hd + col;   // stream row 0, own columns
         const DvT* const dv_lane = dv + col;
-        const int32_t* const bb0 = a.bb + (static_cast<int64_t>(p) * (a.B + 1) + b) * a.steps;
-        const int32_t* const bb1 = bb0 + a.steps;
+        // bucket bounds [P][steps][B + 1]: step t's range of bucket b is [bb0[t * (B + 1)], bb0[t * (B + 1) + 1])
+        const int32_t* const bb0 = a.bb + static_cast<int64_t>(p) * a.steps * (a.B + 1) + b;
         for (int64_t t0 = 0; t0 < nsteps; t0 += 32) {
             // The item's records of (up to) 32 steps, concatenated in step order: lane t holds
             // step t0 + t's range, cum the inclusive prefix of the counts.
             const int tn = static_cast<int>(nsteps - t0 < 32 ? nsteps - t0 : 32);
             int s0l = 0, cntl = 0;
             if (lane < tn) {
-                s0l = __ldg(bb0 + a.step_begin + t0 + lane);
-                cntl = __ldg(bb1 + a.step_begin + t0 + lane) - s0l;
+                const int32_t* const bt = bb0 + (a.step_begin + t0 + lane) * (a.B + 1);
+                s0l = __ldg(bt);
+                cntl = __ldg(bt + 1) - s0l;
             }
             int cum = cntl;
 #pragma unroll
@@ -272,6 +281,24 @@ __global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
     }
 }
 
+// A launch as a programmatic dependent of the previous kernel in the stream: its CTAs may be
+// scheduled before that kernel completes (onto SMs it leaves idle) and wait in the kernel
+// (griddepcontrol.wait) until it has completed and its memory is visible.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename BankT, typename DvT, bool SNAP>
 cudaError_t launch_t1(const DWArgs& a, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;
@@ -286,8 +313,7 @@ cudaError_t launch_t1(const DWArgs& a, cudaStream_t stream) {
     const int64_t need_blocks = (a.items + kDwWarps - 1) / kDwWarps;
     if (blocks > need_blocks) blocks = need_blocks;
     if (blocks < 1) blocks = 1;
-    dw_kernel<BankT, DvT, SNAP><<<static_cast<unsigned>(blocks), kDwThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(dw_kernel<BankT, DvT, SNAP>, dim3(static_cast<unsigned>(blocks)), dim3(kDwThreads), stream, a);
 }
 
 template <typename BankT, typename DvT>
@@ -300,11 +326,8 @@ cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
 cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream) {
     if (a.nchunks <= 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>(a.nchunks));
-    if (dv_bf16)
-        long_kernel<__nv_bfloat16><<<grid, kDwThreads, 0, stream>>>(a);
-    else
-        long_kernel<float><<<grid, kDwThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return dv_bf16 ? launch_dependent(long_kernel<__nv_bfloat16>, grid, dim3(kDwThreads), stream, a)
+                   : launch_dependent(long_kernel<float>, grid, dim3(kDwThreads), stream, a);
 }
 
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream) {

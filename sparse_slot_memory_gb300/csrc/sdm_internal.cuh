@@ -124,7 +124,7 @@ struct P1Args {
     const float* g;
     sdm_p1_out out;
     int4* krec;
-    int32_t* bb;            // [P][B + 1][steps] first record of each slot bucket, per chunk
+    int32_t* bb;            // [P][steps][B + 1] first record of each slot bucket, per chunk
     int32_t* lcnt;          // [N] long groups of each chunk
     int32_t* ldesc;         // [N][maxL] the first tail record of each long group
     int maxL, rstride;
@@ -148,7 +148,7 @@ struct P1Args {
 
 struct DWArgs {
     const int4* krec;
-    const int32_t* bb;  // [P][B + 1][steps]
+    const int32_t* bb;  // [P][steps][B + 1]
     const void* dv;
     void* bank;
     void* snap;         // dense compact snapshot [N, C*W, hd] (bank type) or null
@@ -171,6 +171,7 @@ struct LongArgs {
     const int32_t* ldesc;
     const void* dv;
     float* lacc;
+    uint32_t* claim;    // the DW's work counter, zeroed here (the DW launch follows this one)
     int C, maxL, rstride, hd, nsl;
     int64_t c0, nchunks;
 };

@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     __shared__ uint32_t khead[kMaxRow / 32];
     // long groups: count and tail fill
     __shared__ uint32_t lcnt_s, ltail_s;
+    // the long-group kernel that follows may be scheduled once every CTA of this grid runs (it waits
+    // for this grid's completion before it reads anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         lcnt_s = 0u;
@@ -886,8 +889,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- DW work split: the chunk's slot groups (valid write entries) are partitioned into B
     // buckets by a hash of the slot, each group's records contiguous and in sorted order; the order
-    // of groups inside a bucket does not matter (different slots). bb[p][b][ti] = the bucket's first
-    // record, bb[p][B][ti] = the chunk's valid write entries. Hashing spreads the hot slots of a
+    // of groups inside a bucket does not matter (different slots). bb[p][ti][b] = the bucket's first
+    // record, bb[p][ti][B] = the chunk's valid write entries (one coalesced row per chunk). Hashing spreads the hot slots of a
     // skewed stream over different DW warps.
     {
         const int B = nbk;
@@ -897,7 +900,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         __syncthreads();
         zpace();
         const int64_t p = c % a.P, ti = c / a.P;
-        for (int b = tid; b <= B; b += nthr) a.bb[(p * (B + 1) + b) * a.steps + ti] = static_cast<int32_t>(off[b]);
+        for (int b = tid; b <= B; b += nthr) a.bb[(p * a.steps + ti) * (B + 1) + b] = static_cast<int32_t>(off[b]);
         const int64_t kbase = c * a.rstride;
         // record of the write entry with word kpi at place rec: {token | LAST | extra, slot, sc, cpe}
         auto put_record = [&](uint32_t kpi, uint32_t rec, uint32_t key, uint32_t extra) {

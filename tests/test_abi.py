@@ -2,6 +2,7 @@
 declares, sizes workspaces, and rejects bad arguments before any CUDA call (no launches here)."""
 
 import ctypes
+import dataclasses
 import os
 import re
 
@@ -124,3 +125,33 @@ def test_backward_argument_errors(lib, fn, nptr):
     bad[-1] = ctypes.c_void_p(0x10000 + 8)
     assert f(ctypes.byref(s), 0, *bad, 0, 32, None, None) == -4                          # misaligned
     assert f(ctypes.byref(s), 1, *good, 3, 3, None, None) == 0                           # empty range: no launch
+
+
+def test_binding_rejects_buffers_of_the_wrong_type_or_extent():
+    """The C ABI takes bare pointers; the Python binding checks each tensor's dtype and element count
+    against the shape before any call (a bank of the wrong type once let the DW write past its end)."""
+    import torch
+
+    from sparse_slot_memory_gb300 import api
+
+    shape = api.ShapeSpec(P=1, C=64, W=4, R=4, hd=64, steps=16, S=4096, valid_last=64,
+                          val_dtype="f32", dv_dtype="f32", bank_dtype="f32")
+    dv = torch.zeros(shape.N * shape.C * shape.hd, dtype=torch.float32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(TypeError, match="bank: expected torch.float32"):
+        api.dw(shape, dv, torch.zeros(shape.P * shape.S * shape.hd, dtype=torch.bfloat16), ws)
+    with pytest.raises(ValueError, match="bank: expected at least"):
+        api.dw(shape, dv, torch.zeros(shape.P * shape.S * shape.hd - 1, dtype=torch.float32), ws)
+    with pytest.raises(TypeError, match="dv: expected torch.float32"):
+        api.dw(shape, dv.to(torch.bfloat16), torch.zeros(shape.P * shape.S * shape.hd), ws)
+    k_idx = torch.zeros(shape.N * shape.C * shape.W, dtype=torch.int32)
+    q_idx = torch.zeros(shape.N * shape.C * shape.R, dtype=torch.int32)
+    k_val = torch.zeros(shape.N * shape.C * shape.W)
+    q_val = torch.zeros(shape.N * shape.C * shape.R)
+    g = torch.zeros(shape.N * shape.C)
+    with pytest.raises(ValueError, match="g: expected at least"):
+        api.phase1(dataclasses.replace(shape, gate_per_entry=True), k_idx, q_idx, k_val, q_val, g, {}, ws)
+    with pytest.raises(TypeError, match=r"out\['A'\]: expected torch.float32"):
+        api.phase1(shape, k_idx, q_idx, k_val, q_val, g, {"A": torch.zeros(shape.N * shape.C * shape.C, dtype=torch.float64)}, ws)
+    with pytest.raises(TypeError, match="k_idx: expected torch.int32"):
+        api.forward_chunks(shape, k_idx.long(), q_idx, k_val, q_val, g, dv, torch.zeros(shape.P * shape.S * shape.hd), {}, ws)
