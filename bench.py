@@ -47,6 +47,8 @@ METRIC_GWR = "SDM backward GWR (write-side token gather) tokens/sec and achieved
 NCU_TRAFFIC = {
     "large:dw:c28e9f58496b": 1178147328 + 981000192,
     "large:phase1:6922acd872e5": 55624960 + 718927616,
+    "large:dw:1a9bec971807": 1155819008 + 961666560,
+    "large:phase1:f995602e26cb": 52393472 + 726859776,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
     "large:pa:4c47240459f4": round((106345728 + 43396352) * 4186081 / 4161534),
@@ -255,6 +257,12 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     assert sdm.device_status(ws) == 0
+    # the kernel's own counters of one Phase 1 (untimed): its valid write groups give the DW's bytes
+    sout = sdm.alloc_outputs(shape, fields=("A", "QK", "stats"))
+    p1(shape, d["k_idx"], d["q_idx"], d["k_val"], d["q_val"], d["g"], sout, ws)
+    torch.cuda.synchronize()
+    p1_stats = dict(zip(sdm.STATS, (int(v) for v in sout["stats"].cpu())))
+    del sout
 
     # timed region: K forwards back to back (the DW-side kernels launch early, as programmatic
     # dependents, and wait for their predecessor inside); then the per-kernel durations from a second
@@ -358,7 +366,8 @@ def run_ours(args):
                        "pinned host memory; steps pipelined over two buffer sets and two copy streams; the bank is "
                        "resident state; host wall clock from the first copy to the last byte home"}
 
-    groups = count_groups(x, w)
+    groups = p1_stats["groups"]
+    assert groups == count_groups(x, w), (p1_stats, count_groups(x, w))
     ab = algorithmic_bytes(w, x, groups, saving=args.saving)
     peak, peak_kind = peaks()
     dom = "dw" if dw_ms >= p1_ms else "phase1"
@@ -382,7 +391,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (8 GiB bank)"},
             "hbm_gbs_total": ab["total"] / (ms / 1e3) / 1e9,
             "kernels_ms": {"phase1": p1_ms, "dw": dw_ms},
-            "algorithmic_bytes": ab, "groups": groups,
+            "algorithmic_bytes": ab, "groups": groups, "p1_stats": p1_stats,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                          "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
                          "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": traffic,

@@ -112,6 +112,13 @@ typedef struct {
  *   ngroups [N] int32: the chunk's valid write groups (slots with at least one valid write
  *            entry), i.e. the rows of its dense compact snapshot; written only by the saving
  *            forward's Phase 1 (sdm_phase1_saving, sdm_forward_chunks_saving).
+ *   stats [4] int64: counters of the call's chunks, ADDED to (the caller zeroes them): [0] valid
+ *            write groups (slot groups with at least one valid write entry: the DW's base-row reads
+ *            and row writes), [1] slot groups whose pair terms took the dense rank-1 path, [2] pair
+ *            terms summed one by one (an entry and an earlier write entry of its group, into A or
+ *            QK), [3] A / QK rows the pair phase writes (a token's row in a triangle where one of its
+ *            entries has an earlier valid write entry in its group, or that a dense group
+ *            reaches). [1..3] are counted only when A or QK is requested. Diagnostic counters in the manner of phase1_cuda.py's repeats counter.
  * Position pack: r | min(after, 127) << 17 | min(before + 1 + min(after, 127), 127) << 24 for a
  * valid entry (r = position in the chunk's sorted row, before / after = valid entries of the
  * same kind and slot before / after it), r alone for an invalid entry. Invalid entries:
@@ -136,6 +143,7 @@ typedef struct {
     int32_t* sorted_q;
     int64_t* repeats;
     int32_t* ngroups;
+    int64_t* stats;
 } sdm_p1_out;
 
 /*

@@ -8,6 +8,7 @@ package builds that library in-tree and marshals torch CUDA tensors to it.
 
 from ._build import LIB, build  # noqa: F401
 from .api import (  # noqa: F401
+    STATS,
     SdmError,
     ShapeSpec,
     alloc_outputs,

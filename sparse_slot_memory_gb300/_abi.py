@@ -28,7 +28,7 @@ class Shape(ctypes.Structure):
 
 
 P1_FIELDS = ("log_k", "rex", "cpe", "k_eff", "is_last", "is_only", "pos_k", "log_q", "q_w", "pos_q", "q_last",
-             "q_only", "A", "QK", "sorted_k", "sorted_q", "repeats", "ngroups")
+             "q_only", "A", "QK", "sorted_k", "sorted_q", "repeats", "ngroups", "stats")
 
 
 class P1Out(ctypes.Structure):

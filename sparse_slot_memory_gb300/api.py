@@ -135,8 +135,11 @@ def alloc_workspace(shape: ShapeSpec, device="cuda", stream=None) -> torch.Tenso
     return ws
 
 
-# every Phase-1 output but ngroups (written only by the saving forward's Phase 1)
-PLAIN_FIELDS = tuple(f for f in _abi.P1_FIELDS if f != "ngroups")
+# every Phase-1 output but ngroups (written only by the saving forward's Phase 1) and the
+# diagnostic counters (stats: ask for them by name)
+PLAIN_FIELDS = tuple(f for f in _abi.P1_FIELDS if f not in ("ngroups", "stats"))
+# stats[i]: valid write groups, dense (rank-1) pair groups, exact pair terms, A / QK rows with terms
+STATS = ("groups", "dense_groups", "pair_terms", "rows_with_terms")
 
 
 def _out_spec(shape: ShapeSpec) -> dict:
@@ -149,7 +152,7 @@ def _out_spec(shape: ShapeSpec) -> dict:
         "pos_q": ((N, C, R), torch.int32), "q_last": ((N, C, R), torch.int8), "q_only": ((N, C, R), torch.int8),
         "A": ((N, C, C), torch.float32), "QK": ((N, C, C), torch.float32),
         "sorted_k": ((N, C * W), torch.int32), "sorted_q": ((N, C * R), torch.int32), "repeats": ((2,), torch.int64),
-        "ngroups": ((N,), torch.int32),
+        "ngroups": ((N,), torch.int32), "stats": ((4,), torch.int64),
     }
 
 
@@ -158,7 +161,8 @@ def alloc_outputs(shape: ShapeSpec, device="cuda", fields=PLAIN_FIELDS) -> dict:
     out = {}
     for f in fields:
         shp, dt = spec[f]
-        out[f] = torch.zeros(shp, dtype=dt, device=device) if f == "repeats" else torch.empty(shp, dtype=dt, device=device)
+        out[f] = (torch.zeros(shp, dtype=dt, device=device) if f in ("repeats", "stats")
+                  else torch.empty(shp, dtype=dt, device=device))
     return out
 
 

@@ -306,12 +306,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     __shared__ uint32_t khead[kMaxRow / 32];
     // long groups: count and tail fill
     __shared__ uint32_t lcnt_s, ltail_s;
+    __shared__ uint32_t ngroups_s;   // valid write groups (out.stats)
     // the long-group kernel that follows may be scheduled once every CTA of this grid runs (it waits
     // for this grid's completion before it reads anything)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         lcnt_s = 0u;
+        ngroups_s = 0u;
         ltail_s = 0u;
         row_claim = 0u;
     }
@@ -924,6 +926,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 gpre = __reduce_add_sync(kFull, gpre);
             }
             const uint32_t kp = j < nk ? krpos[j] : 0u;
+            if (a.out.stats != nullptr) {   // this warp's group heads
+                const uint32_t hm = __ballot_sync(kFull, (kp & kKrFirst) != 0u);
+                if (lane == 0 && hm != 0u) atomicAdd(&ngroups_s, static_cast<uint32_t>(__popc(hm)));
+            }
             if (j < nk && a.out.sorted_k != nullptr) {
                 const uint32_t e = kp & kKrEntry;
                 const uint32_t t = tok_of(e);
@@ -1101,6 +1107,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
 
     // ---- 4. pair triangles --------------------------------------------------------------------------
     if (tid == 0) a.lcnt[c] = static_cast<int32_t>(lcnt_s);   // final since the DW split's barrier
+    if (tid == 0 && a.out.stats != nullptr && ngroups_s != 0u)
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.out.stats), static_cast<unsigned long long>(ngroups_s));
     if (a.out.A == nullptr && a.out.QK == nullptr) return;
     while (zero_next < zka + zkq) zero_store();   // the units left; the barrier orders them before the rows' stores
     __syncthreads();   // the key array becomes the row buffers
@@ -1219,6 +1227,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
     }
     __syncthreads();
+    if (tid == 0 && a.out.stats != nullptr && nhot > 0) {   // the groups that took the dense path
+        uint32_t nd = 0;
+        for (int h = 0; h < nhot; ++h) nd += meta[h].ok ? 1u : 0u;
+        if (nd != 0u) atomicAdd(reinterpret_cast<unsigned long long*>(a.out.stats) + 1, static_cast<unsigned long long>(nd));
+    }
     // Only rows flagged in the scan (an entry with an earlier write entry in its group) have
     // terms. Lane u < 2 * mwords holds flag word u (A rows, then QK rows); a warp prefix of the
     // words' counts locates the j-th flagged (triangle, row) pair without any walk over the others.
@@ -1233,6 +1246,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     const uint32_t fexcl = fincl - __popc(fw);
     const uint32_t nflag = __shfl_sync(kFull, fincl, 31);
     // warps take the flagged pairs from a counter (rows differ in work: skewed chunks balance)
+    uint32_t nterm = 0, nrow = 0;   // out.stats: exact pair terms and rows written by this warp
     for (;;) {
         uint32_t jf = 0;
         if (lane == 0) jf = atomicAdd(&row_claim, 1u);
@@ -1277,6 +1291,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                     const bool incl = in && (met + before_me < kb);
                     const int tf = incl ? static_cast<int>(tok_of(f)) : -1;
                     float v = 0.f;
+                    if (a.out.stats != nullptr) nterm += __popc(__ballot_sync(kFull, incl && isk && (qk || tf != i)));
                     if (incl && isk && (qk || tf != i)) {
                         v = __fmul_rn(__fmul_rn(ve, to_f(vals[f])), expf(__fsub_rn(lge, lv[f])));
                     }
@@ -1330,6 +1345,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         }
         __syncwarp();
         if (!any) continue;   // the row stays as the zero fill left it
+        ++nrow;
         float* const row = outp + (c * C + i) * static_cast<int64_t>(C);
         if (vec4) {
             for (int j = lane * 4; j < C; j += 128)
@@ -1338,6 +1354,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
             for (int j = lane; j < C; j += 32) __stcs(row + j, rowbuf[j]);
         }
         __syncwarp();
+    }
+    if (a.out.stats != nullptr && lane == 0) {
+        unsigned long long* const st = reinterpret_cast<unsigned long long*>(a.out.stats);
+        if (nterm != 0u) atomicAdd(st + 2, static_cast<unsigned long long>(nterm));
+        if (nrow != 0u) atomicAdd(st + 3, static_cast<unsigned long long>(nrow));
     }
 }
 

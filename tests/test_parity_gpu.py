@@ -67,6 +67,54 @@ def test_phase1_parity(name):
     print(name, rep)
 
 
+def _expected_stats(x, w):
+    """The Phase-1 counters from their definitions, by plain loops over each chunk's valid entries
+    in entry order (the stable sort keeps it inside a slot group): valid write groups; pair terms
+    (a write entry with an earlier valid write entry of another token: A; a read entry with an
+    earlier valid write entry: QK); rows the pair phase writes (a token with an entry that has an
+    earlier valid write entry in its group, per triangle)."""
+    P, W, R = x["P"], w.W, w.R
+    groups = terms = rows = 0
+    for c in range(x["k_idx"].shape[0]):
+        V = w.valid_last if c // P == w.steps - 1 else w.C
+        seen = {}   # slot -> tokens of its valid write entries so far, in entry order
+        arow, qrow = set(), set()
+        for t in range(V):
+            for a in range(W):
+                s_ = int(x["k_idx"][c][t, a])
+                if 0 <= s_ < w.S:
+                    prev = seen.setdefault(s_, [])
+                    terms += sum(1 for tf in prev if tf != t)
+                    if prev:
+                        arow.add(t)
+                    prev.append(t)
+            for b in range(R):
+                s_ = int(x["q_idx"][c][t, b])
+                if 0 <= s_ < w.S and seen.get(s_):
+                    terms += len(seen[s_])
+                    qrow.add(t)
+        groups += len(seen)
+        rows += len(arow) + len(qrow)
+    return groups, terms, rows
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform_c128", "few_slots", "c1_w1_r1", "bf16_hd4_ragged", "tiny_pe",
+                                  "many_hot"])
+def test_phase1_stats(name):
+    """out.stats against the counts of the definitions; with dense groups (many_hot) the groups
+    exactly and the dense count positive (their pairs are then not counted one by one)."""
+    w, x, shape, d, ws = _setup(name)
+    out = run_phase1(shape, d, ws, fields=("A", "QK", "stats"))
+    st = [int(v) for v in host(out["stats"])]
+    groups, terms, rows = _expected_stats(x, w)
+    assert st[0] == groups, (st, groups)
+    if name in ("many_hot", "few_slots"):   # dense groups: their pairs are not counted one by one, and a
+        assert st[1] > 0 and st[2] < terms and st[3] >= rows, (st, terms, rows)   # row they reach is written
+    else:
+        assert st[1] == 0 and st[2] == terms and st[3] == rows, (st, terms, rows)
+    print(name, dict(zip(sdm.STATS, st)))
+
+
 def _init_bank(w, P):
     """Initial bank rows of every stream as float32 [P, S, hd] (exact for either bank type)."""
     rows = []
@@ -265,8 +313,9 @@ def test_host_checks_before_launch():
     with pytest.raises(sdm.SdmError) as e:
         sdm.dw(shape, d["dv"], bank, ws[:1024], 0, 1)
     assert e.value.status == -5
+    big = torch.zeros(w.P * w.S * w.hd + 64, device="cuda")   # a full-size bank one element off alignment
     with pytest.raises(sdm.SdmError) as e:
-        sdm.dw(shape, d["dv"], bank.view(-1)[1:1 + w.P * w.S * w.hd - 64].view(-1, w.hd), ws, 0, 1)
+        sdm.dw(shape, d["dv"], big[1:1 + w.P * w.S * w.hd].view(-1, w.hd), ws, 0, 1)
     assert e.value.status == -4
     with pytest.raises(sdm.SdmError) as e:
         sdm.dw(shape, d["dv"], bank, ws, 2, 1)

@@ -141,10 +141,12 @@ def test_saving_argument_errors():
     w = CASES["tiny"]
     shape = sdm.ShapeSpec.from_workload(w)
     ws = sdm.alloc_workspace(shape)
-    one = torch.zeros(64, device="cuda")
+    dv = torch.zeros(shape.N * shape.C * shape.hd, device="cuda")
+    bank = torch.zeros(shape.P * shape.S * shape.hd, device="cuda")
+    snap = torch.zeros(shape.N * shape.C * shape.W * shape.hd + 64, device="cuda")
     with pytest.raises(sdm.SdmError) as e:
-        sdm.dw_saving(shape, one, one, None, ws)
+        sdm.dw_saving(shape, dv, bank, None, ws)
     assert e.value.status == -1
-    with pytest.raises(sdm.SdmError) as e:
-        sdm.dw_saving(shape, one, one, one[1:], ws)
+    with pytest.raises(sdm.SdmError) as e:   # a full-size snapshot one element off alignment
+        sdm.dw_saving(shape, dv, bank, snap[1:], ws)
     assert e.value.status == -4
