@@ -5,8 +5,8 @@ TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the b
 CPU-baseline leg may import this package. It shares no code with the CUDA path and never
 imports it. The forward's arithmetic lives in ``sdm_oracle.c`` (plain C, float64, straight
 loops); this module builds it with the host C compiler on first use and marshals numpy arrays.
-``snapshot_slots``, ``pa_chunk`` (Phase A), ``gwr_chunk`` (GWR) and ``gds_chunk`` (GDS) are plain numpy /
-Python loops here.
+``snapshot_slots``, ``pa_chunk`` (Phase A), ``gwr_chunk`` (GWR), ``gds_chunk`` (GDS) and ``read_chunk`` (the
+forward's read-side gather) are plain numpy / Python loops here.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against brute-force and closed-form
 definitions (pair sums over lane pairs, the token-sequential bank recurrence, sort positions by
@@ -15,7 +15,9 @@ single-entry closed form, linearity and the cpe_last rule; for GDS a hand-worked
 adjoint identity between the scatter and the weighted read, and the vector-Jacobian product of a
 plain read loop; for GWR a hand-worked chunk and a
 dense gather matrix applied by a library matmul; GWR and Phase A's decay term also as the
-vector-Jacobian products of the forward DW oracle in the token rows and in the base rows).
+vector-Jacobian products of the forward DW oracle in the token rows and in the base rows; for the
+read a hand-worked chunk, a dense gather matrix applied by a library matmul, and the adjoint
+identity with the GDS dots).
 """
 
 from __future__ import annotations
@@ -319,3 +321,28 @@ def gwr_chunk(grad, k_idx_c, write_w_c, dv_c, *, S, V):
                 d_k_pd[t, n] = float(np.dot(dv_c[t], grad[s]))
                 dmag[t, n] = float(np.sum(np.abs(dv_c[t] * grad[s])))
     return d_delta_v, d_k_pd, mag, dmag
+
+
+def read_chunk(bank, q_idx_c, q_w_c, *, S, V):
+    """The forward's read-side token gather for one chunk: the weighted read of the bank rows at the
+    chunk's read entries, the operand of the GDS dots (mover_da2_cuda.py, module docstring: GDS
+    d_q_w[t, r] = <gr[t], bank[slot]>, the vector-Jacobian product of this read in q_w; the same
+    token_gather form as GWR's d_delta_v in pa_dc_cuda.py's module docstring). Float64, plain loops
+    over tokens and their read lanes in order.
+
+    For every valid token t < V: y[t] = sum over lanes r of q_w[t, r] * bank[q_idx[t, r]] (ids outside
+    [0, S) add nothing); padding tokens get zeros. Inputs: bank [S, hd] (the rows as they are before
+    the chunk's DW), q_idx_c / q_w_c [C, R]. Returns (y [C, hd], mag [C, hd]): mag = sum |q_w * bank
+    row| per token (tolerance bookkeeping).
+    """
+    C, R = q_idx_c.shape
+    hd = bank.shape[1]
+    y = np.zeros((C, hd))
+    mag = np.zeros((C, hd))
+    for t in range(V):
+        for r in range(R):
+            s = int(q_idx_c[t, r])
+            if 0 <= s < S:
+                y[t] += float(q_w_c[t, r]) * bank[s]
+                mag[t] += np.abs(float(q_w_c[t, r]) * bank[s])
+    return y, mag

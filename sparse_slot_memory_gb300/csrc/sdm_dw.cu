@@ -36,7 +36,7 @@ namespace sdm {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kDwThreads = 256;
+constexpr int kDwThreads = 224;   // 7 warps: 4 blocks (28 warps) per SM at <= 72 registers
 constexpr int kDwWarps = kDwThreads / 32;
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -107,10 +107,10 @@ __device__ __forceinline__ void raw_st(__nv_bfloat16* p, const rows::Raw4<__nv_b
 
 // SNAP: the saving forward (a.snap is the dense compact snapshot)
 template <typename BankT, typename DvT, bool SNAP>
-__global__ void __launch_bounds__(kDwThreads, 3) dw_kernel(const DWArgs a) {
+__global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
     // a programmatic dependent of the long-group kernel: nothing is touched before it completes
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    constexpr int kSub = 8;   // entries per sub-batch (3 blocks of 8 warps per SM, 80 registers)
+    constexpr int kSub = 8;   // entries per sub-batch (4 blocks of 7 warps per SM, 72 registers)
     // per warp three window buffers of 32 records (+ 8 slots read by the unrolled loads, never
     // used) and each record's first dv row (its chunk * C)
     __shared__ __align__(16) int4 recs_s[kDwWarps][3][40];

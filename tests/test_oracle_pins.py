@@ -748,3 +748,63 @@ def test_gds_is_the_vjp_of_the_weighted_read():
     dq, *_ = oracle.gds_chunk(grad, bank, q_idx, q_val, log_q, gr, S=S, V=V)
     assert np.allclose(grad, d_bank, rtol=1e-9, atol=1e-9)
     assert np.allclose(dq, d_qw, rtol=1e-9, atol=1e-9)
+
+
+# ---- the forward's read-side gather (oracle.read_chunk) ------------------------------------------
+
+def test_read_hand_chunk_golden():
+    """The hand-worked chunk of tests/golden/hand_read_chunk.json (expressions evaluated here)."""
+    fx = json.load(open(os.path.join(HERE, "golden", "hand_read_chunk.json")))
+    y, _ = oracle.read_chunk(np.array(fx["bank"]), np.array(fx["q_idx"], np.int32), np.array(fx["q_w"]),
+                             S=fx["S"], V=fx["V"])
+    want = np.array([[eval(e) for e in row] for row in fx["y"]])   # noqa: S307 (fixture arithmetic)
+    assert np.array_equal(y, want), (y, want)
+
+
+def _read_by_matrix(bank, q_idx, q_w, S, V):
+    """The read as one dense gather matrix G [C, S] (G[t, s] = sum of token t's q_w on slot s) applied
+    to the bank by a library matmul."""
+    C, R = q_idx.shape
+    G = np.zeros((C, S))
+    for t in range(V):
+        for r in range(R):
+            if 0 <= q_idx[t, r] < S:
+                G[t, q_idx[t, r]] += q_w[t, r]
+    return G @ bank
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_read_equals_a_dense_gather_matrix(seed):
+    rng = np.random.default_rng(seed)
+    S, C, R, hd, V = 11, 9, 5, 6, 7
+    q_idx = rng.integers(-1, S + 2, size=(C, R)).astype(np.int32)   # some ids outside [0, S)
+    q_w, bank = rng.standard_normal((C, R)), rng.standard_normal((S, hd))
+    y, mag = oracle.read_chunk(bank, q_idx, q_w, S=S, V=V)
+    assert np.allclose(y, _read_by_matrix(bank, q_idx, q_w, S, V), rtol=1e-12, atol=1e-12)
+    assert np.all(mag >= np.abs(y) - 1e-12) and np.all(y[V:] == 0.0)
+
+
+def test_read_is_the_adjoint_of_the_gds_dots():
+    """<gr, read(q_w)> = sum_{t, r} d_q_w[t, r] q_w[t, r], d_q_w the GDS dots of the same chunk (GDS is
+    pinned on its own: hand chunk, VJP of a plain read loop)."""
+    rng = np.random.default_rng(7)
+    S, C, R, hd, V = 8, 6, 4, 5, 5
+    q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
+    q_val, log_q = rng.standard_normal((C, R)), -rng.random((C, R))
+    gr, bank = rng.standard_normal((C, hd)), rng.standard_normal((S, hd))
+    q_w = q_val * np.exp(log_q)
+    y, _ = oracle.read_chunk(bank, q_idx, q_w, S=S, V=V)
+    d_q_w, *_ = oracle.gds_chunk(np.zeros((S, hd)), bank, q_idx, q_val, log_q, gr, S=S, V=V)
+    assert np.isclose(float(np.sum(gr * y)), float(np.sum(d_q_w * q_w)), rtol=1e-12, atol=1e-12)
+
+
+def test_planted_read_mistakes_fail_the_pins():
+    """A read that takes the next lane's slot, or drops the last lane, fails the matrix pin."""
+    rng = np.random.default_rng(3)
+    S, C, R, hd, V = 9, 6, 4, 3, 6
+    q_idx = rng.integers(0, S, size=(C, R)).astype(np.int32)
+    q_w, bank = rng.standard_normal((C, R)), rng.standard_normal((S, hd))
+    ref = _read_by_matrix(bank, q_idx, q_w, S, V)
+    shifted = oracle.read_chunk(bank, np.roll(q_idx, 1, axis=1), q_w, S=S, V=V)[0]
+    dropped = oracle.read_chunk(bank, np.where(np.arange(R) == R - 1, -1, q_idx), q_w, S=S, V=V)[0]
+    assert not np.allclose(shifted, ref) and not np.allclose(dropped, ref)
