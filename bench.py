@@ -40,6 +40,7 @@ METRIC_FWD = "SDM forward (Phase1+DW) tokens/sec and achieved HBM GB/s vs GB300 
 METRIC_PA = "SDM backward Phase A (the backward of DW) tokens/sec and achieved HBM GB/s vs GB300 peak"
 METRIC_GDS = "SDM backward GDS (read-side dots + grad scatter) tokens/sec and achieved HBM GB/s vs GB300 peak"
 METRIC_GWR = "SDM backward GWR (write-side token gather) tokens/sec and achieved HBM GB/s vs GB300 peak"
+METRIC_READ = "SDM forward read-side gather tokens/sec and achieved HBM GB/s vs GB300 peak"
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload, kernel and the
 # hash of the kernel's CUDA sources at capture time. A source change voids the figure: the bench
@@ -990,6 +991,182 @@ def run_gwr(args):
     return result
 
 
+def read_algorithmic_bytes(w, x):
+    """Bytes of one read pass over every step: per token its R ids and weights and its f32 output row;
+    per read entry of a valid token with an id in [0, S) one bank row."""
+    vt = 2 if w.val_dtype == "bf16" else 4
+    bt = 2 if w.bank_dtype == "bf16" else 4
+    ids = x["q_idx"]
+    P = x["P"]
+    rows = 0
+    for c in range(ids.shape[0]):
+        V = w.valid_last if c // P == w.steps - 1 else w.C
+        q = ids[c][:V]
+        rows += int(((q >= 0) & (q < w.S)).sum())
+    tok = w.N * w.C
+    return tok * (w.R * (4 + vt) + w.hd * 4) + rows * w.hd * bt
+
+
+def read_cpu_baseline(w, x, qw, budget_s=12.0, max_chunks=None):
+    """The oracle's read as it stands (float64, single thread) on a bounded sample: the chunks of stream
+    0 on the rows that stream reads. ``x`` / ``qw`` hold stream 0 alone."""
+    import oracle
+
+    C = w.C
+    ids = x["q_idx"].ravel()
+    slots = np.unique(ids[ids >= 0])
+    bank = np.random.default_rng(7).standard_normal((len(slots), w.hd))
+    qwf = oracle.as_f64(qw, w.val_dtype)
+    t0 = time.perf_counter()
+    chunks = 0
+    for ti in range(w.steps):
+        V = w.valid_last if ti == w.steps - 1 else C
+        kk = np.searchsorted(slots, x["q_idx"][ti]).astype(np.int32)
+        kk[x["q_idx"][ti] < 0] = -1
+        oracle.read_chunk(bank, kk, qwf[ti], S=len(slots), V=V)
+        chunks += 1
+        if time.perf_counter() - t0 > budget_s or (max_chunks and chunks >= max_chunks):
+            break
+    dt = time.perf_counter() - t0
+    toks = chunks * C
+    return {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks ({toks} tokens) of stream 0: the read gather, float64, {dt:.1f} s single-threaded"}
+
+
+def run_read(args):
+    """The forward's read-side gather over every step: one bench step = sdm_read of each step in turn
+    (one launch per step, as the forward runs it before each step's DW). Read ids are the workload's,
+    weights from the seeded generator in the value dtype, bank rows normal in the bank dtype."""
+    import torch
+
+    import sparse_slot_memory_gb300 as sdm
+    from synth import make_read_weights
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sdm.build()
+    w = WORKLOADS[args.workload]
+    if args.streams:
+        w = scaled(w, P=args.streams)
+    if args.slots:
+        w = scaled(w, S=args.slots)
+    x = make_inputs(w)
+    shape = sdm.ShapeSpec.from_workload(w)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.cuda()
+
+    d = {"q_idx": dev(x["q_idx"], "i"), "q_w": dev(make_read_weights(w), w.val_dtype)}
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5000 + w.seed + rank)
+    bank = (torch.randn(w.P * w.S, w.hd, device="cuda", generator=gen) * w.bank_scale).to(
+        torch.bfloat16 if w.bank_dtype == "bf16" else torch.float32)
+    y = torch.empty((w.N, w.C, w.hd), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for t in range(w.steps):
+            sdm.read(shape, d["q_idx"], d["q_w"], bank, y, t, t + 1, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        h0 = time.time()
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        clk.mark(h0, time.time())
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = valid_tokens(w, w.P)
+    value = tokens * world / (ms / 1e3)
+
+    # End to end with host buffers: per pass the ids and weights H2D from pinned memory, the pass, the
+    # output D2H; bank rows resident.
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v) for k, v in d.items()}
+        y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = y_h.numel() * y_h.element_size()
+
+        def e2e_step():
+            for k, v in pin.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            y_h.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n2 = max(3, min(args.steps, 8))
+        a0 = time.perf_counter()
+        for _ in range(n2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = (time.perf_counter() - a0) * 1e3 / n2
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "per pass: ids and weights H2D from pinned host memory, the pass, the output D2H; one "
+                       "stream; bank rows resident; host wall clock"}
+
+    peak, peak_kind = peaks()
+    ab = read_algorithmic_bytes(w, x)
+    kern_ms = ms / w.steps
+    achieved = ab / w.steps / (kern_ms / 1e3) / 1e9
+    key = f"{args.workload}:read:{src_hash('read')}"
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            cpu = cpu_baselines("read", args, w, read_cpu_baseline(w, make_inputs(w, streams=[0]),
+                                                                   make_read_weights(w, streams=[0]),
+                                                                   budget_s=args.cpu_seconds))
+        result = {
+            "metric": METRIC_READ,
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generators)",
+            "config": {"workload": w.name + "+read", **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "tokens_per_step_per_gpu": tokens, "parallelism": f"replicas x{world} (independent streams)",
+                       "l2": "inputs larger than L2"},
+            "kernels_ms": {"read_per_launch": kern_ms}, "algorithmic_bytes": ab,
+            "roofline": {"bound": "hbm", "kernel": "read", "achieved": achieved, "peak": peak,
+                         "peak_kind": f"{peak_kind} (hbm copy GB/s)", "unit": "GB/s", "frac": achieved / peak,
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS, "traffic": NCU_TRAFFIC.get(key),
+                         "traffic_source": traffic_source(key, NCU_TRAFFIC.get(key))},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": w.steps * args.steps,
+            "clocks": clk.summary(ms * args.steps), "impl": "ours",
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
 def cpu_baseline(w, x, budget_s=15.0, max_chunks=None):
     """The oracle as it stands (float64, single thread) on a bounded sample: whole steps of one
     stream (Phase 1 with the pair triangles, then DW), until ~budget_s seconds have passed."""
@@ -1067,6 +1244,9 @@ def _stream_sample(job):
         elif kind == "gwr":
             from synth import make_write_weights
             extra = make_write_weights(w, streams=[p])
+        elif kind == "read":
+            from synth import make_read_weights
+            extra = make_read_weights(w, streams=[p])
         _WORKER[key] = (w, x, extra)
     w, x, extra = _WORKER[key]
     if kind == "pa":
@@ -1075,6 +1255,8 @@ def _stream_sample(job):
         return gds_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
     if kind == "gwr":
         return gwr_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
+    if kind == "read":
+        return read_cpu_baseline(w, x, extra, budget_s=budget, max_chunks=mc)
     return cpu_baseline(w, x, budget_s=budget, max_chunks=mc)
 
 
@@ -1117,7 +1299,7 @@ def cpu_baselines(kind: str, args, w, single: dict) -> dict:
 
 
 def run_reference(args):
-    """The reference arm: the float64 oracle of the same mode (forward, or --pa / --gds / --gwr) on
+    """The reference arm: the float64 oracle of the same mode (forward, or --pa / --gds / --gwr / --read) on
     bounded samples of the same workload, on this host's cores; rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -1130,9 +1312,11 @@ def run_reference(args):
         metric, name = METRIC_GDS, w.name + "+gds" + grad_sfx
     elif args.gwr:
         metric, name = METRIC_GWR, w.name + "+gwr" + grad_sfx
+    elif args.read:
+        metric, name = METRIC_READ, w.name + "+read"
     else:
         metric, name = METRIC_FWD, w.name
-    kind = "pa" if args.pa else "gds" if args.gds else "gwr" if args.gwr else "fwd"
+    kind = "pa" if args.pa else "gds" if args.gds else "gwr" if args.gwr else "read" if args.read else "fwd"
     pool = CpuPool(kind, args.workload, (), w.P)   # every host core, one stream each
     try:
         for _ in range(args.warmup):
@@ -1173,6 +1357,7 @@ def main():
     ap.add_argument("--pa", action="store_true", help="time the backward's Phase A over every step instead")
     ap.add_argument("--gds", action="store_true", help="time the backward's GDS (read side) over every step instead")
     ap.add_argument("--gwr", action="store_true", help="time the backward's GWR (write-side gather) over every step")
+    ap.add_argument("--read", action="store_true", help="time the forward's read-side gather over every step")
     ap.add_argument("--pa-grad", default="f32", choices=["f32", "bf16"], help="grad row format of --pa / --gds")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -1183,6 +1368,8 @@ def main():
         run_gds(args)
     elif args.gwr:
         run_gwr(args)
+    elif args.read:
+        run_read(args)
     else:
         run_ours(args)
 

@@ -250,6 +250,28 @@ sdm_status sdm_forward_chunks_noalloc(const sdm_shape* shape, const int32_t* k_i
                                       int32_t* status_out, sdm_stream_t stream);
 
 /*
+ * The forward's read-side token gather (mover_fx_cuda.py: fx_fwd_steps, each step's gather before its
+ * dual matmul and DW; the weighted read whose vector-Jacobian product in q_w is the GDS dot
+ * d_q_w[t, r] = <gr[t], bank[slot]> of mover_da2_cuda.py's module docstring; the token_gather form of
+ * GWR's d_delta_v, pa_dc_cuda.py's module docstring), for every chunk c = ti * P + p of steps
+ * [step_begin, step_end):
+ *   y[c, t] = acc, acc = 0; acc = fmaf(q_w[c, t, r], bank[p*S + q_idx[c, t, r]], acc) over the read
+ *   lanes r = 0 .. R-1 in order (float32; a lane whose id lies outside [0, S) adds nothing) for valid
+ *   tokens t; padding tokens (t >= valid_last in the last step) get zeros.
+ *   q_idx [N, C, R] int32, q_w [N, C, R] val_dtype (Phase 1's q_w output, or any weights),
+ *   bank [P*S, hd] bank_dtype, read only: the rows as they are when the kernel runs, so a range of
+ *   several steps reads one bank state (the forward's order is the caller's: the read of step t, then
+ *   the DW of step t); y [N, C, hd] float32, only the range's chunks written. The pages' "dual matmul"
+ *   (the chunk-internal part of the read, from A / QK) is not printed there and is not provided.
+ *   status (nullable): SDM_DEV_BAD_SLOT is OR-ed when a valid token reads an id outside [0, S).
+ * Errors: the shape's (SDM_ERR_SHAPE / DTYPE / ALIGN for hd % 4), SDM_ERR_ARG (step range, null
+ * q_idx / q_w / bank / y), SDM_ERR_ALIGN (bank or y not 16-byte aligned), before any launch.
+ * One launch (resident warps looping over (token, 128-column slice) units).
+ */
+sdm_status sdm_read(const sdm_shape* shape, const int32_t* q_idx, const void* q_w, const void* bank, float* y,
+                    int64_t step_begin, int64_t step_end, uint32_t* status, sdm_stream_t stream);
+
+/*
  * Phase A of the backward (pa_dc_cuda.py, module docstring: "PA per write group"; records kernel):
  * the backward of DW for the steps [step_begin, step_end), LAST step first (one launch per step;
  * step ti reads the grad rows step ti + 1 wrote). Per valid write group of chunk c = ti * P + p

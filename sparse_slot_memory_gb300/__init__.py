@@ -25,5 +25,6 @@ from .api import (  # noqa: F401
     pa,
     phase1,
     phase1_saving,
+    read,
     workspace_bytes,
 )

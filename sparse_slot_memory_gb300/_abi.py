@@ -15,7 +15,7 @@ SDM_DEV_BAD_SLOT = 0x1
 
 # every symbol include/sdm.h declares
 EXPORTS = ("sdm_workspace_bytes", "sdm_workspace_init", "sdm_phase1", "sdm_dw", "sdm_forward_chunks",
-           "sdm_phase1_saving", "sdm_dw_saving", "sdm_forward_chunks_saving", "sdm_forward_chunks_noalloc", "sdm_pa", "sdm_gwr", "sdm_gds",
+           "sdm_phase1_saving", "sdm_dw_saving", "sdm_forward_chunks_saving", "sdm_forward_chunks_noalloc", "sdm_read", "sdm_pa", "sdm_gwr", "sdm_gds",
            "sdm_device_status",
            "sdm_status_string")
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -69,6 +69,8 @@ def load(path: str = LIB):
     lib.sdm_forward_chunks_noalloc.argtypes = [sp, c_p, c_p, c_p, c_p, c_p, c_p, c_p, op, c_i64, c_i64, c_p, c_p]
     lib.sdm_pa.restype = c_i32
     lib.sdm_pa.argtypes = [sp, c_i32] + [c_p] * 12 + [c_i64, c_i64, c_p, c_p]
+    lib.sdm_read.restype = c_i32
+    lib.sdm_read.argtypes = [sp] + [c_p] * 4 + [c_i64, c_i64, c_p, c_p]
     lib.sdm_gwr.restype = c_i32
     lib.sdm_gwr.argtypes = [sp, c_i32] + [c_p] * 6 + [c_i64, c_i64, c_p, c_p]
     lib.sdm_gds.restype = c_i32

@@ -264,6 +264,22 @@ def forward_chunks_noalloc(shape: ShapeSpec, k_idx, q_idx, k_val, q_val, g, dv, 
     _check(st, "sdm_forward_chunks_noalloc")
 
 
+def read(shape: ShapeSpec, q_idx, q_w, bank, y, step_begin=0, step_end=None, status=None, stream=None):
+    """sdm_read: the forward's read-side token gather of steps [step_begin, step_end):
+    y[c, t] = sum over read lanes (in order, float32) of q_w[c, t, r] * bank[p*S + q_idx[c, t, r]].
+    ``bank`` is read as it is (run it for a step before that step's DW); ``y`` is [N, C, hd] float32;
+    ``status`` (optional) is a CUDA int32 tensor of one element to which SDM_DEV_* bits are OR-ed."""
+    N, C, R = shape.N, shape.C, shape.R
+    _need(q_idx, torch.int32, N * C * R, "q_idx")
+    _need(q_w, _TORCH_DT[shape.val_dtype], N * C * R, "q_w")
+    _need(bank, _TORCH_DT[shape.bank_dtype], shape.P * shape.S * shape.hd, "bank")
+    _need(y, torch.float32, N * C * shape.hd, "y")
+    step_end = shape.steps if step_end is None else step_end
+    st = _abi.load().sdm_read(ctypes.byref(shape.c()), _ptr(q_idx), _ptr(q_w), _ptr(bank), _ptr(y), step_begin,
+                              step_end, _ptr(status), _stream(stream))
+    _check(st, "sdm_read")
+
+
 def pa(shape: ShapeSpec, sorted_k, k_idx, k_val, log_k, cpe, beta, dva, grad, bank, snap, d_k_eff, grad_g,
        step_begin=0, step_end=None, status=None, stream=None):
     """sdm_pa: Phase A of the backward for steps [step_begin, step_end), last step first.

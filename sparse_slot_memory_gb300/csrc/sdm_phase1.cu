@@ -23,7 +23,7 @@
 //      and the DW records, partitioned into hashed slot buckets;
 //   3. every entry-order output written from shared memory by consecutive threads (4 entries per
 //      thread, vector loads and stores, when W and R are multiples of 4);
-//   4. pair triangles: A and QK are zero-filled by 16-byte streaming stores of every thread, paced
+//   4. pair triangles: A and QK are zero-filled by 16-byte L1-bypassing stores of every thread, paced
 //      by the SM clock over phases 0-3 (a steady stream under the compute); then one warp per
 //      (row, triangle) walks: 32 earlier positions per step, lanes of one cell summed by a fixed
 //      shuffle tree, one lane adds the cell's partial to the warp's row buffer; only rows with
@@ -240,13 +240,38 @@ __device__ __noinline__ void zero_triangles(float* A, float* QK, int64_t c, int6
     }
 }
 
+// Global stores of Phase 1 bypass L1 (L1::no_allocate): the stores of a chunk (its outputs, 512 KB of
+// zeros, its DW records) would otherwise evict the lines its spills and loads use. Measured on the
+// large workload: with the streaming hint instead 2 us slower per Phase 1; plain write-back stores of
+// the zeros 70 us slower.
+__device__ __forceinline__ void st_na(float* p, float v) { asm volatile("st.global.L1::no_allocate.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory"); }
+__device__ __forceinline__ void st_na(int32_t* p, int32_t v) { asm volatile("st.global.L1::no_allocate.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory"); }
+__device__ __forceinline__ void st_na(int8_t* p, int8_t v) { asm volatile("st.global.L1::no_allocate.s8 [%0], %1;" ::"l"(p), "r"(static_cast<int>(v)) : "memory"); }
+__device__ __forceinline__ void st_na(__nv_bfloat16* p, __nv_bfloat16 v) {
+    asm volatile("st.global.L1::no_allocate.b16 [%0], %1;" ::"l"(p), "h"(__bfloat16_as_ushort(v)) : "memory");
+}
+__device__ __forceinline__ void st_na(int4* p, int4 v) {
+    asm volatile("st.global.L1::no_allocate.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_na(float4* p, float4 v) {
+    asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_na(uint4* p, uint4 v) {
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_na(uint2* p, uint2 v) {
+    asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_na(uint32_t* p, uint32_t v) {
+    asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 template <typename T>
 __device__ __forceinline__ void st_stream(T* p, T v) {
-    __stcs(p, v);
+    st_na(p, v);
 }
 
 // Four consecutive values of the value type: loaded from shared memory as one vector (8 bytes for
-// bfloat16, 16 for float32), stored to global memory as one streaming vector store.
+// bfloat16, 16 for float32), stored to global memory as one vector store (L1 bypassed).
 __device__ __forceinline__ void ld4(const float* p, float (&v)[4]) {
     const float4 x = *reinterpret_cast<const float4*>(p);
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
@@ -257,18 +282,18 @@ __device__ __forceinline__ void ld4(const __nv_bfloat16* p, float (&v)[4]) {
     v[2] = __uint_as_float(x.y << 16); v[3] = __uint_as_float(x.y & 0xFFFF0000u);
 }
 __device__ __forceinline__ void st4(float* p, const float (&v)[4]) {
-    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    st_na(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
 }
 __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&v)[4]) {
     const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[0]))) |
                         static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[1]))) << 16;
     const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2]))) |
                         static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[3]))) << 16;
-    __stcs(reinterpret_cast<uint2*>(p), make_uint2(lo, hi));
+    st_na(reinterpret_cast<uint2*>(p), make_uint2(lo, hi));
 }
-// Four int8 flags packed into one 4-byte streaming store.
+// Four int8 flags packed into one 4-byte store.
 __device__ __forceinline__ void st4_flags(int8_t* p, uint32_t f0, uint32_t f1, uint32_t f2, uint32_t f3) {
-    __stcs(reinterpret_cast<uint32_t*>(p), f0 | f1 << 8 | f2 << 16 | f3 << 24);
+    st_na(reinterpret_cast<uint32_t*>(p), f0 | f1 << 8 | f2 << 16 | f3 << 24);
 }
 
 // ORD: the saving forward's Phase 1 -- each group's FIRST record also carries its dense ordinal
@@ -405,7 +430,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         for (int b = tid; b < (1 << a.bucket_bits); b += nthr) bc[b] = 0u;
     }
     __syncthreads();
-    // A and QK of the chunk start as zeros written by every thread with 16-byte streaming stores,
+    // A and QK of the chunk start as zeros written by every thread with 16-byte stores (L1 bypassed),
     // paced by the SM clock: a warp stores one unit per thread each kZeroPeriod cycles (the warps
     // a 1/32 period apart), checked once per item in the per-item loops below. The stores so form
     // a steady stream under the block's compute; issued in bursts at the phase boundaries they
@@ -422,7 +447,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
     uint32_t zdl = static_cast<uint32_t>(clock()) + static_cast<uint32_t>(warp) * (kZeroPeriod / 32u);
     auto zero_store = [&]() {
         float* const p = zero_next < zka ? za + zero_next * zstride : zq + (zero_next - zka) * zstride;
-        __stcs(reinterpret_cast<float4*>(p), make_float4(0.f, 0.f, 0.f, 0.f));
+        st_na(reinterpret_cast<float4*>(p), make_float4(0.f, 0.f, 0.f, 0.f));
         ++zero_next;
     };
     auto zpace = [&]() {   // one unit when this warp's next time has come
@@ -1049,7 +1074,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 auto only = [&](int q) -> uint32_t { return ((p4[q] >> kPosSizeShift) & kPosCountMax) == 1u; };
                 if (a.out.is_last) st4_flags(a.out.is_last + kbase + o, last(0), last(1), last(2), last(3));
                 if (a.out.is_only) st4_flags(a.out.is_only + kbase + o, only(0), only(1), only(2), only(3));
-                if (a.out.pos_k) __stcs(reinterpret_cast<uint4*>(a.out.pos_k + kbase + o), pk);
+                if (a.out.pos_k) st_na(reinterpret_cast<uint4*>(a.out.pos_k + kbase + o), pk);
             }
             for (int o = 4 * tid; o < nq; o += 4 * nthr) {
                 const int t = static_cast<int>(__umulhi(static_cast<uint32_t>(o), a.r_magic)), e = t * wr + W + (o - t * R);
@@ -1071,7 +1096,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
                 auto only = [&](int q) -> uint32_t { return ((p4[q] >> kPosSizeShift) & kPosCountMax) == 1u; };
                 if (a.out.q_last) st4_flags(a.out.q_last + qbase + o, last(0), last(1), last(2), last(3));
                 if (a.out.q_only) st4_flags(a.out.q_only + qbase + o, only(0), only(1), only(2), only(3));
-                if (a.out.pos_q) __stcs(reinterpret_cast<uint4*>(a.out.pos_q + qbase + o), pk);
+                if (a.out.pos_q) st_na(reinterpret_cast<uint4*>(a.out.pos_q + qbase + o), pk);
             }
         } else {
             for (int o = tid; o < nk; o += nthr) {
@@ -1349,9 +1374,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) p1_kernel(const P1Args a) {
         float* const row = outp + (c * C + i) * static_cast<int64_t>(C);
         if (vec4) {
             for (int j = lane * 4; j < C; j += 128)
-                __stcs(reinterpret_cast<float4*>(row + j), *reinterpret_cast<const float4*>(rowbuf + j));
+                st_na(reinterpret_cast<float4*>(row + j), *reinterpret_cast<const float4*>(rowbuf + j));
         } else {
-            for (int j = lane; j < C; j += 32) __stcs(row + j, rowbuf[j]);
+            for (int j = lane; j < C; j += 32) st_na(row + j, rowbuf[j]);
         }
         __syncwarp();
     }

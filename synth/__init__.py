@@ -1,5 +1,5 @@
 """Seeded synthetic inputs for the sparse-delta-memory forward (Phase 1 + decay-and-write) and
-the backward's Phase A, GWR and GDS.
+the backward's Phase A, GWR and GDS, and the forward's read-side gather.
 
 This package is shared by the tests, the benchmark and the oracle's callers. It only draws
 random numbers and lays them out; it holds none of the method's arithmetic.
@@ -16,6 +16,7 @@ from .workloads import (  # noqa: F401
     make_snapshot_chunk,
     make_inputs,
     make_read_grads,
+    make_read_weights,
     make_write_weights,
     scaled,
 )

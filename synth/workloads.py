@@ -226,6 +226,19 @@ def make_read_grads(w: Workload, streams=None) -> np.ndarray:
     return gr.reshape(st * Ps, C, hd)
 
 
+def make_read_weights(w: Workload, streams=None) -> np.ndarray:
+    """q_w [N, C, R]: the weights of the forward's read-side gather, normal with the workload's value
+    scale, in the value dtype (uint16 bits for bf16), chunk-major like make_inputs."""
+    streams = list(range(w.P)) if streams is None else list(streams)
+    Ps, st, C, R = len(streams), w.steps, w.C, w.R
+    out = np.empty((st, Ps, C, R), np.float32)
+    for i, p in enumerate(streams):
+        rng = np.random.default_rng(np.random.SeedSequence([w.seed, p, 29]))
+        out[:, i] = (rng.standard_normal((st, C, R), dtype=np.float32) * np.float32(w.val_scale)).astype(np.float32)
+    out = out.reshape(st * Ps, C, R)
+    return f32_to_bf16_bits(out) if w.val_dtype == "bf16" else out
+
+
 def make_write_weights(w: Workload, streams=None) -> np.ndarray:
     """write_w [N, C, W] float32: the weights of the backward's token gather (GWR), normal with the
     workload's value scale, chunk-major like make_inputs."""

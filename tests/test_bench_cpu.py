@@ -46,9 +46,9 @@ def test_reference_arm_every_mode(capsys):
     import json
 
     for mode, metric in (("", bench.METRIC_FWD), ("pa", bench.METRIC_PA), ("gds", bench.METRIC_GDS),
-                         ("gwr", bench.METRIC_GWR)):
+                         ("gwr", bench.METRIC_GWR), ("read", bench.METRIC_READ)):
         args = argparse.Namespace(workload="tiny", steps=1, warmup=0, cpu_seconds=0.2, pa=mode == "pa",
-                                  gds=mode == "gds", gwr=mode == "gwr", pa_grad="f32")
+                                  gds=mode == "gds", gwr=mode == "gwr", read=mode == "read", pa_grad="f32")
         bench.run_reference(args)
         d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
         assert d["impl"] == "reference" and d["metric"] == metric and d["value"] > 0
