@@ -54,48 +54,53 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 template <typename DvT>
 __global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
     // Launched as a programmatic dependent of the kernel before it (Phase 1): nothing is read or
-    // written before that grid completes and its memory is visible.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // written before that grid completes and its memory is visible. It does not trigger its own
+    // dependent (the DW) early: DW blocks resident during Phase 1's last wave made the forward slower
+    // (large workload 711 -> 753 us, wide_ragged 181 -> 198 us); the DW launches at this grid's end.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.claim = 0u;   // the DW's work counter (the DW waits for this grid)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t c = a.c0 + blockIdx.x;   // one block per chunk
-    const int nl = a.lcnt[c];
     const DvT* const dv = static_cast<const DvT*>(a.dv);
     const uint32_t hdu = static_cast<uint32_t>(a.hd);
-    for (int item = warp; item < nl * a.nsl; item += kDwWarps) {
-        const int li = item / a.nsl, sl = item - li * a.nsl;
-        const int col = sl * 128 + lane * 4;
-        const bool active = col < a.hd;
-        const int4* const rec = a.krec + c * a.rstride;
-        const DvT* const dv_lane = dv + static_cast<int64_t>(c) * a.C * a.hd + col;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        // records from the group's first tail record to its LAST (never past the chunk's records)
-        for (int base = a.ldesc[c * a.maxL + li]; base < a.rstride; base += 16) {
-            int4 r = make_int4(0, 0, 0, 0);
-            const bool in = lane < 16 && base + lane < a.rstride;
-            if (in) r = __ldcg(rec + base + lane);
-            const uint32_t lastm = __ballot_sync(kFull, in && (static_cast<uint32_t>(r.x) & kLast));
-            const int n = lastm ? __ffs(lastm) : 16;   // the group's records in this batch
-            rows::Raw4<DvT> dvv[16];
+    // a block per chunk, a grid of at most two blocks per SM looping over the chunks (on uniform
+    // slots nothing is to be done: the kernel is only its launch)
+    for (int64_t cb = blockIdx.x; cb < a.nchunks; cb += gridDim.x) {
+        const int64_t c = a.c0 + cb;
+        const int nl = a.lcnt[c];
+        for (int item = warp; item < nl * a.nsl; item += kDwWarps) {
+            const int li = item / a.nsl, sl = item - li * a.nsl;
+            const int col = sl * 128 + lane * 4;
+            const bool active = col < a.hd;
+            const int4* const rec = a.krec + c * a.rstride;
+            const DvT* const dv_lane = dv + static_cast<int64_t>(c) * a.C * a.hd + col;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // records from the group's first tail record to its LAST (never past the chunk's records)
+            for (int base = a.ldesc[c * a.maxL + li]; base < a.rstride; base += 16) {
+                int4 r = make_int4(0, 0, 0, 0);
+                const bool in = lane < 16 && base + lane < a.rstride;
+                if (in) r = __ldcg(rec + base + lane);
+                const uint32_t lastm = __ballot_sync(kFull, in && (static_cast<uint32_t>(r.x) & kLast));
+                const int n = lastm ? __ffs(lastm) : 16;   // the group's records in this batch
+                rows::Raw4<DvT> dvv[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const uint32_t w0 = __shfl_sync(kFull, static_cast<uint32_t>(r.x), k);
-                if (k < n && active && base + k < a.rstride) dvv[k].ld(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float sc = __int_as_float(__shfl_sync(kFull, r.z, k));
-                if (k < n && base + k < a.rstride) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t w0 = __shfl_sync(kFull, static_cast<uint32_t>(r.x), k);
+                    if (k < n && active && base + k < a.rstride) dvv[k].ld(dv_lane + static_cast<uint64_t>(w0 & kRecTokMask) * hdu);
                 }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float sc = __int_as_float(__shfl_sync(kFull, r.z, k));
+                    if (k < n && base + k < a.rstride) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, dvv[k][i], acc[i]);
+                    }
+                }
+                if (lastm != 0u) break;
             }
-            if (lastm != 0u) break;
+            if (active)
+                __stcg(reinterpret_cast<float4*>(a.lacc + (static_cast<int64_t>(c) * a.maxL + li) * a.hd + col),
+                       make_float4(acc[0], acc[1], acc[2], acc[3]));
         }
-        if (active)
-            __stcg(reinterpret_cast<float4*>(a.lacc + (static_cast<int64_t>(c) * a.maxL + li) * a.hd + col),
-                   make_float4(acc[0], acc[1], acc[2], acc[3]));
     }
 }
 
@@ -325,7 +330,11 @@ cudaError_t launch_t(const DWArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream) {
     if (a.nchunks <= 0) return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(a.nchunks));
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(a.nchunks < 2 * static_cast<int64_t>(sms) ? a.nchunks : 2 * static_cast<int64_t>(sms)));
     return dv_bf16 ? launch_dependent(long_kernel<__nv_bfloat16>, grid, dim3(kDwThreads), stream, a)
                    : launch_dependent(long_kernel<float>, grid, dim3(kDwThreads), stream, a);
 }
