@@ -286,24 +286,6 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
     }
 }
 
-// A launch as a programmatic dependent of the previous kernel in the stream: its CTAs may be
-// scheduled before that kernel completes (onto SMs it leaves idle) and wait in the kernel
-// (griddepcontrol.wait) until it has completed and its memory is visible.
-template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream, Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 template <typename BankT, typename DvT, bool SNAP>
 cudaError_t launch_t1(const DWArgs& a, cudaStream_t stream) {
     int dev = 0, sms = 0, per_sm = 0;

@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/sdm.h"
 
 namespace sdm {
@@ -159,6 +161,24 @@ struct DWArgs {
     int64_t step_begin, step_end;
     int64_t items;      // P * B * nsl
 };
+
+// A launch as a programmatic dependent of the previous kernel in the stream: its CTAs may be
+// scheduled before that kernel completes (onto SMs it leaves idle) and wait in the kernel
+// (griddepcontrol.wait) until it has completed and its memory is visible.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_phase1(const P1Args& a, int val_bf16, int ordinals, int64_t nchunks, int threads, size_t smem,

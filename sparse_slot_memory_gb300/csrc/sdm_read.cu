@@ -10,7 +10,8 @@
 //             over the read lanes r = 0 .. R-1 in order (a lane whose id is outside [0, S) adds nothing).
 //
 // GB300 design: a grid of resident warps (as many as the SMs hold), each looping over (token, 128-column
-// slice) units. A unit's 16 read rows are all in flight at once (each lane its 4 columns, kept in the
+// slice) units, launched as a programmatic dependent of the previous kernel (its launch latency is
+// hidden). A unit's 16 read rows are all in flight at once (each lane its 4 columns, kept in the
 // storage type), then summed in lane order; the next unit's ids and weights load while the current
 // unit's rows are in flight. HBM-bound: per token R ids and weights, one bank row per valid read lane,
 // one f32 output row.
@@ -44,6 +45,9 @@ struct ReadArgs {
 
 template <typename BankT, typename WT>
 __global__ void __launch_bounds__(kReadThreads) read_kernel(const ReadArgs a, int64_t total_warps) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's read or DW, or
+    // any kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     int64_t u = static_cast<int64_t>(blockIdx.x) * kReadWarps + (threadIdx.x >> 5);
     if (u >= a.units) return;   // warp-uniform
@@ -129,8 +133,8 @@ cudaError_t launch_r(const ReadArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t want = (a.units + kReadWarps - 1) / kReadWarps;
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * std::max(per_sm, 1)));
-    read_kernel<BankT, WT><<<static_cast<unsigned>(blocks), kReadThreads, 0, stream>>>(a, blocks * kReadWarps);
-    return cudaGetLastError();
+    return launch_dependent(read_kernel<BankT, WT>, dim3(static_cast<unsigned>(blocks)), dim3(kReadThreads), stream, a,
+                            static_cast<int64_t>(blocks * kReadWarps));
 }
 
 }  // namespace
