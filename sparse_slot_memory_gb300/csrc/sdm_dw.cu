@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
                                     float o[4];
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) o[i] = fmaf(bv[k][i], cp, acc[i]);
-                                    rows::st4(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
+                                    rows::st4cs(bank_lane + static_cast<uint64_t>(static_cast<uint32_t>(r.y)) * hdu, o);
                                 }
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) acc[i] = 0.f;
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kDwThreads, 4) dw_kernel(const DWArgs a) {
                         const float cp = __int_as_float(r.w);
                         const float o[4] = {fmaf(bv[0], cp, la.x), fmaf(bv[1], cp, la.y), fmaf(bv[2], cp, la.z),
                                             fmaf(bv[3], cp, la.w)};
-                        rows::st4(row, o);
+                        rows::st4cs(row, o);
                     }
                 };
                 const uint32_t longm = __ballot_sync(kFull, lane < n && (static_cast<uint32_t>(rs[lane].x) & kRecLong));

@@ -121,6 +121,19 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, const float (&o)[4]) {
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+// store with the streaming hint (evict-first in L2): f32 as is, bf16 rounded to nearest even
+__device__ __forceinline__ void st4cs(float* p, const float (&o)[4]) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(o[0], o[1], o[2], o[3]));
+}
+__device__ __forceinline__ void st4cs(__nv_bfloat16* p, const float (&o)[4]) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(p), u);
+}
+
 // store 8 columns: f32 as is, bf16 rounded to nearest even
 __device__ __forceinline__ void st8(float* p, const float (&o)[8]) {
     reinterpret_cast<float4*>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
