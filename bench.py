@@ -220,6 +220,8 @@ def run_ours(args):
         w = scaled(w, P=args.streams)
     if args.slots:
         w = scaled(w, S=args.slots)
+    if getattr(args, "idx", None):
+        w = scaled(w, idx=args.idx)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -483,6 +485,8 @@ def run_pa(args):
         w = scaled(w, P=args.streams)
     if args.slots:
         w = scaled(w, S=args.slots)
+    if getattr(args, "idx", None):
+        w = scaled(w, idx=args.idx)
     x = make_inputs(w)
     b = make_backward_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
@@ -691,6 +695,8 @@ def run_gds(args):
         w = scaled(w, P=args.streams)
     if args.slots:
         w = scaled(w, S=args.slots)
+    if getattr(args, "idx", None):
+        w = scaled(w, idx=args.idx)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -875,6 +881,8 @@ def run_gwr(args):
         w = scaled(w, P=args.streams)
     if args.slots:
         w = scaled(w, S=args.slots)
+    if getattr(args, "idx", None):
+        w = scaled(w, idx=args.idx)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -1055,6 +1063,8 @@ def run_read(args):
         w = scaled(w, P=args.streams)
     if args.slots:
         w = scaled(w, S=args.slots)
+    if getattr(args, "idx", None):
+        w = scaled(w, idx=args.idx)
     x = make_inputs(w)
     shape = sdm.ShapeSpec.from_workload(w)
 
@@ -1288,7 +1298,8 @@ class CpuPool:
 def cpu_baselines(kind: str, args, w, single: dict) -> dict:
     """The two CPU rows of a GPU arm's line: the oracle on all host cores (the row's value) and on one
     core (``single_core``)."""
-    over = tuple(sorted({k: v for k, v in (("P", args.streams), ("S", args.slots)) if v}.items()))
+    over = tuple(sorted({k: v for k, v in (("P", args.streams), ("S", args.slots), ("idx", getattr(args, "idx", None)))
+                         if v}.items()))
     pool = CpuPool(kind, args.workload, over, w.P)
     try:
         allc = pool.sample(args.cpu_seconds)
@@ -1353,6 +1364,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--streams", type=int, default=0, help="override the workload's stream count (profiling runs)")
     ap.add_argument("--slots", type=int, default=0, help="override the workload's slots per stream (profiling runs)")
+    ap.add_argument("--idx", choices=["uniform", "zipf"], default=None,
+                    help="override the workload's slot-id distribution (the same shape with other ids)")
     ap.add_argument("--saving", action="store_true", help="time the saving forward (DW writes the dense snapshot)")
     ap.add_argument("--pa", action="store_true", help="time the backward's Phase A over every step instead")
     ap.add_argument("--gds", action="store_true", help="time the backward's GDS (read side) over every step instead")
