@@ -50,6 +50,10 @@ NCU_TRAFFIC = {
     "large:phase1:6922acd872e5": 55624960 + 718927616,
     "large:dw:1a9bec971807": 1155819008 + 961666560,
     "large:phase1:f995602e26cb": 52393472 + 726859776,
+    "large:dw:3470f76f6aa3": 2141972736,
+    "large:phase1:1f1e23527340": 775642112,
+    # the read gather (bench.py --read): one launch (one step) of the timed pass
+    "large:read:1043e442d83a": 34294784,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
     "large:pa:4c47240459f4": round((106345728 + 43396352) * 4186081 / 4161534),
