@@ -36,7 +36,7 @@ def test_traffic_keys_name_known_kernels():
     for key in bench.NCU_TRAFFIC:
         workload, dom, h = key.split(":")
         assert workload in WORKLOADS and len(h) == 12
-        assert dom.split("_")[0] in ("dw", "phase1", "pa", "gds", "gwr")
+        assert dom.split("_")[0] in ("dw", "phase1", "pa", "gds", "gwr", "read")
 
 
 def test_reference_arm_every_mode(capsys):
