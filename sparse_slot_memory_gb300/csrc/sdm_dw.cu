@@ -300,7 +300,7 @@ cudaError_t launch_t1(const DWArgs& a, cudaStream_t stream) {
     const int64_t need_blocks = (a.items + kDwWarps - 1) / kDwWarps;
     if (blocks > need_blocks) blocks = need_blocks;
     if (blocks < 1) blocks = 1;
-    return launch_dependent(dw_kernel<BankT, DvT, SNAP>, dim3(static_cast<unsigned>(blocks)), dim3(kDwThreads), stream, a);
+    return launch_dependent(dw_kernel<BankT, DvT, SNAP>, dim3(static_cast<unsigned>(blocks)), dim3(kDwThreads), 0, stream, a);
 }
 
 template <typename BankT, typename DvT>
@@ -317,8 +317,8 @@ cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.nchunks < 2 * static_cast<int64_t>(sms) ? a.nchunks : 2 * static_cast<int64_t>(sms)));
-    return dv_bf16 ? launch_dependent(long_kernel<__nv_bfloat16>, grid, dim3(kDwThreads), stream, a)
-                   : launch_dependent(long_kernel<float>, grid, dim3(kDwThreads), stream, a);
+    return dv_bf16 ? launch_dependent(long_kernel<__nv_bfloat16>, grid, dim3(kDwThreads), 0, stream, a)
+                   : launch_dependent(long_kernel<float>, grid, dim3(kDwThreads), 0, stream, a);
 }
 
 cudaError_t launch_dw(const DWArgs& a, int dv_bf16, int bank_bf16, cudaStream_t stream) {

@@ -60,6 +60,9 @@ __device__ __forceinline__ bool valid_first(uint32_t v) { return (v & kFirst) !=
 // ---- (1) dots, one warp per token -----------------------------------------------------------------
 template <typename BankT>
 __global__ void __launch_bounds__(kGdsThreads) gds_dots_kernel(const GDSArgs a) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cl = static_cast<int>(blockIdx.x / a.dgroups);
     const int dg = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.dgroups);
@@ -121,6 +124,9 @@ __global__ void __launch_bounds__(kGdsThreads) gds_dots_kernel(const GDSArgs a) 
 // next token's ids and reading gradient load while the current token's bank rows are in flight.
 template <typename BankT>
 __global__ void __launch_bounds__(kGdsThreads) gds_dots_loop_kernel(const GDSArgs a, int total_warps) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int ntok = a.P * a.C;
     int it = blockIdx.x * kGdsWarps + (threadIdx.x >> 5);
@@ -296,6 +302,9 @@ struct GdsRing {
 
 template <typename GradT, typename ValT>
 __global__ void __launch_bounds__(kGdsThreads, 2) gds_scatter_kernel(const GDSArgs a) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(16) unsigned char gds_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     GdsRing<GradT>& ring = reinterpret_cast<GdsRing<GradT>*>(gds_smem)[warp];
@@ -399,8 +408,8 @@ cudaError_t launch_scatter(const GDSArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(gds_scatter_kernel<GradT, ValT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    gds_scatter_kernel<GradT, ValT><<<static_cast<unsigned>(a.P) * a.tiles, kGdsThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(gds_scatter_kernel<GradT, ValT>, dim3(static_cast<unsigned>(a.P) * a.tiles), dim3(kGdsThreads),
+                            smem, stream, a);
 }
 
 template <typename BankT>
@@ -414,11 +423,11 @@ cudaError_t launch_dots(const GDSArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         const int ntok = a.P * a.C;
         const int blocks = std::max(1, std::min((ntok + kGdsWarps - 1) / kGdsWarps, sms * std::max(per_sm, 1)));
-        gds_dots_loop_kernel<BankT><<<blocks, kGdsThreads, 0, stream>>>(a, blocks * kGdsWarps);
-    } else {
-        gds_dots_kernel<BankT><<<static_cast<unsigned>(a.P) * a.dgroups, kGdsThreads, 0, stream>>>(a);
+        return launch_dependent(gds_dots_loop_kernel<BankT>, dim3(blocks), dim3(kGdsThreads), 0, stream, a,
+                                blocks * kGdsWarps);
     }
-    return cudaGetLastError();
+    return launch_dependent(gds_dots_kernel<BankT>, dim3(static_cast<unsigned>(a.P) * a.dgroups), dim3(kGdsThreads), 0,
+                            stream, a);
 }
 
 cudaError_t launch_gds(const GDSArgs& a, int grad_bf16, int bank_bf16, int val_bf16, cudaStream_t stream) {

@@ -46,6 +46,9 @@ struct GWRArgs {
 
 template <typename GradT, typename DvT>
 __global__ void __launch_bounds__(kGwrThreads) gwr_kernel(const GWRArgs a) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cl = static_cast<int>(blockIdx.x / a.groups);
     const int tg = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.groups);
@@ -118,6 +121,9 @@ __global__ void __launch_bounds__(kGwrThreads) gwr_kernel(const GWRArgs a) {
 // token's ids, weights and dv row load while the current token's grad rows are in flight.
 template <typename GradT, typename DvT>
 __global__ void __launch_bounds__(kGwrThreads) gwr_loop_kernel(const GWRArgs a, int total_warps) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int ntok = a.P * a.C;
     int it = blockIdx.x * kGwrWarps + (threadIdx.x >> 5);
@@ -203,11 +209,11 @@ cudaError_t launch_gd(const GWRArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         const int ntok = a.P * a.C;
         const int blocks = std::max(1, std::min((ntok + kGwrWarps - 1) / kGwrWarps, sms * std::max(per_sm, 1)));
-        gwr_loop_kernel<GradT, DvT><<<blocks, kGwrThreads, 0, stream>>>(a, blocks * kGwrWarps);
-    } else {
-        gwr_kernel<GradT, DvT><<<static_cast<unsigned>(a.P) * a.groups, kGwrThreads, 0, stream>>>(a);
+        return launch_dependent(gwr_loop_kernel<GradT, DvT>, dim3(blocks), dim3(kGwrThreads), 0, stream, a,
+                                blocks * kGwrWarps);
     }
-    return cudaGetLastError();
+    return launch_dependent(gwr_kernel<GradT, DvT>, dim3(static_cast<unsigned>(a.P) * a.groups), dim3(kGwrThreads), 0,
+                            stream, a);
 }
 
 template <typename GradT>

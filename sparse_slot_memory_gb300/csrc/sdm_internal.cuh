@@ -164,13 +164,15 @@ struct DWArgs {
 
 // A launch as a programmatic dependent of the previous kernel in the stream: its CTAs may be
 // scheduled before that kernel completes (onto SMs it leaves idle) and wait in the kernel
-// (griddepcontrol.wait) until it has completed and its memory is visible.
+// (griddepcontrol.wait) until it has completed and its memory is visible. Every kernel launched so
+// waits before its first memory access, so stream order holds whatever kernel came before.
 template <typename... Params, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream, Args&&... args) {
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

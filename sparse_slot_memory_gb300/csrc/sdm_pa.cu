@@ -118,41 +118,109 @@ __device__ __forceinline__ Member member_window(const PAArgs& a, const int32_t* 
     return m;
 }
 
-// acc += the window's terms on this lane's 4 columns; returns this lane's member's <dva, snap> sum
-// over the slice (lanes >= m.n get 0). Members go in blocks of 16: the block's 16 token rows are
-// cp.async-copied into the warp's shared-memory ring at once (one round trip per block; each lane
-// copies and reads back its own 4 columns, zeros past the row), then their dot partials are reduced
-// across the lanes together (rows::tsum16, the tree of rows::allsum): member k's sum lands in lane k.
-__device__ __forceinline__ float window_terms(const Member& m, const float* dva_col, bool dva_on, int hd,
-                                              const float (&sn)[4], float (&acc)[4], int lane, float4* buf) {
-    float mine = 0.f;
-    const uint32_t okm = __ballot_sync(kFull, m.ok);   // members that name an entry of the chunk
-    for (int k0 = 0; k0 < m.n; k0 += 16) {   // k0 = 0 or 16
+// The hot-group walk's token rows stream through the warp's buffer in sub-blocks of kWalkSub members:
+// sub-block g of a slice's walk (window g / 4, its members kWalkSub * (g % 4) .. + kWalkSub - 1) is
+// cp.async-copied into slots kWalkSub * (g % kWalkDepth) .. + kWalkSub - 1 of the buffer (each lane
+// copies and reads back its own 4 columns, zeros past the row), and kWalkDepth sub-blocks are in flight
+// at once, across window boundaries (the next window's scalars are loaded one window ahead).
+constexpr int kWalkSub = 8;
+constexpr int kWalkDepth = 3;
+constexpr int kWalkRows = kWalkSub * kWalkDepth;   // row slots per lane
+
+// sub-block g's copies: members of a window with n members, tokens tok (lane k holds member k), okm
+// the members that name an entry of the chunk
+__device__ __forceinline__ void walk_issue(int g, int n, int tok, uint32_t okm, const float* dva_col, bool dva_on,
+                                           int hd, int lane, float4* buf) {
+    const int slot = g % kWalkDepth;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int k = k0 + u;
-            const int tk = __shfl_sync(kFull, m.tok, k & 31);
-            if (k < m.n && ((okm >> (k & 31)) & 1u))   // warp-uniform
-                cp4z(reinterpret_cast<float*>(&buf[u * 32 + lane]), dva_col + static_cast<int64_t>(tk) * hd, dva_on);
-        }
-        cp_commit();
+    for (int u = 0; u < kWalkSub; ++u) {
+        const int k = kWalkSub * (g & 3) + u;
+        const int tk = __shfl_sync(kFull, tok, k);
+        if (k < n && ((okm >> k) & 1u))   // warp-uniform
+            cp4z(reinterpret_cast<float*>(&buf[(slot * kWalkSub + u) * 32 + lane]), dva_col + static_cast<int64_t>(tk) * hd,
+                 dva_on);
+    }
+    cp_commit();
+}
+
+// wait until at most `pend` copy groups issued after the one needed are still in flight
+__device__ __forceinline__ void walk_wait(int pend) {
+    if (pend >= 2)
+        cp_wait<2>();
+    else if (pend == 1)
+        cp_wait<1>();
+    else
         cp_wait<0>();
-        float v[16];
+}
+
+// sub-block g of window m: acc += its terms (member order); v[OFF + u] = member u's dot partial
+template <int OFF>
+__device__ __forceinline__ void walk_sub(const Member& m, uint32_t okm, int g, const float (&sn)[4], float (&acc)[4],
+                                         float (&v)[16], int lane, const float4* buf) {
+    const int slot = g % kWalkDepth;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int k = k0 + u;
-            const float scu = __shfl_sync(kFull, m.sc, k & 31);
-            v[u] = 0.f;
-            if (k < m.n && ((okm >> (k & 31)) & 1u)) {   // warp-uniform
-                float d[4];
-                get4(reinterpret_cast<const float*>(&buf[u * 32 + lane]), d);
+    for (int u = 0; u < kWalkSub; ++u) {
+        const int k = kWalkSub * (g & 3) + u;
+        const float scu = __shfl_sync(kFull, m.sc, k);
+        v[OFF + u] = 0.f;
+        if (k < m.n && ((okm >> k) & 1u)) {   // warp-uniform
+            float d[4];
+            get4(reinterpret_cast<const float*>(&buf[(slot * kWalkSub + u) * 32 + lane]), d);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[i], acc[i]);
-                v[u] = dot4(d, sn);
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(scu, d[i], acc[i]);
+            v[OFF + u] = dot4(d, sn);
+        }
+    }
+}
+
+// Window w of the walk (members m; nm the next window's when `more`): acc += the window's terms on
+// this lane's 4 columns in member order; returns this lane's member's <dva, snap> sum over the slice
+// (lanes >= m.n get 0). The dot partials of 16 members are reduced across the lanes together
+// (rows::tsum16, the tree of rows::allsum): member k's sum lands in lane k. `issued` counts the
+// slice's sub-blocks issued so far (0 at the slice's first window).
+__device__ __forceinline__ float window_terms(const Member& m, const Member& nm, bool more, int w, int& issued,
+                                              const float* dva_col, bool dva_on, int hd, const float (&sn)[4],
+                                              float (&acc)[4], int lane, float4* buf) {
+    static_assert(kWalkSub == 8 && kWalkDepth <= 5, "4 sub-blocks per window; at most one window ahead");
+    float mine = 0.f;
+    const uint32_t okm = __ballot_sync(kFull, m.ok);
+    const int nsb = (m.n + kWalkSub - 1) / kWalkSub;                  // this window's sub-blocks (1..4)
+    const int nsn = more ? (nm.n + kWalkSub - 1) / kWalkSub : 0;      // the next window's
+    uint32_t okn = 0u;
+    bool have_okn = false;
+    auto top_up = [&](int g) {   // sub-blocks up to g + kWalkDepth - 1 in flight
+        while (issued < g + kWalkDepth) {
+            const int wi = issued >> 2, ji = issued & 3;
+            if (wi == w) {
+                if (ji >= nsb) break;
+                walk_issue(issued, m.n, m.tok, okm, dva_col, dva_on, hd, lane, buf);
+            } else {
+                if (ji >= nsn) break;   // wi == w + 1
+                if (!have_okn) {
+                    okn = __ballot_sync(kFull, nm.ok);
+                    have_okn = true;
+                }
+                walk_issue(issued, nm.n, nm.tok, okn, dva_col, dva_on, hd, lane, buf);
             }
+            ++issued;
+        }
+    };
+    const int g0 = 4 * w;
+    for (int h = 0; 2 * h < nsb; ++h) {   // members 16h .. 16h + 15: sub-blocks 2h and 2h + 1
+        float v[16];
+        top_up(g0 + 2 * h);
+        walk_wait(issued - 1 - (g0 + 2 * h));
+        walk_sub<0>(m, okm, g0 + 2 * h, sn, acc, v, lane, buf);
+        if (2 * h + 1 < nsb) {
+            top_up(g0 + 2 * h + 1);
+            walk_wait(issued - 1 - (g0 + 2 * h + 1));
+            walk_sub<kWalkSub>(m, okm, g0 + 2 * h + 1, sn, acc, v, lane, buf);
+        } else {
+#pragma unroll
+            for (int u = 0; u < kWalkSub; ++u) v[kWalkSub + u] = 0.f;
         }
         const float red = tsum16(v, lane);
-        if ((lane >> 4) == (k0 >> 4)) mine = red;
+        if ((lane >> 4) == h) mine = red;
     }
     return mine;
 }
@@ -195,10 +263,11 @@ __device__ __noinline__ void open_group(const PAArgs& a, const int32_t* srow, in
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         float cpl = 1.f;
         Member m = member_window<ValT>(a, srow, f, c, lane);
-        for (int q = f;; q += 32) {
+        int issued = 0;   // the walk's sub-blocks issued (this slice)
+        for (int q = f, w = 0;; q += 32, ++w) {
             Member nm = m;
             if (!m.last) nm = member_window<ValT>(a, srow, q + 32, c, lane);   // the next window's scalars in flight
-            const float r = window_terms(m, dva_chunk + (on ? col : 0), on, hd, s4, acc, lane, buf);
+            const float r = window_terms(m, nm, !m.last, w, issued, dva_chunk + (on ? col : 0), on, hd, s4, acc, lane, buf);
             if (m.ok) {
                 if (a.nsl == 1) {   // one slice: the sums are final
                     a.d_k_eff[m.o] = -m.beta * (0.f + r);
@@ -240,16 +309,28 @@ struct PaRing {
     BankT snap[kPaRing][32][4];
 };
 
+// One warp's shared memory: the ring, or (a hot group's walk, once the ring is idle) kWalkRows token-row
+// slots per lane.
 template <typename GradT, typename BankT>
-constexpr size_t pa_smem_bytes() { return sizeof(PaRing<GradT, BankT>) * kPaWarps; }
+union PaWarpSmem {
+    PaRing<GradT, BankT> ring;
+    float4 walk[kWalkRows][32];
+};
+
+template <typename GradT, typename BankT>
+constexpr size_t pa_smem_bytes() { return sizeof(PaWarpSmem<GradT, BankT>) * kPaWarps; }
 
 template <typename GradT, typename BankT, typename ValT>
 __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
+    // launched as a programmatic dependent of the kernel before it (the previous step's kernel, or any
+    // kernel of the caller's): nothing is read or written before that grid completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ int before_s[kPaWarps];   // valid FIRSTs before the tile, per warp's share of the count
     __shared__ int in_s[kPaWarps];       // valid FIRSTs in each warp's 32 positions
     extern __shared__ __align__(16) unsigned char pa_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    PaRing<GradT, BankT>& ring = reinterpret_cast<PaRing<GradT, BankT>*>(pa_smem)[warp];
+    PaWarpSmem<GradT, BankT>& wsm = reinterpret_cast<PaWarpSmem<GradT, BankT>*>(pa_smem)[warp];
+    PaRing<GradT, BankT>& ring = wsm.ring;
     const int cl = static_cast<int>(blockIdx.x / a.tiles);   // stream of the chunk
     const int tile = static_cast<int>(blockIdx.x - static_cast<int64_t>(cl) * a.tiles);
     const int64_t c = a.c0 + cl;
@@ -428,11 +509,9 @@ __global__ void __launch_bounds__(kPaThreads, 2) pa_kernel(const PAArgs a) {
             a.grad_g[o] = mybad ? 0.f : cp * gs;
         }
     }
-    // the walk reuses the warp's ring (idle by now: every copy has landed) as 16 token-row slots
-    static_assert(sizeof(PaRing<GradT, BankT>) >= 16 * 32 * sizeof(float4), "the ring holds 16 rows per lane");
+    // the walk reuses the warp's ring (idle by now: every copy has landed) as kWalkRows token-row slots
     if (open)
-        open_group<GradT, BankT, ValT>(a, srow, c, cl, q0 + flast, ord0 + __popc(fmask) - 1, lane, &bad,
-                                       reinterpret_cast<float4*>(&ring));
+        open_group<GradT, BankT, ValT>(a, srow, c, cl, q0 + flast, ord0 + __popc(fmask) - 1, lane, &bad, &wsm.walk[0][0]);
     if (bad && lane == 0 && a.status != nullptr) atomicOr(a.status, kDevBadSlot);
 }
 
@@ -443,8 +522,7 @@ cudaError_t launch_t(const PAArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pa_kernel<GradT, BankT, ValT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    pa_kernel<GradT, BankT, ValT><<<blocks, kPaThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(pa_kernel<GradT, BankT, ValT>, dim3(blocks), dim3(kPaThreads), smem, stream, a);
 }
 
 template <typename GradT, typename BankT>

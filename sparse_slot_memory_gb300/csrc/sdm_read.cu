@@ -133,7 +133,7 @@ cudaError_t launch_r(const ReadArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t want = (a.units + kReadWarps - 1) / kReadWarps;
     const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * std::max(per_sm, 1)));
-    return launch_dependent(read_kernel<BankT, WT>, dim3(static_cast<unsigned>(blocks)), dim3(kReadThreads), stream, a,
+    return launch_dependent(read_kernel<BankT, WT>, dim3(static_cast<unsigned>(blocks)), dim3(kReadThreads), 0, stream, a,
                             static_cast<int64_t>(blocks * kReadWarps));
 }
 
