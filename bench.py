@@ -46,22 +46,19 @@ METRIC_READ = "SDM forward read-side gather tokens/sec and achieved HBM GB/s vs 
 # hash of the kernel's CUDA sources at capture time. A source change voids the figure: the bench
 # line then reports null traffic.
 NCU_TRAFFIC = {
-    "large:dw:c28e9f58496b": 1178147328 + 981000192,
-    "large:phase1:6922acd872e5": 55624960 + 718927616,
-    "large:dw:1a9bec971807": 1155819008 + 961666560,
-    "large:phase1:f995602e26cb": 52393472 + 726859776,
-    "large:dw:3470f76f6aa3": 2141972736,
-    "large:phase1:1f1e23527340": 775642112,
+    # the forward (bench.py): the timed loop's Phase 1 (all outputs) and DW, one launch each at full size
+    "large:dw:620f34b88826": 1162350592 + 979562496,
+    "large:phase1:c65c2d4457e8": 52400896 + 723014912,
     # the read gather (bench.py --read): one launch (one step) of the timed pass
-    "large:read:1043e442d83a": 34294784,
+    "large:read:3cabff777f24": 34291712 + 2048,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:4c47240459f4": round((106345728 + 43396352) * 4186081 / 4161534),
+    "large:pa:58247df1fae2": round((106349824 + 43308288) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
-    "large:gds:58ed4c9cbe68": round((38026496 + 256 + 72660992 + 19850240) * 4185964 / 4161643),
+    "large:gds:df64f6c34f54": round((38027008 + 512 + 72662272 + 19415808) * 4185964 / 4161643),
     # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
-    "large:gwr:e67855001ebf": 69737728 + 52992,
+    "large:gwr:25ea3b0dc7dd": 69719296 + 78336,
 }
 
 
