@@ -48,9 +48,14 @@ class ShapeSpec:
         return self.steps * self.P
 
     def c(self) -> _abi.Shape:
-        return _abi.Shape(self.P, self.C, self.W, self.R, self.hd, self.valid_last, self.steps, self.S,
-                          _DT[self.val_dtype], _DT[self.dv_dtype], _DT[self.bank_dtype], int(self.gate_per_entry),
-                          int(self.dw_log_buckets), int(self.p1_warps))
+        """The C struct of the shape (built once: the spec is immutable and the library only reads it)."""
+        cs = self.__dict__.get("_cstruct")
+        if cs is None:
+            cs = _abi.Shape(self.P, self.C, self.W, self.R, self.hd, self.valid_last, self.steps, self.S,
+                            _DT[self.val_dtype], _DT[self.dv_dtype], _DT[self.bank_dtype], int(self.gate_per_entry),
+                            int(self.dw_log_buckets), int(self.p1_warps))
+            object.__setattr__(self, "_cstruct", cs)
+        return cs
 
     @classmethod
     def from_workload(cls, w, P=None) -> "ShapeSpec":
@@ -60,13 +65,14 @@ class ShapeSpec:
 
 
 def _ptr(t):
+    """The device address of a contiguous CUDA tensor (an int: ctypes passes it as void*)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError("expected a CUDA tensor (the library runs on the GPU only)")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _need(t, dtype, numel: int, name: str):
@@ -110,9 +116,18 @@ def _need_rows(shape: "ShapeSpec", dv, bank, snap=None):
     _need(snap, _TORCH_DT[shape.bank_dtype], shape.N * shape.C * shape.W * shape.hd, "snap")
 
 
+# the current stream's handle without building a torch.cuda.Stream object per call (a per-step call
+# such as read() is otherwise dominated by it); the public route where torch lacks these
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        if _raw_stream is not None and _cur_device is not None:
+            return _raw_stream(_cur_device())
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _check(st: int, what: str):
@@ -171,7 +186,7 @@ def _p1out(out):
     if out:
         for f in _abi.P1_FIELDS:
             if f in out and out[f] is not None:
-                setattr(o, f, _ptr(out[f]).value)
+                setattr(o, f, _ptr(out[f]))
     return o
 
 
