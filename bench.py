@@ -53,10 +53,10 @@ NCU_TRAFFIC = {
     "large:read:3cabff777f24": 34291712 + 2048,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:58247df1fae2": round((106349824 + 43308288) * 4186081 / 4161534),
+    "large:pa:c24c52eb0c83": round((106358528 + 43712768) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
-    "large:gds:df64f6c34f54": round((38027008 + 512 + 72662272 + 19415808) * 4185964 / 4161643),
+    "large:gds:bcaade7fd42d": round((38027264 + 0 + 72673536 + 19556096) * 4185964 / 4161643),
     # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
     "large:gwr:25ea3b0dc7dd": 69719296 + 78336,
 }
