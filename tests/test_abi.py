@@ -155,3 +155,17 @@ def test_binding_rejects_buffers_of_the_wrong_type_or_extent():
         api.phase1(shape, k_idx, q_idx, k_val, q_val, g, {"A": torch.zeros(shape.N * shape.C * shape.C, dtype=torch.float64)}, ws)
     with pytest.raises(TypeError, match="k_idx: expected torch.int32"):
         api.forward_chunks(shape, k_idx.long(), q_idx, k_val, q_val, g, dv, torch.zeros(shape.P * shape.S * shape.hd), {}, ws)
+
+
+def test_shape_struct_is_built_once_and_matches_the_spec(lib):
+    """The binding hands the library one C struct per ShapeSpec (the spec is immutable): the same
+    object on every call, with the spec's fields, and the spec's equality and hashing untouched."""
+    spec = sdm.ShapeSpec(P=3, C=16, W=2, R=4, hd=8, steps=5, S=1000, valid_last=9, val_dtype="f32",
+                         bank_dtype="f32", dw_log_buckets=2, p1_warps=1)
+    cs = spec.c()
+    assert spec.c() is cs
+    assert (cs.P, cs.C, cs.W, cs.R, cs.hd, cs.valid_last, cs.steps, cs.S) == (3, 16, 2, 4, 8, 9, 5, 1000)
+    assert (cs.val_dtype, cs.dv_dtype, cs.bank_dtype) == (_abi.SDM_F32, _abi.SDM_BF16, _abi.SDM_F32)
+    twin = dataclasses.replace(spec)
+    assert twin == spec and hash(twin) == hash(spec) and twin.c() is not cs
+    assert lib.sdm_workspace_bytes(ctypes.byref(cs)) == lib.sdm_workspace_bytes(ctypes.byref(twin.c())) > 0
