@@ -87,7 +87,7 @@ constexpr uint32_t kRecTokMask = 0xFFFFu;
 // records go to the chunk's tail (after the buckets' records), where the long-group kernel sums
 // them (the DW walk's very FMA chain) before the DW, which takes the sum at the reference record.
 constexpr uint32_t kRecLong = 1u << 29;
-constexpr int kLongMin = 32;
+constexpr int kLongMin = 8;
 constexpr int kMaxLong = kMaxRow / kLongMin;   // long groups per chunk at most
 static_assert(kMaxRow + kMaxLong < (1 << 15), "a chunk's record places fit bits 16..30 of a write-row word");
 // the group's dense ordinal in its chunk (valid write groups before it in sorted order), carried by
