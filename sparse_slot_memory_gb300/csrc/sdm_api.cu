@@ -12,7 +12,12 @@ namespace {
 
  // DW work items (stream, slot bucket, column slice) aimed at per launch: ~3x the warps a GB300 holds.
 constexpr int64_t kDwTargetItems = 32768;
-constexpr int kMaxLogBuckets = 11;
+constexpr int kMaxLogBuckets = 11;   // the most a caller may ask for (sdm_shape.dw_log_buckets)
+// The most chosen by default. Each bucket costs Phase 1 8 bytes of shared memory per CTA: with 2^11
+// buckets a 512-thread CTA (C * (W + R) = 4096) needed 120 KB, one CTA per SM; with 2^10 it needs
+// 112 KB and two CTAs share an SM (zipf_c256: Phase 1 455 -> 326 us; its DW and that of
+// uniform_c128 are faster too with the fewer, fuller buckets).
+constexpr int kAutoLogBuckets = 10;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -69,11 +74,11 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
         g->bucket_bits = std::min(std::min(kb, kBucketBits), lg);
     }
     g->nsl = (s->hd + 127) / 128;
-    // DW buckets per stream: about kDwTargetItems items per launch, at most 2^11 and no more
-    // buckets than 2^key_bits
+    // DW buckets per stream: about kDwTargetItems items per launch, at most 2^kAutoLogBuckets and no
+    // more buckets than 2^key_bits
     int64_t want = kDwTargetItems / (static_cast<int64_t>(s->P) * g->nsl);
     int lb = 0;
-    while ((int64_t(1) << lb) < want && lb < kMaxLogBuckets && lb < kb) ++lb;
+    while ((int64_t(1) << lb) < want && lb < kAutoLogBuckets && lb < kb) ++lb;
     if (s->dw_log_buckets != 0) {
         if (s->dw_log_buckets < 1 || s->dw_log_buckets > kMaxLogBuckets || s->dw_log_buckets > kb) return SDM_ERR_SHAPE;
         lb = s->dw_log_buckets;
@@ -112,15 +117,16 @@ sdm_status geometry(const sdm_shape* s, Geometry* g) {
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
     g->sm_kslot = off;
     off += round_up(static_cast<size_t>(g->nk) * 4, 16);
+    // the DW bucket counters, and at least kHotExtra bytes: the dense pair path's vectors run on into
+    // this region, idle by then
     g->sm_bcnt = off;
-    off += round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16);
+    off += std::max<size_t>(round_up((2 * static_cast<size_t>(g->B) + 1) * 4, 16), kHotExtra);
     // The dense pair path keeps its groups' vectors (3 * C floats each, after kHotMax 16-byte
-    // descriptors) in the rex .. scratch region, free by then: the rex / cpe / write-row arrays, the
-    // bucket counters and kHotExtra bytes more. How many groups it takes must not depend on the
-    // launch geometry (the DW bucket count changes that region), or other geometries would round
-    // some A / QK cells differently: it is derived from the part every geometry has.
+    // descriptors) in the rex .. scratch region, free by then: the rex / cpe / write-row arrays and
+    // the bucket-counter region. How many groups it takes must not depend on the launch geometry (the
+    // DW bucket count changes that region), or other geometries would round some A / QK cells
+    // differently: it is derived from the part every geometry has (3 arrays + kHotExtra).
     g->sm_zero = off;
-    off += kHotExtra;
     {
         const size_t room = 3 * round_up(static_cast<size_t>(g->nk) * 4, 16) + kHotExtra - kHotMax * 16;
         g->hot_cap = static_cast<int>(std::min<size_t>(kHotMax, room / (12 * static_cast<size_t>(g->C))));
