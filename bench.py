@@ -47,18 +47,18 @@ METRIC_READ = "SDM forward read-side gather tokens/sec and achieved HBM GB/s vs 
 # line then reports null traffic.
 NCU_TRAFFIC = {
     # the forward (bench.py): the timed loop's Phase 1 (all outputs) and DW, one launch each at full size
-    "large:dw:620f34b88826": 1162350592 + 979562496,
-    "large:phase1:c65c2d4457e8": 52400896 + 723014912,
+    "large:dw:0a920160d349": 1162267136 + 980053248,
+    "large:phase1:1828b06a29da": 52794624 + 723314944,
     # the read gather (bench.py --read): one launch (one step) of the timed pass
-    "large:read:3cabff777f24": 34291712 + 2048,
+    "large:read:1d24d3bcefdd": 34294528 + 512,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:c24c52eb0c83": round((106358528 + 43712768) * 4186081 / 4161534),
+    "large:pa:9b6a1a6ba66d": round((106365440 + 43506688) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
-    "large:gds:bcaade7fd42d": round((38027264 + 0 + 72673536 + 19556096) * 4185964 / 4161643),
+    "large:gds:3eee62049e95": round((38027264 + 0 + 72658432 + 19464448) * 4185964 / 4161643),
     # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
-    "large:gwr:25ea3b0dc7dd": 69719296 + 78336,
+    "large:gwr:25443e716394": 69721600 + 67840,
 }
 
 
