@@ -47,10 +47,10 @@ METRIC_READ = "SDM forward read-side gather tokens/sec and achieved HBM GB/s vs 
 # line then reports null traffic.
 NCU_TRAFFIC = {
     # the forward (bench.py): the timed loop's Phase 1 (all outputs) and DW, one launch each at full size
-    "large:dw:0a920160d349": 1162267136 + 980053248,
+    "large:dw:2901ae5e38ba": 1162311168 + 979830784,
     "large:phase1:1828b06a29da": 52794624 + 723314944,
     # the read gather (bench.py --read): one launch (one step) of the timed pass
-    "large:read:1d24d3bcefdd": 34294528 + 512,
+    "large:read:851079abb9ec": 34298368 + 4864,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
     "large:pa:9b6a1a6ba66d": round((106365440 + 43506688) * 4186081 / 4161534),

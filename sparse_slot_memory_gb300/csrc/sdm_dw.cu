@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kDwThreads) long_kernel(const LongArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const DvT* const dv = static_cast<const DvT*>(a.dv);
     const uint32_t hdu = static_cast<uint32_t>(a.hd);
-    // a block per chunk, a grid of at most two blocks per SM looping over the chunks (on uniform
+    // a block per chunk, a grid of at most four blocks per SM looping over the chunks (on uniform
     // slots nothing is to be done: the kernel is only its launch)
     for (int64_t cb = blockIdx.x; cb < a.nchunks; cb += gridDim.x) {
         const int64_t c = a.c0 + cb;
@@ -316,7 +316,7 @@ cudaError_t launch_long(const LongArgs& a, int dv_bf16, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(a.nchunks < 2 * static_cast<int64_t>(sms) ? a.nchunks : 2 * static_cast<int64_t>(sms)));
+    const dim3 grid(static_cast<unsigned>(a.nchunks < 4 * static_cast<int64_t>(sms) ? a.nchunks : 4 * static_cast<int64_t>(sms)));
     return dv_bf16 ? launch_dependent(long_kernel<__nv_bfloat16>, grid, dim3(kDwThreads), 0, stream, a)
                    : launch_dependent(long_kernel<float>, grid, dim3(kDwThreads), 0, stream, a);
 }
