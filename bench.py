@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "large:read:851079abb9ec": 34298368 + 4864,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:9b6a1a6ba66d": round((106365440 + 43506688) * 4186081 / 4161534),
+    "large:pa:7eedfe0b88a0": round((106385408 + 43750656) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
     "large:gds:3eee62049e95": round((38027264 + 0 + 72658432 + 19464448) * 4185964 / 4161643),

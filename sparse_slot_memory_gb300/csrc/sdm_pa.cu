@@ -160,8 +160,8 @@ __device__ __forceinline__ void walk_wait(int pend) {
 // shared loads then issue together (a hot group's walk runs on one warp, bound by its own
 // dependency path: this made the skewed Phase A 27 % faster).
 template <int OFF>
-__device__ __forceinline__ void walk_sub(const Member& m, uint32_t okm, int g, const float (&sn)[4], float (&acc)[4],
-                                         float (&v)[16], int lane, const float4* buf) {
+__device__ __forceinline__ void walk_sub(const Member& m, int g, const float (&sn)[4], float (&acc)[4], float (&v)[16],
+                                         int lane, const float4* buf) {
     const int slot = g % kWalkDepth;
 #pragma unroll
     for (int u = 0; u < kWalkSub; ++u) {
@@ -212,11 +212,11 @@ __device__ __forceinline__ float window_terms(const Member& m, const Member& nm,
         float v[16];
         top_up(g0 + 2 * h);
         walk_wait(issued - 1 - (g0 + 2 * h));
-        walk_sub<0>(m, okm, g0 + 2 * h, sn, acc, v, lane, buf);
+        walk_sub<0>(m, g0 + 2 * h, sn, acc, v, lane, buf);
         if (2 * h + 1 < nsb) {
             top_up(g0 + 2 * h + 1);
             walk_wait(issued - 1 - (g0 + 2 * h + 1));
-            walk_sub<kWalkSub>(m, okm, g0 + 2 * h + 1, sn, acc, v, lane, buf);
+            walk_sub<kWalkSub>(m, g0 + 2 * h + 1, sn, acc, v, lane, buf);
         } else {
 #pragma unroll
             for (int u = 0; u < kWalkSub; ++u) v[kWalkSub + u] = 0.f;
