@@ -169,3 +169,14 @@ def test_shape_struct_is_built_once_and_matches_the_spec(lib):
     twin = dataclasses.replace(spec)
     assert twin == spec and hash(twin) == hash(spec) and twin.c() is not cs
     assert lib.sdm_workspace_bytes(ctypes.byref(cs)) == lib.sdm_workspace_bytes(ctypes.byref(twin.c())) > 0
+
+
+def test_default_bucket_count_is_capped_at_two_to_the_ten(lib):
+    """With dw_log_buckets = 0 a stream gets about 32768 / P DW buckets, at most 2^10 (more would push a
+    512-thread Phase-1 block past two blocks per SM): the default's workspace equals the explicit 2^10
+    one for P = 8 (which would want 2^12) and the explicit 2^9 one for P = 64."""
+    def ws(P, k):
+        spec = sdm.ShapeSpec(P=P, C=256, W=8, R=8, hd=128, steps=4, S=1 << 16, valid_last=256, dw_log_buckets=k)
+        return lib.sdm_workspace_bytes(ctypes.byref(spec.c()))
+    assert ws(8, 0) == ws(8, 10) != ws(8, 11)
+    assert ws(64, 0) == ws(64, 9) != ws(64, 10)
