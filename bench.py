@@ -47,18 +47,18 @@ METRIC_READ = "SDM forward read-side gather tokens/sec and achieved HBM GB/s vs 
 # line then reports null traffic.
 NCU_TRAFFIC = {
     # the forward (bench.py): the timed loop's Phase 1 (all outputs) and DW, one launch each at full size
-    "large:dw:2901ae5e38ba": 1162311168 + 979830784,
-    "large:phase1:1828b06a29da": 52794624 + 723314944,
+    "large:dw:ef4ffb8f7982": 1162345728 + 979819008,
+    "large:phase1:4c17089261ec": 52839680 + 723335680,
     # the read gather (bench.py --read): one launch (one step) of the timed pass
-    "large:read:851079abb9ec": 34298368 + 4864,
+    "large:read:4629bd9f0dbc": 34294528 + 6400,
     # Phase A (bench.py --pa): one launch captured on the large workload with S = 2^18 slots per stream
     # (same grid and group count per chunk), scaled by the groups ratio 4186081 / 4161534
-    "large:pa:7eedfe0b88a0": round((106385408 + 43750656) * 4186081 / 4161534),
+    "large:pa:25bcbddec3cb": round((106349824 + 43558912) * 4186081 / 4161534),
     # GDS (bench.py --gds): the dots and the scatter launch of one step (S = 2^18 capture, same grid),
     # scaled by the read-groups ratio 4185964 / 4161643
-    "large:gds:3eee62049e95": round((38027264 + 0 + 72658432 + 19464448) * 4185964 / 4161643),
+    "large:gds:4a65ad955f9a": round((38026752 + 72657920 + 19646208) * 4185964 / 4161643),
     # GWR (bench.py --gwr): one launch (S = 2^18 capture; the same write entries, rows per entry)
-    "large:gwr:25443e716394": 69721600 + 67840,
+    "large:gwr:8ac2b9913f79": 69718784 + 85760,
 }
 
 

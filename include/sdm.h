@@ -88,7 +88,8 @@ typedef struct {
      * the input), only how the work is split:
      *   dw_log_buckets 1..11 (<= ceil(log2 S)): the DW walk's hashed slot buckets per stream, 2^k
      *                  (changes sdm_workspace_bytes and Phase 1's shared memory per block: 8 bytes a
-     *                  bucket); 0 = about 32768 DW work items per launch, at most 2^10 buckets;
+     *                  bucket); 0 = about 32768 / ceil(hd / 128) DW work items per launch, at most 2^10
+     *                  buckets;
      *   p1_warps       the automatic count .. 32: warps of a Phase-1 block (extra warps hold
      *                  padding entries; more shared memory per block). */
     int32_t dw_log_buckets;
